@@ -1,0 +1,107 @@
+"""CPU oracle for CSR SpMM (C = alpha * A * B + beta * C0), fp64 accumulation.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` use it; the product path never does.  The
+arithmetic lives in ``spmm_oracle.c`` (plain C, compiled here with gcc, with
+floating-point contraction off so results are identical on every host); this
+module only builds it and marshals numpy arrays into it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "spmm_oracle.c")
+_LIB_DIR = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_LIB_DIR, "liboracle.so")
+
+OK, BAD_ARGS, BAD_CSR, NO_MEMORY = 0, -1, -2, -3
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into oracle/_build/liboracle.so (if stale) and return its path."""
+    os.makedirs(_LIB_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
+                        "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def load_library(path: str):
+    """ctypes handle on a build of spmm_oracle.c, with argument types declared."""
+    lib = ctypes.CDLL(path)
+    i64, p = ctypes.c_int64, ctypes.c_void_p
+    lib.oracle_spmm.restype = ctypes.c_int
+    lib.oracle_spmm.argtypes = [ctypes.c_int, i64, i64, i64, ctypes.c_double, p, p, p, p,
+                                i64, ctypes.c_double, p, i64, p, i64, p, p, i64]
+    lib.oracle_csr_check.restype = ctypes.c_int
+    lib.oracle_csr_check.argtypes = [i64, i64, i64, p, p]
+    return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        _lib = load_library(build())
+    return _lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def csr_check(m: int, k: int, row_ptr: np.ndarray, col_idx: np.ndarray) -> int:
+    """0 when (row_ptr, col_idx) is a valid m x k CSR structure, else BAD_CSR."""
+    row_ptr = np.ascontiguousarray(row_ptr, dtype=np.int32)
+    col_idx = np.ascontiguousarray(col_idx, dtype=np.int32)
+    nnz = int(row_ptr[m]) if row_ptr.size > m else -1
+    if nnz < 0 or col_idx.size < nnz:
+        return BAD_CSR
+    return _load().oracle_csr_check(m, k, nnz, _ptr(row_ptr), _ptr(col_idx))
+
+
+def spmm(m: int, k: int, n: int, alpha: float, row_ptr, col_idx, values, B, ldb: int,
+         beta: float, C0=None, ldc: int = 0, rows: Optional[np.ndarray] = None, _lib=None):
+    """Evaluate alpha * A * B + beta * C0 in fp64 for all rows (or ``rows``).
+
+    ``values``, ``B`` and ``C0`` must share one dtype, float32 or float64;
+    B is addressed as B.flat[col * ldb + c] and C0 as C0.flat[i * ldc + c].
+    Returns ``(out, bound)``, both float64 of shape [len(rows) or m, n]:
+    the result and the error-bound scale |alpha| sum|a||b| + |beta||C0|.
+    ``_lib`` substitutes another build of ``spmm_oracle.c`` (the tests use it
+    to show that deliberately broken copies fail the pins).
+    """
+    values = np.ascontiguousarray(values)
+    dt = values.dtype
+    if dt not in (np.float32, np.float64):
+        raise TypeError("values must be float32 or float64")
+    B = np.ascontiguousarray(B, dtype=dt)
+    C0 = None if C0 is None else np.ascontiguousarray(C0, dtype=dt)
+    row_ptr = np.ascontiguousarray(row_ptr, dtype=np.int32)
+    col_idx = np.ascontiguousarray(col_idx, dtype=np.int32)
+    rsel = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    nrows = m if rsel is None else int(rsel.size)
+    out = np.zeros((nrows, n), dtype=np.float64)
+    bound = np.zeros((nrows, n), dtype=np.float64)
+    lib = _load() if _lib is None else _lib
+    rc = lib.oracle_spmm(dt.itemsize, m, k, n, float(alpha), _ptr(row_ptr), _ptr(col_idx),
+                         _ptr(values), _ptr(B), ldb, float(beta), _ptr(C0), ldc,
+                         _ptr(rsel), nrows, _ptr(out), _ptr(bound), n)
+    if rc != OK:
+        raise ValueError(f"oracle_spmm rejected its inputs (status {rc})")
+    return out, bound
+
+
+def spmm_problem(p, rows: Optional[np.ndarray] = None):
+    """Oracle on a :class:`synth.Problem`."""
+    return spmm(p.m, p.k, p.n, p.alpha, p.row_ptr, p.col_idx, p.values, p.B, p.ldb,
+                p.beta, p.C0, p.ldc, rows)

@@ -1,0 +1,142 @@
+/*
+ * CPU oracle for CSR SpMM:  C = alpha * A * B + beta * C0.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may include, link or
+ * call this file: it is used by the tests, by the smoke check and by the
+ * benchmark's CPU-baseline leg, and by nothing else.  It shares no code,
+ * header or constant with the CUDA library.
+ *
+ * What it computes (oxicuda-sparse, ops/spmm.rs):
+ *   - module doc and `spmm` doc comment: C = alpha * A * B + beta * C, A an
+ *     m x k CSR matrix (row_ptr, col_idx, values), B a dense k x n matrix and
+ *     C a dense m x n matrix, both row-major with leading dimensions;
+ *   - device-test oracle `cpu_spmm`: per row, one accumulator per output
+ *     column, summed over the row's stored entries in CSR order in f64, then
+ *     alpha * acc + beta * C0;
+ *   - CPU test reference `cpu_csr_spmm`: B addressed as B[col * ldb + c].
+ *
+ * Readings where the page is silent or departs from the arithmetic
+ * (the conventions of dense BLAS):
+ *   - beta == 0: C0 is not read (NaN/Inf in C0 do not propagate);
+ *   - alpha == 0: A and B are not read; the result is beta * C0 (+0 if beta == 0);
+ *   - k == 0 or an empty row: the accumulator stays +0, so the row is
+ *     alpha * 0 + beta * C0;
+ *   - duplicate column indices each contribute; explicit zeros multiply.
+ *
+ * Products of two binary32 numbers are exact in binary64, so for f32 inputs
+ * the only rounding is in the f64 running sums.
+ *
+ * Every call also returns, per output, the error-bound scale
+ *   bound = |alpha| * sum_p |a_p| * |b_{col_p, c}| + |beta| * |C0|
+ * (the second term only when beta != 0), used by the parity tests.
+ *
+ * Plain loops, no blocking or reordering; single-threaded.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#define ORACLE_OK 0
+#define ORACLE_BAD_ARGS -1
+#define ORACLE_BAD_CSR -2
+#define ORACLE_NO_MEMORY -3
+
+/* Element i of an array of binary32 (esize 4) or binary64 (esize 8), widened. */
+static double load(const void *p, int64_t i, int esize)
+{
+    if (esize == 4) return (double)((const float *)p)[i];
+    return ((const double *)p)[i];
+}
+
+/* CSR structure check: row_ptr[0] == 0, non-decreasing, row_ptr[m] == nnz,
+ * 0 <= col_idx[p] < k for every stored entry. */
+int oracle_csr_check(int64_t m, int64_t k, int64_t nnz, const int32_t *row_ptr,
+                     const int32_t *col_idx)
+{
+    if (m < 0 || k < 0 || nnz < 0 || !row_ptr) return ORACLE_BAD_ARGS;
+    if (row_ptr[0] != 0 || (int64_t)row_ptr[m] != nnz) return ORACLE_BAD_CSR;
+    for (int64_t i = 0; i < m; ++i)
+        if (row_ptr[i + 1] < row_ptr[i]) return ORACLE_BAD_CSR;
+    for (int64_t p = 0; p < nnz; ++p)
+        if (col_idx[p] < 0 || (int64_t)col_idx[p] >= k) return ORACLE_BAD_CSR;
+    return ORACLE_OK;
+}
+
+/*
+ * out[r * ldo + c] = alpha * sum_{p in row i} values[p] * B[col_idx[p] * ldb + c]
+ *                    + beta * C0[i * ldc + c]
+ * for the rows i = rows[r], r < nrows (all rows 0..m-1 in order when rows is
+ * NULL) and every column c < n.  bound (may be NULL) gets the error-bound
+ * scale described above, with the same layout.
+ * esize is the element size of values, B and C0: 4 (binary32) or 8 (binary64).
+ */
+int oracle_spmm(int esize, int64_t m, int64_t k, int64_t n, double alpha,
+                const int32_t *row_ptr, const int32_t *col_idx, const void *values,
+                const void *B, int64_t ldb, double beta, const void *C0, int64_t ldc,
+                const int64_t *rows, int64_t nrows, double *out, double *bound, int64_t ldo)
+{
+    if ((esize != 4 && esize != 8) || m < 0 || k < 0 || n < 0 || ldo < n) return ORACLE_BAD_ARGS;
+    if (!rows) nrows = m;
+    if (nrows <= 0 || n == 0) return ORACLE_OK;
+    if (beta != 0.0 && (!C0 || ldc < n)) return ORACLE_BAD_ARGS;
+    if (alpha != 0.0 && (!row_ptr || ldb < n)) return ORACLE_BAD_ARGS;
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t i = rows ? rows[r] : r;
+        if (i < 0 || i >= m) return ORACLE_BAD_ARGS;
+        if (alpha == 0.0) continue;
+        if (row_ptr[i + 1] < row_ptr[i]) return ORACLE_BAD_CSR;
+        for (int64_t p = row_ptr[i]; p < (int64_t)row_ptr[i + 1]; ++p)
+            if (col_idx[p] < 0 || (int64_t)col_idx[p] >= k) return ORACLE_BAD_CSR;
+    }
+
+    double *acc = (double *)malloc(sizeof(double) * (size_t)n);
+    double *absacc = (double *)malloc(sizeof(double) * (size_t)n);
+    if (!acc || !absacc) {
+        free(acc);
+        free(absacc);
+        return ORACLE_NO_MEMORY;
+    }
+
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t i = rows ? rows[r] : r;
+        double *o = out + r * ldo;
+        double *bd = bound ? bound + r * ldo : NULL;
+
+        if (alpha == 0.0) {                      /* A and B not referenced */
+            for (int64_t c = 0; c < n; ++c) {
+                double c0 = (beta == 0.0) ? 0.0 : load(C0, i * ldc + c, esize);
+                o[c] = (beta == 0.0) ? 0.0 : beta * c0;
+                if (bd) bd[c] = fabs(beta) * fabs(c0);
+            }
+            continue;
+        }
+
+        for (int64_t c = 0; c < n; ++c) {
+            acc[c] = 0.0;
+            absacc[c] = 0.0;
+        }
+        for (int64_t p = row_ptr[i]; p < (int64_t)row_ptr[i + 1]; ++p) {
+            int64_t j = col_idx[p];
+            double a = load(values, p, esize);
+            for (int64_t c = 0; c < n; ++c) {
+                double b = load(B, j * ldb + c, esize);
+                acc[c] += a * b;
+                absacc[c] += fabs(a) * fabs(b);
+            }
+        }
+        for (int64_t c = 0; c < n; ++c) {
+            double v = alpha * acc[c];
+            double e = fabs(alpha) * absacc[c];
+            if (beta != 0.0) {                   /* C0 read only when beta != 0 */
+                double c0 = load(C0, i * ldc + c, esize);
+                v += beta * c0;
+                e += fabs(beta) * fabs(c0);
+            }
+            o[c] = v;
+            if (bd) bd[c] = e;
+        }
+    }
+    free(acc);
+    free(absacc);
+    return ORACLE_OK;
+}

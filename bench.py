@@ -1,0 +1,414 @@
+#!/usr/bin/env python3
+"""CSR SpMM benchmark on GB300: GFLOP/s (2 * nnz * n) and achieved HBM GB/s.
+
+One step = one C = alpha * A * B + beta * C product through the C ABI
+(pre-pass, per-bin kernels, fixup) on one synthetic workload with every input
+resident in HBM.  The L2 is flushed (a 2x-L2 buffer is written) before every
+timed step so that B, A and C start in HBM, as the byte model assumes.
+Each step is timed with CUDA events on the launching stream; ``value`` is
+GFLOP/s over the K timed steps.  Under torchrun every rank runs its own
+replica of the workload (the product does not shard here), timing is the max
+over ranks and ``value`` counts the work of all ranks.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference      # the CPU oracle on a bounded sample
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "SpMM GFLOP/s (2·nnz·N) and achieved HBM GB/s vs ~8 TB/s peak, 1×GB300"
+DEFAULT_WORKLOAD = "seacells_knn"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest():
+    csrc = os.path.join(ROOT, "csr_spmm_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch of the rows kernel from the committed ncu summary,
+    or None if absent or taken on kernel sources other than the current ones."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[workload]
+        if e.get("source_sha256") != source_digest():
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        rows = [ln.strip().split(", ") for ln in self.out.read().splitlines() if ln.strip()]
+        os.unlink(self.out.name)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax = float(r[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def rows_kernel_bytes(p, prof):
+    """Algorithmic bytes of the short/medium-rows kernel for one launch: its rows'
+    row_ptr entries and C row(s), its entries' (col_idx, value), and its share
+    (by entries) of reading B once."""
+    es = p.values.dtype.itemsize
+    rows = prof["rows_short"] + prof["rows_medium"]
+    entries = p.nnz - prof["long_nnz"]
+    share = entries / p.nnz if p.nnz else 1.0
+    c_bytes = es * p.n * rows * (2 if p.beta != 0.0 else 1)
+    return 4 * (rows + 1) + (4 + es) * entries + share * es * p.k * p.n + c_bytes
+
+
+def oracle_baseline(p, target_s=10.0, max_passes=5):
+    """Time the CPU oracle (as it stands, single-threaded) on the full workload,
+    repeating whole passes until ~target_s of work or max_passes; for workloads
+    whose single pass would exceed the budget, a strided row sample instead."""
+    import numpy as np
+
+    import oracle
+    t0 = time.perf_counter()
+    probe = np.arange(0, p.m, max(1, p.m // 2000), dtype=np.int64)
+    oracle.spmm_problem(p, probe)
+    t_probe = time.perf_counter() - t0
+    nnz_probe = int(np.diff(p.row_ptr)[probe].sum()) + len(probe)
+    est_full = t_probe * (p.nnz + p.m) / max(1, nnz_probe)
+    if est_full <= target_s:
+        rows, desc = None, "all rows"
+        flops_pass = p.flops()
+    else:
+        stride = int(np.ceil(est_full / target_s))
+        rows = np.arange(0, p.m, stride, dtype=np.int64)
+        desc = f"every {stride}th row ({len(rows)} rows)"
+        flops_pass = 2 * int(np.diff(p.row_ptr)[rows].sum()) * p.n
+    passes, elapsed = 0, 0.0
+    while passes < max_passes and (passes == 0 or elapsed < target_s):
+        t0 = time.perf_counter()
+        oracle.spmm_problem(p, rows)
+        elapsed += time.perf_counter() - t0
+        passes += 1
+    gflops = flops_pass * passes / elapsed / 1e9
+    return {"value": round(gflops, 4), "unit": "GFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"{p.name}: {desc} x {passes} pass(es), {elapsed:.1f} s, fp64 accumulation"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from synth import workloads
+    p = workloads.WORKLOADS[args.workload]()
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    lens = np.diff(p.row_ptr)
+    # each step: a bounded strided row sample of the workload (~0.5 s of oracle work)
+    probe = np.arange(0, p.m, max(1, p.m // 1000), dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.spmm_problem(p, probe)
+    t_probe = time.perf_counter() - t0
+    est_full = t_probe * (p.nnz + p.m) / max(1, int(lens[probe].sum()) + len(probe))
+    stride = max(1, int(np.ceil(est_full / 0.5)))
+    rows = np.arange(0, p.m, stride, dtype=np.int64)
+    flops = 2 * int(lens[rows].sum()) * p.n
+    for _ in range(args.warmup):
+        oracle.spmm_problem(p, rows)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.spmm_problem(p, rows)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = flops * args.steps / total / 1e9
+    sample = f"{p.name}: every {stride}th row ({len(rows)} rows) per step, fp64 accumulation"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": p.name, "m": p.m, "k": p.k, "n": p.n, "nnz": p.nnz,
+                   "sampled_rows_per_step": int(len(rows))},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GFLOP/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import csr_spmm_gb300 as cs
+    from csr_spmm_gb300 import build as csb
+    from synth import workloads
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    if rank == 0:
+        csb.build()
+    if pg:
+        pg.barrier()
+    cs.library()
+
+    p = workloads.WORKLOADS[args.workload]()
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    rp, ci, va, B = t(p.row_ptr), t(p.col_idx), t(p.values), t(p.B)
+    C0 = t(p.C0) if p.C0 is not None else None
+    C = torch.empty((p.m, p.ldc), dtype=va.dtype, device=dev)
+    if C0 is not None:
+        C.copy_(C0)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    h = cs.Handle(local)
+    h.reserve(p.m, p.n, p.values.dtype.itemsize)
+    cs.spmm_set_profiling(h.ptr, True)
+    fn = cs.spmm_csr_f32 if p.values.dtype == np.float32 else cs.spmm_csr_f64
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+
+    def call(Cbuf):
+        fn(h.ptr, p.alpha, rp.data_ptr(), ci.data_ptr(), va.data_ptr(), p.m, p.k, B.data_ptr(),
+           p.ldb, p.n, p.beta, Cbuf.data_ptr(), p.ldc, sptr)
+
+    for _ in range(max(3, args.warmup)):
+        if C0 is not None:
+            C.copy_(C0)
+        flush.zero_()
+        call(C)
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, device-timed, barrier + sync on both sides ----
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    profs = []
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.25)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        if C0 is not None:
+            C.copy_(C0)
+        flush.zero_()
+        ev[i][0].record(stream)
+        call(C)
+        ev[i][1].record(stream)
+        ev[i][1].synchronize()
+        profs.append(cs.spmm_get_profile(h.ptr))
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(step_ms)
+    if pg:
+        tt = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    flops = p.flops()
+    value = flops * args.steps * world / (total_ms / 1e3) / 1e9
+
+    # ---- roofline of the dominant kernel (short/medium rows) ----
+    peak, peak_kind = measured_hbm_peak()
+    rows_ms = statistics.mean(pr["rows_ms"] for pr in profs)
+    kbytes = rows_kernel_bytes(p, profs[-1])
+    achieved = kbytes / (rows_ms / 1e3) / 1e9
+    traffic = recorded_traffic(p.name)
+    launches = int(sum(pr["launches"] for pr in profs))
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+        h_rp, h_ci, h_va, h_B = pin(p.row_ptr), pin(p.col_idx), pin(p.values), pin(p.B)
+        h_C0 = pin(p.C0) if p.C0 is not None else None
+        h_C = torch.empty((p.m, p.ldc), dtype=va.dtype).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in (h_rp, h_ci, h_va, h_B) if x is not None)
+        h2d += 0 if h_C0 is None else h_C0.numel() * h_C0.element_size()
+        d2h = h_C.numel() * h_C.element_size()
+
+        def e2e_step():
+            rp.copy_(h_rp, non_blocking=True)
+            ci.copy_(h_ci, non_blocking=True)
+            va.copy_(h_va, non_blocking=True)
+            B.copy_(h_B, non_blocking=True)
+            if h_C0 is not None:
+                C.copy_(h_C0, non_blocking=True)
+            call(C)
+            h_C.copy_(C, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e_steps = max(3, min(args.steps, 50))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if pg:
+            pg.barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1)
+        if pg:
+            tt = torch.tensor([e_ms], device=dev, dtype=torch.float64)
+            pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+            e_ms = float(tt.item())
+        e2e = {"value": round(flops * e_steps * world / (e_ms / 1e3) / 1e9, 3), "unit": "GFLOP/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": round(e_ms / e_steps, 4), "steps": e_steps}
+    h.close()
+
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return 0
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_baseline(p)
+    alg = p.algorithmic_bytes()
+    mean_ms = total_ms / args.steps
+    dtype = {"float32": "f32", "float64": "f64"}[str(p.values.dtype)]
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "GFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
+        "data": "synthetic",
+        "config": {"workload": p.name, "m": p.m, "k": p.k, "n": p.n, "nnz": p.nnz,
+                   "alpha": p.alpha, "beta": p.beta, "algorithmic_bytes": alg,
+                   "l2_flush": "2x L2 buffer written before every timed step",
+                   "parallelism": f"replicas x{world}",
+                   "hbm_gbs_whole_call": round(alg / (mean_ms / 1e3) / 1e9, 1),
+                   "plan": {k: profs[-1][k] for k in ("panels", "panel_cols", "vec_elems",
+                                                       "group_lanes", "slots", "short_max",
+                                                       "long_min", "rows_short", "rows_medium",
+                                                       "rows_long", "long_nnz")},
+                   "stage_ms": {k: round(statistics.mean(pr[k] for pr in profs), 5)
+                                for k in ("prepass_ms", "rows_ms", "long_ms", "fixup_ms")}},
+        "roofline": {"bound": "hbm", "kernel": "rows_kernel", "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": int(kbytes)},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

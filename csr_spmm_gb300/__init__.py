@@ -1,0 +1,99 @@
+"""GB300-native CSR SpMM: C = alpha * A * B + beta * C on one sm_103a GPU.
+
+The product runs in hand-written CUDA kernels behind the C ABI of
+``include/csr_spmm.h`` (library ``csr_spmm_gb300/lib/libcsrspmm.so``).  This
+package is the Python face of that ABI:
+
+* :mod:`csr_spmm_gb300._lib` -- the C entry points under their C names
+  (``spmm_create``, ``spmm_csr_f32``, ...), pointers as integers;
+* :class:`Handle` and :func:`spmm` -- the same call taking torch CUDA tensors
+  (PyTorch supplies device memory and the current stream only).
+
+There is no CPU path: without the built library every call raises.
+"""
+from __future__ import annotations
+
+from ._lib import (EXPORTED, SPMM_ERR_ALLOC, SPMM_ERR_CUDA, SPMM_ERR_DIMENSION_MISMATCH,
+                   SPMM_ERR_INVALID_ARGUMENT, SPMM_ERR_INVALID_CSR, SPMM_ERR_NULL_POINTER,
+                   SPMM_ERR_UNSUPPORTED_DEVICE, SPMM_OK, SpmmError, library, spmm_create,
+                   spmm_csr_check, spmm_csr_f32, spmm_csr_f64, spmm_destroy, spmm_get_profile,
+                   spmm_reserve, spmm_set_profiling, status_string)
+
+__all__ = ["Handle", "spmm", "csr_check", "SpmmError", "library", "spmm_create", "spmm_destroy",
+           "spmm_reserve", "spmm_csr_f32", "spmm_csr_f64", "spmm_csr_check", "status_string",
+           "spmm_set_profiling", "spmm_get_profile", "EXPORTED"]
+
+
+class Handle:
+    """Owns one ``spmm_handle_t`` (scratch for row bins and long-row partials)."""
+
+    def __init__(self, device: int | None = None):
+        import torch
+        self.device = torch.cuda.current_device() if device is None else int(device)
+        self.ptr = spmm_create(self.device)
+
+    def reserve(self, m: int, n: int, elem_size: int) -> None:
+        spmm_reserve(self.ptr, m, n, elem_size)
+
+    def close(self) -> None:
+        if self.ptr:
+            spmm_destroy(self.ptr)
+            self.ptr = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _ptr(t):
+    return 0 if t is None else t.data_ptr()
+
+
+def spmm(handle: Handle, alpha: float, row_ptr, col_idx, values, k: int, B, beta: float, C,
+         stream=None) -> None:
+    """C <- alpha * A * B + beta * C, A given by CSR tensors (int32, int32, float32/64).
+
+    ``B`` is a [k, n] CUDA tensor and ``C`` an [m, n] CUDA tensor, each with
+    unit column stride (any row stride: the leading dimension).  Enqueued on
+    ``stream`` (default: torch's current stream); returns without waiting.
+    """
+    import torch
+    m = int(row_ptr.numel()) - 1
+    n = int(C.shape[1])
+    if C.dim() != 2 or B.dim() != 2 or C.stride(1) != 1 or B.stride(1) != 1:
+        raise ValueError("B and C must be 2-D with unit column stride")
+    if B.shape[0] != k or B.shape[1] != n or C.shape[0] != m:
+        raise ValueError(f"shape mismatch: A {m}x{k}, B {tuple(B.shape)}, C {tuple(C.shape)}")
+    if row_ptr.dtype != torch.int32 or col_idx.dtype != torch.int32:
+        raise TypeError("row_ptr and col_idx must be int32")
+    if not (values.dtype == B.dtype == C.dtype):
+        raise TypeError("values, B and C must share one dtype")
+    st = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+    ldb = B.stride(0) if B.shape[0] > 1 else max(1, n)
+    ldc = C.stride(0) if C.shape[0] > 1 else max(1, n)
+    args = (handle.ptr, alpha, _ptr(row_ptr), _ptr(col_idx), _ptr(values), m, k, _ptr(B), ldb, n,
+            beta, _ptr(C), ldc, st)
+    if values.dtype == torch.float32:
+        spmm_csr_f32(*args)
+    elif values.dtype == torch.float64:
+        spmm_csr_f64(*args)
+    else:
+        raise TypeError("values must be float32 or float64")
+
+
+def csr_check(handle: Handle, row_ptr, col_idx, k: int, stream=None) -> int:
+    """Device-side CSR structure check; returns the status bit mask (0 = valid)."""
+    import torch
+    m = int(row_ptr.numel()) - 1
+    nnz = int(col_idx.numel())
+    st = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+    _, mask = spmm_csr_check(handle.ptr, _ptr(row_ptr), _ptr(col_idx), m, k, nnz, st)
+    return mask

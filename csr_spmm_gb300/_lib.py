@@ -1,0 +1,148 @@
+"""ctypes binding of the C ABI declared in include/csr_spmm.h.
+
+Argument marshalling only: every step of the product runs in the CUDA
+library.  Functions keep the C names; pointers are passed as Python ints
+(device addresses), streams as ints (``torch.cuda.Stream.cuda_stream``) or 0.
+If the library is missing, importing the functions raises at once: there is
+no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "lib", "libcsrspmm.so")
+
+SPMM_OK = 0
+SPMM_ERR_INVALID_ARGUMENT = 1
+SPMM_ERR_DIMENSION_MISMATCH = 2
+SPMM_ERR_NULL_POINTER = 3
+SPMM_ERR_UNSUPPORTED_DEVICE = 4
+SPMM_ERR_ALLOC = 5
+SPMM_ERR_CUDA = 6
+SPMM_ERR_INVALID_CSR = 7
+
+# every symbol include/csr_spmm.h declares
+EXPORTED = ("spmm_create", "spmm_destroy", "spmm_reserve", "spmm_csr_f32", "spmm_csr_f64",
+            "spmm_csr_check", "spmm_set_profiling", "spmm_get_profile", "spmm_status_string")
+
+
+class SpmmProfile(ctypes.Structure):
+    """Mirror of spmm_profile_t."""
+    _fields_ = [("prepass_ms", ctypes.c_float), ("rows_ms", ctypes.c_float),
+                ("long_ms", ctypes.c_float), ("fixup_ms", ctypes.c_float),
+                ("total_ms", ctypes.c_float), ("launches", ctypes.c_int32),
+                ("rows_short", ctypes.c_int32), ("rows_medium", ctypes.c_int32),
+                ("rows_long", ctypes.c_int32), ("long_nnz", ctypes.c_int32),
+                ("panels", ctypes.c_int32), ("panel_cols", ctypes.c_int32),
+                ("vec_elems", ctypes.c_int32), ("group_lanes", ctypes.c_int32),
+                ("slots", ctypes.c_int32), ("short_max", ctypes.c_int32),
+                ("long_min", ctypes.c_int32)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class SpmmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+_lib = None
+
+
+def library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the shared library (once) and declare the C signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(
+            f"CUDA library not built: {path} is missing. Run `python -m csr_spmm_gb300.build` "
+            "(or __graft_entry__.build()); there is no CPU fallback.")
+    lib = ctypes.CDLL(path)
+    i64, i32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+    st = ctypes.c_int
+    lib.spmm_create.argtypes = [ctypes.POINTER(vp), ctypes.c_int]
+    lib.spmm_create.restype = st
+    lib.spmm_destroy.argtypes = [vp]
+    lib.spmm_destroy.restype = st
+    lib.spmm_reserve.argtypes = [vp, i64, i64, ctypes.c_int]
+    lib.spmm_reserve.restype = st
+    lib.spmm_csr_f32.argtypes = [vp, ctypes.c_float, vp, vp, vp, i64, i64, vp, i64, i64,
+                                 ctypes.c_float, vp, i64, vp]
+    lib.spmm_csr_f32.restype = st
+    lib.spmm_csr_f64.argtypes = [vp, ctypes.c_double, vp, vp, vp, i64, i64, vp, i64, i64,
+                                 ctypes.c_double, vp, i64, vp]
+    lib.spmm_csr_f64.restype = st
+    lib.spmm_csr_check.argtypes = [vp, vp, vp, i64, i64, i64, vp, ctypes.POINTER(i32)]
+    lib.spmm_csr_check.restype = st
+    lib.spmm_set_profiling.argtypes = [vp, ctypes.c_int]
+    lib.spmm_set_profiling.restype = st
+    lib.spmm_get_profile.argtypes = [vp, ctypes.POINTER(SpmmProfile)]
+    lib.spmm_get_profile.restype = st
+    lib.spmm_status_string.argtypes = [ctypes.c_int]
+    lib.spmm_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return library().spmm_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != SPMM_OK:
+        raise SpmmError(status, where)
+
+
+def spmm_create(device: int = 0) -> int:
+    h = ctypes.c_void_p()
+    _check(library().spmm_create(ctypes.byref(h), int(device)), "spmm_create")
+    return h.value
+
+
+def spmm_destroy(handle: int) -> None:
+    _check(library().spmm_destroy(handle), "spmm_destroy")
+
+
+def spmm_reserve(handle: int, m: int, n: int, elem_size: int) -> None:
+    _check(library().spmm_reserve(handle, m, n, elem_size), "spmm_reserve")
+
+
+def spmm_csr_f32(handle, alpha, row_ptr, col_idx, values, m, k, B, ldb, n, beta, C, ldc,
+                 stream=0, check=True) -> int:
+    s = library().spmm_csr_f32(handle, float(alpha), row_ptr, col_idx, values, m, k, B, ldb, n,
+                               float(beta), C, ldc, stream or None)
+    if check:
+        _check(s, "spmm_csr_f32")
+    return s
+
+
+def spmm_csr_f64(handle, alpha, row_ptr, col_idx, values, m, k, B, ldb, n, beta, C, ldc,
+                 stream=0, check=True) -> int:
+    s = library().spmm_csr_f64(handle, float(alpha), row_ptr, col_idx, values, m, k, B, ldb, n,
+                               float(beta), C, ldc, stream or None)
+    if check:
+        _check(s, "spmm_csr_f64")
+    return s
+
+
+def spmm_csr_check(handle, row_ptr, col_idx, m, k, nnz, stream=0):
+    """Returns (status, mask); mask 0 means the CSR structure is valid."""
+    mask = ctypes.c_int32(-1)
+    s = library().spmm_csr_check(handle, row_ptr, col_idx, m, k, nnz, stream or None,
+                                 ctypes.byref(mask))
+    return s, mask.value
+
+
+def spmm_set_profiling(handle, enable: bool) -> None:
+    _check(library().spmm_set_profiling(handle, 1 if enable else 0), "spmm_set_profiling")
+
+
+def spmm_get_profile(handle) -> dict:
+    prof = SpmmProfile()
+    _check(library().spmm_get_profile(handle, ctypes.byref(prof)), "spmm_get_profile")
+    return prof.as_dict()

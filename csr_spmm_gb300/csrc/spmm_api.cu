@@ -1,0 +1,433 @@
+// Host driver behind the C ABI in include/csr_spmm.h: argument validation,
+// the handle and its scratch, the column-panel / geometry plan, and the
+// launch sequence
+//   pre-pass (row bins) -> short/medium rows -> long-row CTA split -> fixup.
+// No step synchronises the stream; no device value is read back.
+#include <algorithm>
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "csr_spmm.h"
+#include "spmm_internal.h"
+
+using namespace spmm;
+
+struct spmm_handle_s {
+    int device = 0;
+    int num_sms = 0;
+    int64_t l2_bytes = 0;
+    void* scratch = nullptr;
+    size_t scratch_bytes = 0;
+    int* check_status = nullptr;
+    // occupancy cache of the rows kernel, keyed by (element size, W, G, R)
+    struct OccEntry { int es, W, G, R, blocks; };
+    OccEntry occ[32];
+    int nocc = 0;
+    // profiling: events around the stages of the last profiled call
+    bool profiling = false;
+    bool have_profile = false;
+    cudaEvent_t ev[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+    spmm_profile_t prof{};
+    const int* prof_hdr = nullptr;     // device header of the last profiled call
+};
+
+namespace {
+
+// Fraction of L2 a B column panel may occupy; panels are only used when B
+// itself exceeds PANEL_TRIGGER of L2.
+constexpr double PANEL_FRACTION = 0.5;
+constexpr double PANEL_TRIGGER = 0.75;
+// Rows at least this long go to the CTA-split kernel.
+constexpr int LONG_MIN_ROW = 1024;
+// Long-row grid: CTAs per SM.
+constexpr int LONG_CTAS_PER_SM = 2;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline int next_pow2(int x) {
+    int p = 1;
+    while (p < x) p <<= 1;
+    return p;
+}
+
+struct ScratchLayout {
+    size_t hdr, tile_counts, tile_offsets, rowlist, long_pre, partials, total;
+};
+
+ScratchLayout layout_for(int64_t m, int64_t n, int es, int long_grid) {
+    ScratchLayout L{};
+    const int64_t tiles = (m + BIN_TILE - 1) / BIN_TILE;
+    size_t off = 0;
+    L.hdr = off;          off = align_up(off + sizeof(int) * HDR_WORDS, 256);
+    L.tile_counts = off;  off = align_up(off + sizeof(int) * 4 * (size_t)std::max<int64_t>(tiles, 1), 256);
+    L.tile_offsets = off; off = align_up(off + sizeof(int) * 4 * (size_t)std::max<int64_t>(tiles, 1), 256);
+    L.rowlist = off;      off = align_up(off + sizeof(int) * (size_t)std::max<int64_t>(m, 1), 256);
+    L.long_pre = off;     off = align_up(off + sizeof(int) * (size_t)(m + 1), 256);
+    L.partials = off;     off = align_up(off + (size_t)es * 2 * long_grid * (size_t)std::max<int64_t>(n, 1), 256);
+    L.total = off;
+    return L;
+}
+
+int long_grid_of(const spmm_handle_s* h) { return LONG_CTAS_PER_SM * h->num_sms; }
+
+spmm_status_t ensure_scratch(spmm_handle_s* h, size_t bytes) {
+    if (bytes <= h->scratch_bytes) return SPMM_OK;
+    if (h->scratch) {
+        cudaDeviceSynchronize();     // earlier calls may still use the old buffer
+        cudaFree(h->scratch);
+        h->scratch = nullptr;
+        h->scratch_bytes = 0;
+    }
+    const size_t want = align_up(bytes + bytes / 4, 1 << 20);
+    if (cudaMalloc(&h->scratch, want) != cudaSuccess) {
+        cudaGetLastError();
+        h->scratch = nullptr;
+        return SPMM_ERR_ALLOC;
+    }
+    h->scratch_bytes = want;
+    return SPMM_OK;
+}
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Plan {
+    Geometry geo;
+    int panel_cols;
+    int npanels;
+    int short_max;
+    int long_min;
+};
+
+template <typename T>
+Plan make_plan(const spmm_handle_s* h, int64_t k, int64_t n, const T* B, int64_t ldb, const T* C,
+               int64_t ldc) {
+    const int es = (int)sizeof(T);
+    const int WV = 16 / es;
+    const bool vec = aligned(B, 16) && aligned(C, 16) && ldb % WV == 0 && ldc % WV == 0;
+    Plan P{};
+    P.geo.W = vec ? WV : 1;
+    const int W = P.geo.W;
+
+    // column panels: keep the B panel being gathered resident in L2
+    int64_t panel = n;
+    const double bbytes = (double)k * (double)n * es;
+    if (h->l2_bytes > 0 && bbytes > PANEL_TRIGGER * (double)h->l2_bytes) {
+        const int64_t align = std::max<int64_t>(W, 128 / es);      // whole 128-byte lines
+        int64_t cols = (int64_t)(PANEL_FRACTION * (double)h->l2_bytes / ((double)k * es));
+        cols = cols / align * align;
+        if (cols < align) cols = std::max<int64_t>(W, align);
+        const int64_t np = (n + cols - 1) / cols;
+        panel = (n + np - 1) / np;
+        panel = (panel + W - 1) / W * W;
+    }
+    P.panel_cols = (int)std::min<int64_t>(panel, n);
+    P.npanels = (int)((n + P.panel_cols - 1) / P.panel_cols);
+
+    const int nvec = (P.panel_cols + W - 1) / W;
+    if (nvec <= 32) {
+        P.geo.G = next_pow2(nvec);
+        P.geo.R = 1;
+    } else {
+        P.geo.G = 32;
+        P.geo.R = nvec <= 64 ? 2 : 4;
+    }
+    // bin thresholds
+    const int bytes_per_entry = P.geo.R * W * es;
+    const int U = std::min(8, std::max(1, 128 / bytes_per_entry));
+    const int CH = std::max(P.geo.G, U);
+    P.long_min = LONG_MIN_ROW;
+    P.short_max = (P.geo.G == 32) ? P.long_min - 1 : std::min(P.long_min - 1, 2 * CH);
+    return P;
+}
+
+int rows_grid(spmm_handle_s* h, int es, const Geometry& g) {
+    for (int i = 0; i < h->nocc; ++i) {
+        const auto& e = h->occ[i];
+        if (e.es == es && e.W == g.W && e.G == g.G && e.R == g.R) return e.blocks * h->num_sms;
+    }
+    const int b = es == 4 ? rows_blocks_per_sm<float>(g) : rows_blocks_per_sm<double>(g);
+    if (h->nocc < 32) h->occ[h->nocc++] = {es, g.W, g.G, g.R, b};
+    return b * h->num_sms;
+}
+
+// Records event i of the profiled call (no-op when profiling is off).
+inline void mark(spmm_handle_s* h, int i, cudaStream_t st) {
+    if (h->profiling) cudaEventRecord(h->ev[i], st);
+}
+
+template <typename T>
+spmm_status_t spmm_csr_impl(spmm_handle_t h, T alpha, const int32_t* row_ptr,
+                            const int32_t* col_idx, const T* values, int64_t m, int64_t k,
+                            const T* B, int64_t ldb, int64_t n, T beta, T* C, int64_t ldc,
+                            void* stream) {
+    // ---- validation (oxicuda-sparse, ops/spmm.rs, `spmm`: dimension checks) ----
+    if (!h) return SPMM_ERR_INVALID_ARGUMENT;
+    if (m < 0 || k < 0 || n < 0) return SPMM_ERR_INVALID_ARGUMENT;
+    if (m > (int64_t)INT_MAX - BIN_TILE || k > (int64_t)INT_MAX || n > (int64_t)INT_MAX)
+        return SPMM_ERR_INVALID_ARGUMENT;
+    if (ldb < std::max<int64_t>(1, n) || ldc < std::max<int64_t>(1, n))
+        return SPMM_ERR_DIMENSION_MISMATCH;
+    if (m == 0 || n == 0) return SPMM_OK;             // nothing to compute (as on the page)
+    if (!C) return SPMM_ERR_NULL_POINTER;
+    const bool uses_a = alpha != T(0) && k > 0;
+    if (uses_a && (!row_ptr || !col_idx || !values || !B)) return SPMM_ERR_NULL_POINTER;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device) {
+        cudaGetLastError();
+        return SPMM_ERR_INVALID_ARGUMENT;
+    }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+    if (!uses_a) {
+        // alpha == 0 or k == 0: C = beta * C, A and B not read
+        const int grid = h->num_sms * 8;
+        if (h->profiling) {
+            h->prof = spmm_profile_t{};
+            h->prof.launches = 1;
+            h->prof_hdr = nullptr;
+            for (int i = 0; i < 5; ++i) mark(h, i, st);
+            h->have_profile = true;
+        }
+        return launch_scale<T>(C, ldc, (int)m, (int)n, beta, grid, st) == cudaSuccess
+                   ? SPMM_OK : SPMM_ERR_CUDA;
+    }
+
+    const Plan P = make_plan<T>(h, k, n, B, ldb, C, ldc);
+    const int lg = long_grid_of(h);
+    const ScratchLayout L = layout_for(m, n, (int)sizeof(T), lg);
+    spmm_status_t s = ensure_scratch(h, L.total);
+    if (s != SPMM_OK) return s;
+    char* base = static_cast<char*>(h->scratch);
+
+    BinScratch bs{};
+    bs.hdr = reinterpret_cast<int*>(base + L.hdr);
+    bs.tile_counts = reinterpret_cast<int*>(base + L.tile_counts);
+    bs.tile_offsets = reinterpret_cast<int*>(base + L.tile_offsets);
+    bs.rowlist = reinterpret_cast<int*>(base + L.rowlist);
+    bs.long_pre = reinterpret_cast<int*>(base + L.long_pre);
+    bs.tiles = (int)((m + BIN_TILE - 1) / BIN_TILE);
+
+    mark(h, 0, st);
+    if (launch_binning(row_ptr, (int)m, P.short_max, P.long_min, bs, st) != cudaSuccess)
+        return SPMM_ERR_CUDA;
+    mark(h, 1, st);
+
+    SpmmParams<T> p{};
+    p.row_ptr = row_ptr;
+    p.col_idx = col_idx;
+    p.values = values;
+    p.B = B;
+    p.ldb = ldb;
+    p.C = C;
+    p.ldc = ldc;
+    p.m = (int)m;
+    p.n = (int)n;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.panel_cols = P.panel_cols;
+    p.npanels = P.npanels;
+    p.rowlist = bs.rowlist;
+    p.long_pre = bs.long_pre;
+    p.hdr = bs.hdr;
+    p.partials = reinterpret_cast<T*>(base + L.partials);
+    p.long_grid = lg;
+
+    if (launch_rows<T>(p, P.geo, rows_grid(h, (int)sizeof(T), P.geo), st) != cudaSuccess)
+        return SPMM_ERR_CUDA;
+    mark(h, 2, st);
+    if (launch_long<T>(p, P.geo, st) != cudaSuccess) return SPMM_ERR_CUDA;
+    mark(h, 3, st);
+    if (launch_fixup<T>(p, st) != cudaSuccess) return SPMM_ERR_CUDA;
+    mark(h, 4, st);
+    if (h->profiling) {
+        h->prof = spmm_profile_t{};
+        h->prof.launches = 6;
+        h->prof.panels = P.npanels;
+        h->prof.panel_cols = P.panel_cols;
+        h->prof.vec_elems = P.geo.W;
+        h->prof.group_lanes = P.geo.G;
+        h->prof.slots = P.geo.R;
+        h->prof.short_max = P.short_max;
+        h->prof.long_min = P.long_min;
+        h->prof_hdr = bs.hdr;
+        h->have_profile = true;
+    }
+    return SPMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+spmm_status_t spmm_create(spmm_handle_t* out, int device) {
+    if (!out) return SPMM_ERR_NULL_POINTER;
+    *out = nullptr;
+    int count = 0;
+    if (cudaGetDeviceCount(&count) != cudaSuccess) {
+        cudaGetLastError();
+        return SPMM_ERR_UNSUPPORTED_DEVICE;
+    }
+    if (device < 0 || device >= count) return SPMM_ERR_INVALID_ARGUMENT;
+    int major = 0, minor = 0, sms = 0, l2 = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, device) != cudaSuccess) {
+        cudaGetLastError();
+        return SPMM_ERR_CUDA;
+    }
+    // the library carries sm_103a code only
+    if (major != 10 || minor != 3) return SPMM_ERR_UNSUPPORTED_DEVICE;
+    spmm_handle_s* h = new (std::nothrow) spmm_handle_s();
+    if (!h) return SPMM_ERR_ALLOC;
+    h->device = device;
+    h->num_sms = sms;
+    h->l2_bytes = l2;
+    *out = h;
+    return SPMM_OK;
+}
+
+spmm_status_t spmm_destroy(spmm_handle_t h) {
+    if (!h) return SPMM_OK;
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != h->device) cudaSetDevice(h->device);
+    cudaDeviceSynchronize();
+    for (auto& e : h->ev)
+        if (e) cudaEventDestroy(e);
+    if (h->scratch) cudaFree(h->scratch);
+    if (h->check_status) cudaFree(h->check_status);
+    if (cur >= 0 && cur != h->device) cudaSetDevice(cur);
+    cudaGetLastError();
+    delete h;
+    return SPMM_OK;
+}
+
+spmm_status_t spmm_reserve(spmm_handle_t h, int64_t m, int64_t n, int elem_size) {
+    if (!h || m < 0 || n < 0 || (elem_size != 4 && elem_size != 8)) return SPMM_ERR_INVALID_ARGUMENT;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device) {
+        cudaGetLastError();
+        return SPMM_ERR_INVALID_ARGUMENT;
+    }
+    return ensure_scratch(h, layout_for(m, n, elem_size, long_grid_of(h)).total);
+}
+
+spmm_status_t spmm_csr_f32(spmm_handle_t h, float alpha, const int32_t* row_ptr,
+                           const int32_t* col_idx, const float* values, int64_t m, int64_t k,
+                           const float* B, int64_t ldb, int64_t n, float beta, float* C,
+                           int64_t ldc, void* stream) {
+    return spmm_csr_impl<float>(h, alpha, row_ptr, col_idx, values, m, k, B, ldb, n, beta, C, ldc,
+                                stream);
+}
+
+spmm_status_t spmm_csr_f64(spmm_handle_t h, double alpha, const int32_t* row_ptr,
+                           const int32_t* col_idx, const double* values, int64_t m, int64_t k,
+                           const double* B, int64_t ldb, int64_t n, double beta, double* C,
+                           int64_t ldc, void* stream) {
+    return spmm_csr_impl<double>(h, alpha, row_ptr, col_idx, values, m, k, B, ldb, n, beta, C,
+                                 ldc, stream);
+}
+
+spmm_status_t spmm_csr_check(spmm_handle_t h, const int32_t* row_ptr, const int32_t* col_idx,
+                             int64_t m, int64_t k, int64_t nnz, void* stream,
+                             int32_t* host_status) {
+    if (!h || !host_status) return !h ? SPMM_ERR_INVALID_ARGUMENT : SPMM_ERR_NULL_POINTER;
+    if (m < 0 || k < 0 || nnz < 0) return SPMM_ERR_INVALID_ARGUMENT;
+    if (!row_ptr || (nnz > 0 && !col_idx)) return SPMM_ERR_NULL_POINTER;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device) {
+        cudaGetLastError();
+        return SPMM_ERR_INVALID_ARGUMENT;
+    }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (!h->check_status && cudaMalloc(&h->check_status, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        h->check_status = nullptr;
+        return SPMM_ERR_ALLOC;
+    }
+    int status = 0;
+    if (cudaMemsetAsync(h->check_status, 0, sizeof(int), st) != cudaSuccess ||
+        launch_csr_check(row_ptr, col_idx, m, k, nnz, h->check_status, st) != cudaSuccess ||
+        cudaMemcpyAsync(&status, h->check_status, sizeof(int), cudaMemcpyDeviceToHost, st) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess) {
+        cudaGetLastError();
+        return SPMM_ERR_CUDA;
+    }
+    *host_status = status;
+    return status == 0 ? SPMM_OK : SPMM_ERR_INVALID_CSR;
+}
+
+spmm_status_t spmm_set_profiling(spmm_handle_t h, int enable) {
+    if (!h) return SPMM_ERR_INVALID_ARGUMENT;
+    if (enable && !h->ev[0]) {
+        int cur = -1;
+        if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device) {
+            cudaGetLastError();
+            return SPMM_ERR_INVALID_ARGUMENT;
+        }
+        for (auto& e : h->ev) {
+            if (cudaEventCreate(&e) != cudaSuccess) {
+                cudaGetLastError();
+                return SPMM_ERR_CUDA;
+            }
+        }
+    }
+    h->profiling = enable != 0;
+    return SPMM_OK;
+}
+
+spmm_status_t spmm_get_profile(spmm_handle_t h, spmm_profile_t* out) {
+    if (!h || !h->have_profile) return SPMM_ERR_INVALID_ARGUMENT;
+    if (!out) return SPMM_ERR_NULL_POINTER;
+    if (cudaEventSynchronize(h->ev[4]) != cudaSuccess) {
+        cudaGetLastError();
+        return SPMM_ERR_CUDA;
+    }
+    spmm_profile_t p = h->prof;
+    float t[4] = {0, 0, 0, 0};
+    for (int i = 0; i < 4; ++i)
+        if (cudaEventElapsedTime(&t[i], h->ev[i], h->ev[i + 1]) != cudaSuccess) {
+            cudaGetLastError();
+            return SPMM_ERR_CUDA;
+        }
+    p.prepass_ms = t[0];
+    p.rows_ms = t[1];
+    p.long_ms = t[2];
+    p.fixup_ms = t[3];
+    cudaEventElapsedTime(&p.total_ms, h->ev[0], h->ev[4]);
+    if (h->prof_hdr) {
+        int hdr[HDR_WORDS];
+        if (cudaMemcpy(hdr, h->prof_hdr, sizeof(hdr), cudaMemcpyDeviceToHost) != cudaSuccess) {
+            cudaGetLastError();
+            return SPMM_ERR_CUDA;
+        }
+        p.rows_short = hdr[HDR_COUNT_SHORT];
+        p.rows_medium = hdr[HDR_COUNT_MEDIUM];
+        p.rows_long = hdr[HDR_COUNT_LONG];
+        p.long_nnz = hdr[HDR_LONG_NNZ];
+    }
+    *out = p;
+    return SPMM_OK;
+}
+
+const char* spmm_status_string(spmm_status_t s) {
+    switch (s) {
+        case SPMM_OK: return "SPMM_OK";
+        case SPMM_ERR_INVALID_ARGUMENT: return "SPMM_ERR_INVALID_ARGUMENT: invalid argument";
+        case SPMM_ERR_DIMENSION_MISMATCH:
+            return "SPMM_ERR_DIMENSION_MISMATCH: leading dimension smaller than the column count";
+        case SPMM_ERR_NULL_POINTER: return "SPMM_ERR_NULL_POINTER: required pointer is NULL";
+        case SPMM_ERR_UNSUPPORTED_DEVICE:
+            return "SPMM_ERR_UNSUPPORTED_DEVICE: needs a compute capability 10.3 (sm_103) GPU";
+        case SPMM_ERR_ALLOC: return "SPMM_ERR_ALLOC: scratch allocation failed";
+        case SPMM_ERR_CUDA: return "SPMM_ERR_CUDA: CUDA runtime or launch error";
+        case SPMM_ERR_INVALID_CSR: return "SPMM_ERR_INVALID_CSR: malformed CSR structure";
+    }
+    return "unknown spmm status";
+}
+
+}  // extern "C"

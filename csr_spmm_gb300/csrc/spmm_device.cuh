@@ -1,0 +1,160 @@
+// Device-side building blocks shared by the CSR SpMM kernels (sm_103a).
+//
+// Loads carry explicit cache policy:
+//   * B rows are gathered with L2 evict_last (the B panel being multiplied
+//     should stay resident in the 126 MB L2 while A and C stream past it);
+//   * the CSR stream (row_ptr, col_idx, values) is read once, with
+//     L1::no_allocate and L2 evict_first;
+//   * C is read (beta != 0) and written with the streaming (.cs) policy.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "spmm_internal.h"
+
+namespace spmm {
+
+// ---------------------------------------------------------------------------
+// cache policies (created once per thread; cheap)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// ---------------------------------------------------------------------------
+// CSR stream loads (read once)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int ld_stream(const int* p, uint64_t pol) {
+    int v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.b32 %0, [%1], %2;"
+                 : "=r"(v) : "l"(p), "l"(pol));
+    return v;
+}
+__device__ __forceinline__ float ld_stream(const float* p, uint64_t pol) {
+    float v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.f32 %0, [%1], %2;"
+                 : "=f"(v) : "l"(p), "l"(pol));
+    return v;
+}
+__device__ __forceinline__ double ld_stream(const double* p, uint64_t pol) {
+    double v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.f64 %0, [%1], %2;"
+                 : "=d"(v) : "l"(p), "l"(pol));
+    return v;
+}
+
+// ---------------------------------------------------------------------------
+// B gathers: W consecutive elements (W * sizeof(T) = 4, 8, 16 or 32 bytes)
+// ---------------------------------------------------------------------------
+template <typename T, int W> struct BLoad;
+
+template <> struct BLoad<float, 1> {
+    __device__ __forceinline__ static void run(const float* p, float (&v)[1], uint64_t pol) {
+        asm volatile("ld.global.nc.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v[0]) : "l"(p), "l"(pol));
+    }
+};
+template <> struct BLoad<float, 4> {
+    __device__ __forceinline__ static void run(const float* p, float (&v)[4], uint64_t pol) {
+        asm volatile("ld.global.nc.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
+                     : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]) : "l"(p), "l"(pol));
+    }
+};
+template <> struct BLoad<float, 8> {
+    __device__ __forceinline__ static void run(const float* p, float (&v)[8], uint64_t) {
+        asm volatile("ld.global.nc.L2::evict_last.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]),
+                       "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7]) : "l"(p));
+    }
+};
+template <> struct BLoad<double, 1> {
+    __device__ __forceinline__ static void run(const double* p, double (&v)[1], uint64_t pol) {
+        asm volatile("ld.global.nc.L2::cache_hint.f64 %0, [%1], %2;" : "=d"(v[0]) : "l"(p), "l"(pol));
+    }
+};
+template <> struct BLoad<double, 2> {
+    __device__ __forceinline__ static void run(const double* p, double (&v)[2], uint64_t pol) {
+        asm volatile("ld.global.nc.L2::cache_hint.v2.f64 {%0,%1}, [%2], %3;"
+                     : "=d"(v[0]), "=d"(v[1]) : "l"(p), "l"(pol));
+    }
+};
+template <> struct BLoad<double, 4> {
+    __device__ __forceinline__ static void run(const double* p, double (&v)[4], uint64_t) {
+        asm volatile("ld.global.nc.L2::evict_last.v4.f64 {%0,%1,%2,%3}, [%4];"
+                     : "=d"(v[0]), "=d"(v[1]), "=d"(v[2]), "=d"(v[3]) : "l"(p));
+    }
+};
+
+// Element-wise load of the first `cnt` (< W) elements; the rest are zero.
+template <typename T, int W>
+__device__ __forceinline__ void load_b_partial(const T* p, int cnt, T (&v)[W], uint64_t pol) {
+#pragma unroll
+    for (int e = 0; e < W; ++e) {
+        T x[1] = {T(0)};
+        if (e < cnt) BLoad<T, 1>::run(p + e, x, pol);
+        v[e] = x[0];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// C epilogue: C = alpha * acc (beta == 0, C not read) or alpha * acc + beta * C
+// ---------------------------------------------------------------------------
+template <typename T>
+__device__ __forceinline__ T epi(T alpha, T acc, T beta, T c_old) {
+    return alpha * acc + beta * c_old;
+}
+
+template <typename T, int W>
+__device__ __forceinline__ void store_c(T* c, int cnt, const T (&acc)[W], T alpha, T beta,
+                                        bool read_c) {
+    if (cnt == W && (W * sizeof(T)) % 16 == 0) {
+        // W * sizeof(T) is 16 or 32 bytes: use 16-byte streaming accesses
+        constexpr int PER = 16 / sizeof(T);
+#pragma unroll
+        for (int h = 0; h < W; h += PER) {
+            if constexpr (sizeof(T) == 4) {
+                float4* q = reinterpret_cast<float4*>(c + h);
+                float4 o;
+                if (read_c) {
+                    float4 old = __ldcs(q);
+                    o = make_float4(epi<float>(alpha, acc[h], beta, old.x),
+                                    epi<float>(alpha, acc[h + 1], beta, old.y),
+                                    epi<float>(alpha, acc[h + 2], beta, old.z),
+                                    epi<float>(alpha, acc[h + 3], beta, old.w));
+                } else {
+                    o = make_float4(alpha * acc[h], alpha * acc[h + 1], alpha * acc[h + 2],
+                                    alpha * acc[h + 3]);
+                }
+                __stcs(q, o);
+            } else {
+                double2* q = reinterpret_cast<double2*>(c + h);
+                double2 o;
+                if (read_c) {
+                    double2 old = __ldcs(q);
+                    o = make_double2(epi<double>(alpha, acc[h], beta, old.x),
+                                     epi<double>(alpha, acc[h + 1], beta, old.y));
+                } else {
+                    o = make_double2(alpha * acc[h], alpha * acc[h + 1]);
+                }
+                __stcs(q, o);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < W; ++e) {
+            if (e < cnt) {
+                T o = read_c ? epi<T>(alpha, acc[e], beta, __ldcs(c + e)) : alpha * acc[e];
+                __stcs(c + e, o);
+            }
+        }
+    }
+}
+
+}  // namespace spmm

@@ -1,0 +1,102 @@
+// Internal interfaces between the host driver (spmm_api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace spmm {
+
+constexpr unsigned FULL = 0xffffffffu;
+
+// Row bins produced by the pre-pass.  A row of length len goes to
+//   SHORT  if len <= short_max   (one lane group per row)
+//   MEDIUM if len <  long_min    (one warp per row)
+//   LONG   otherwise             (split across CTAs, partial sums + fixup)
+enum Bin { BIN_SHORT = 0, BIN_MEDIUM = 1, BIN_LONG = 2, NUM_BINS = 3 };
+
+// Device header written by the pre-pass (int32 words).
+enum HeaderWord {
+    HDR_COUNT_SHORT = 0,
+    HDR_COUNT_MEDIUM = 1,
+    HDR_COUNT_LONG = 2,
+    HDR_LONG_NNZ = 3,   // total entries in long rows
+    HDR_WORDS = 8
+};
+
+// Rows per pre-pass tile: 256 threads x 8 rows.
+constexpr int BIN_THREADS = 256;
+constexpr int BIN_ITEMS = 8;
+constexpr int BIN_TILE = BIN_THREADS * BIN_ITEMS;
+
+// Long-row kernel geometry.
+constexpr int LONG_THREADS = 512;
+constexpr int LONG_WARPS = LONG_THREADS / 32;
+constexpr int LONG_MIN_SEGMENT = 2048;   // smallest per-CTA share of long-row entries
+
+// Rows kernel block size.
+constexpr int ROWS_THREADS = 256;
+
+struct BinScratch {
+    int* rowlist;       // [m]  short rows, then medium rows, then long rows (each ascending)
+    int* long_pre;      // [m + 1] exclusive prefix of long-row lengths (stable order)
+    int* tile_counts;   // [tiles * 4]  per tile: short, medium, long counts, long nnz
+    int* tile_offsets;  // [tiles * 4]  exclusive scans of the above over tiles
+    int* hdr;           // [HDR_WORDS]
+    int tiles;
+};
+
+template <typename T>
+struct SpmmParams {
+    const int* row_ptr;
+    const int* col_idx;
+    const T* values;
+    const T* B;
+    int64_t ldb;
+    T* C;
+    int64_t ldc;
+    int m;
+    int n;               // total columns
+    T alpha;
+    T beta;
+    int panel_cols;      // columns per L2 panel (multiple of the vector width)
+    int npanels;
+    // bins
+    const int* rowlist;
+    const int* long_pre;
+    const int* hdr;
+    // long-row partial sums: [2 * long_grid, n]
+    T* partials;
+    int long_grid;
+};
+
+// Kernel geometry chosen on the host for one call.
+struct Geometry {
+    int W;        // elements per vector access (1, 2, 4 or 8)
+    int G;        // lanes per row group (power of two <= 32)
+    int R;        // vector slots per lane per column pass (1..4)
+};
+
+// ---- pre-pass (spmm_bin.cu) ----
+cudaError_t launch_binning(const int* row_ptr, int m, int short_max, int long_min,
+                           const BinScratch& s, cudaStream_t st);
+
+// ---- per-bin kernels (spmm_rows_*.cu, spmm_long_*.cu) ----
+template <typename T>
+cudaError_t launch_rows(const SpmmParams<T>& p, const Geometry& g, int grid, cudaStream_t st);
+template <typename T>
+cudaError_t launch_long(const SpmmParams<T>& p, const Geometry& g, cudaStream_t st);
+template <typename T>
+cudaError_t launch_fixup(const SpmmParams<T>& p, cudaStream_t st);
+
+// ---- epilogue-only and checking kernels (spmm_misc.cu) ----
+template <typename T>
+cudaError_t launch_scale(T* C, int64_t ldc, int m, int n, T beta, int grid, cudaStream_t st);
+cudaError_t launch_csr_check(const int* row_ptr, const int* col_idx, int64_t m, int64_t k,
+                             int64_t nnz, int* status, cudaStream_t st);
+
+// Blocks per SM the rows kernel reaches for this geometry (occupancy query).
+template <typename T>
+int rows_blocks_per_sm(const Geometry& g);
+
+}  // namespace spmm

@@ -1,0 +1,156 @@
+/*
+ * csr_spmm.h -- C ABI of the GB300 (sm_103a) CSR SpMM library.
+ *
+ * Operation (oxicuda-sparse, ops/spmm.rs: module doc and `spmm` doc comment):
+ *
+ *     C = alpha * A * B + beta * C
+ *
+ * A is an m x k sparse matrix in CSR form: row_ptr (int32, m + 1 entries),
+ * col_idx (int32, nnz entries) and values (nnz entries), nnz = row_ptr[m].
+ * B is a dense k x n matrix and C a dense m x n matrix, both row-major with
+ * leading dimensions ldb and ldc (element (r, c) of B lives at B[r * ldb + c]).
+ * The page's `spmm` takes (handle, alpha, A, B, beta, C) and launches with the
+ * arguments (row_ptr, col_idx, values, B, C, alpha, beta, m, n, ldb, ldc) on
+ * the handle's stream; this ABI passes the same quantities flat, plus k and the
+ * stream.
+ *
+ * Conventions (the page always reads C and returns early when k == 0; these
+ * are the readings this library implements, those of dense BLAS):
+ *   - beta == 0: C is write-only; its previous contents (even NaN/Inf) are
+ *     never read.
+ *   - alpha == 0: A and B are not read; C = beta * C (C = 0 when beta == 0).
+ *   - k == 0 (every row empty): C = beta * C.  An empty row i gives
+ *     C[i, :] = beta * C[i, :].
+ *   - m == 0 or n == 0: nothing is done.
+ *   - Duplicate column indices within a row each contribute; explicit zeros
+ *     are multiplied like any other entry.
+ *   - Results are deterministic: the same inputs give bit-identical C on every
+ *     call (no floating-point atomics; every sum has a fixed order).
+ *
+ * Memory and ownership: every array argument is a DEVICE pointer on the
+ * handle's device, owned by the caller and not retained after the call
+ * returns.  The handle owns its scratch memory (row bins, long-row partial
+ * sums) and grows it on demand; growth calls cudaMalloc/cudaFree, which
+ * synchronise the device, so reserve it first (spmm_reserve) when the call
+ * will be captured in a CUDA graph.  C must not overlap A or B.
+ *
+ * Asynchrony: the products are enqueued on `stream` (a cudaStream_t passed as
+ * void*; NULL means the legacy default stream) and return without
+ * synchronising.  Launch errors are returned; a fault inside a kernel
+ * surfaces at the caller's next synchronisation.  A handle may be used by one
+ * stream at a time (its scratch is shared by its calls).
+ *
+ * CSR contents are a precondition: row_ptr[0] == 0, row_ptr non-decreasing,
+ * 0 <= col_idx[p] < k.  They are not checked on the product path (nor are
+ * they on the page); spmm_csr_check verifies them on the device.
+ */
+#ifndef CSR_SPMM_H
+#define CSR_SPMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes.  The page's error kinds map as: DimensionMismatch ->
+ * SPMM_ERR_DIMENSION_MISMATCH, InvalidArgument -> SPMM_ERR_INVALID_ARGUMENT,
+ * Cuda -> SPMM_ERR_CUDA (oxicuda-sparse, ops/spmm.rs, `spmm` "Errors"). */
+typedef enum {
+    SPMM_OK = 0,
+    SPMM_ERR_INVALID_ARGUMENT = 1,   /* bad handle, negative or oversize m/k/n, wrong device */
+    SPMM_ERR_DIMENSION_MISMATCH = 2, /* ldb < max(1, n) or ldc < max(1, n) */
+    SPMM_ERR_NULL_POINTER = 3,       /* a pointer that the call must dereference is NULL */
+    SPMM_ERR_UNSUPPORTED_DEVICE = 4, /* device is not compute capability 10.x / sm_103 family */
+    SPMM_ERR_ALLOC = 5,              /* scratch allocation failed */
+    SPMM_ERR_CUDA = 6,               /* a CUDA runtime call or kernel launch failed */
+    SPMM_ERR_INVALID_CSR = 7         /* spmm_csr_check found a malformed CSR structure */
+} spmm_status_t;
+
+typedef struct spmm_handle_s *spmm_handle_t;
+
+/* Create a handle for `device` (a CUDA ordinal).  Queries the SM count and
+ * L2 size used to size grids and column panels.  Does not change the current
+ * device.  *h is set to NULL on failure. */
+spmm_status_t spmm_create(spmm_handle_t *h, int device);
+
+/* Release the handle and its scratch.  Synchronises the handle's device.
+ * NULL is accepted and ignored. */
+spmm_status_t spmm_destroy(spmm_handle_t h);
+
+/* Grow the handle's scratch for products with up to m rows and n columns of
+ * the given element size (4 or 8 bytes), so that later calls of that size
+ * allocate nothing.  Synchronous. */
+spmm_status_t spmm_reserve(spmm_handle_t h, int64_t m, int64_t n, int elem_size);
+
+/* C = alpha * A * B + beta * C in binary32 (oxicuda-sparse, ops/spmm.rs, `spmm`
+ * with T = f32).  Arguments as described at the top of this file:
+ *   row_ptr [m+1], col_idx [nnz], values [nnz]   CSR of A (m x k)
+ *   B  [k rows, stride ldb]   dense, row-major, only columns 0..n-1 are read
+ *   C  [m rows, stride ldc]   dense, row-major, columns 0..n-1 are written
+ * Requires m, k, n >= 0, m < 2^31 - 1, k <= 2^31 - 1, ldb >= max(1, n),
+ * ldc >= max(1, n); the current device must be the handle's device.
+ * Pointers may be NULL only where the conventions above say the array is not
+ * read (A and B when alpha == 0 or k == 0; everything when m == 0 or n == 0).
+ * The library cannot see nnz, so col_idx and values must be valid addresses
+ * whenever A is read, even for nnz == 0. */
+spmm_status_t spmm_csr_f32(spmm_handle_t h, float alpha,
+                           const int32_t *row_ptr, const int32_t *col_idx, const float *values,
+                           int64_t m, int64_t k,
+                           const float *B, int64_t ldb, int64_t n,
+                           float beta, float *C, int64_t ldc, void *stream);
+
+/* Same in binary64 (the page's `spmm` with T = f64). */
+spmm_status_t spmm_csr_f64(spmm_handle_t h, double alpha,
+                           const int32_t *row_ptr, const int32_t *col_idx, const double *values,
+                           int64_t m, int64_t k,
+                           const double *B, int64_t ldb, int64_t n,
+                           double beta, double *C, int64_t ldc, void *stream);
+
+/* Check the CSR structure on the device: row_ptr[0] == 0, row_ptr
+ * non-decreasing, row_ptr[m] == nnz, and 0 <= col_idx[p] < k for p < nnz.
+ * Reads exactly row_ptr[0..m] and col_idx[0..nnz-1].  Synchronises `stream`
+ * and stores a bit mask in *host_status (0 = valid; bit 0: row_ptr[0] != 0,
+ * bit 1: row_ptr decreases, bit 2: row_ptr[m] != nnz, bit 3: a column index
+ * out of range).  Returns SPMM_ERR_INVALID_CSR when the mask is non-zero.
+ * A debugging aid: the product entry points never run it. */
+spmm_status_t spmm_csr_check(spmm_handle_t h, const int32_t *row_ptr, const int32_t *col_idx,
+                             int64_t m, int64_t k, int64_t nnz, void *stream,
+                             int32_t *host_status);
+
+/* Per-stage record of the most recent product issued on a handle with
+ * profiling enabled (a tracing aid; the pages have no counterpart).  Times are
+ * GPU durations between CUDA events recorded on the call's stream around each
+ * stage; the counts come from the device-side row bins. */
+typedef struct {
+    float prepass_ms;      /* row-binning pre-pass (3 launches) */
+    float rows_ms;         /* short + medium rows kernel (1 launch) */
+    float long_ms;         /* long-row CTA split (1 launch) */
+    float fixup_ms;        /* long-row fixup (1 launch) */
+    float total_ms;        /* first event to last event */
+    int32_t launches;      /* kernels the product launched */
+    int32_t rows_short, rows_medium, rows_long;  /* rows per bin */
+    int32_t long_nnz;      /* entries in long rows */
+    int32_t panels, panel_cols;                  /* column panels of B/C */
+    int32_t vec_elems, group_lanes, slots;       /* kernel geometry: W, G, R */
+    int32_t short_max, long_min;                 /* bin thresholds (row lengths) */
+} spmm_profile_t;
+
+/* Turn per-stage event recording on (enable != 0) or off for later calls on
+ * this handle.  Off by default; recording adds a few events per call. */
+spmm_status_t spmm_set_profiling(spmm_handle_t h, int enable);
+
+/* Read the record of the most recent profiled product (waits for its events
+ * and copies the bin counts to the host).  SPMM_ERR_INVALID_ARGUMENT if no
+ * profiled product has been issued.  Only the epilogue-only path ran when
+ * launches == 1 and rows_ms == 0. */
+spmm_status_t spmm_get_profile(spmm_handle_t h, spmm_profile_t *out);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char *spmm_status_string(spmm_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSR_SPMM_H */

@@ -1,0 +1,74 @@
+"""The C ABI library: loads, exports every declared symbol, host-side behaviour (no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import csr_spmm_gb300 as cs
+from csr_spmm_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build_library()
+    return _lib.library()
+
+
+def _declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(spmm_\w+)\s*\(", text))
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared_symbols()
+    assert {"spmm_create", "spmm_destroy", "spmm_csr_f32", "spmm_csr_f64",
+            "spmm_csr_check", "spmm_status_string"} <= declared
+    for name in declared:
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+    assert declared == set(_lib.EXPORTED)
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        s = cs.status_string(code)
+        assert s.startswith("SPMM_")
+    assert "unknown" in cs.status_string(99)
+
+
+def test_null_handle_is_rejected_before_any_device_work(lib):
+    vp = ctypes.c_void_p
+    assert lib.spmm_csr_f32(None, 1.0, None, None, None, 4, 4, None, 4, 4, 0.0, None, 4,
+                            None) == cs.SPMM_ERR_INVALID_ARGUMENT
+    assert lib.spmm_csr_f64(None, 1.0, None, None, None, 4, 4, None, 4, 4, 0.0, None, 4,
+                            None) == cs.SPMM_ERR_INVALID_ARGUMENT
+    assert lib.spmm_reserve(None, 4, 4, 4) == cs.SPMM_ERR_INVALID_ARGUMENT
+    st = ctypes.c_int32(0)
+    assert lib.spmm_csr_check(None, None, None, 1, 1, 0, None,
+                              ctypes.byref(st)) == cs.SPMM_ERR_INVALID_ARGUMENT
+    assert lib.spmm_create(None, 0) == cs.SPMM_ERR_NULL_POINTER
+    assert lib.spmm_destroy(None) == cs.SPMM_OK
+    del vp
+
+
+def test_create_without_gpu_fails_cleanly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = ctypes.c_void_p(1)
+    s = lib.spmm_create(ctypes.byref(h), 0)
+    assert s != cs.SPMM_OK and h.value is None
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(ImportError):
+        _lib.library(str(tmp_path / "nope.so"))

@@ -53,21 +53,25 @@ def _digest(units, deps, extra) -> str:
     return h.hexdigest()
 
 
-def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
-    """Compile and link the library if anything changed; return its path."""
+def build(verbose: bool = False, force: bool = False, extra_flags=(), out: str = LIB) -> str:
+    """Compile and link the library if anything changed; return its path.
+
+    ``extra_flags`` (e.g. -D tuning macros) and ``out`` build a variant
+    library elsewhere, with its own object directory."""
     units, deps = _sources()
     digest = _digest(units, deps, extra_flags)
-    stamp = LIB + ".sha256"
-    if not force and os.path.exists(LIB) and os.path.exists(stamp):
+    stamp = out + ".sha256"
+    obj_dir = OBJ_DIR if out == LIB else out + ".objs"
+    if not force and os.path.exists(out) and os.path.exists(stamp):
         with open(stamp) as f:
             if f.read().strip() == digest:
-                return LIB
+                return out
     nvcc = _nvcc()
-    os.makedirs(OBJ_DIR, exist_ok=True)
-    os.makedirs(LIB_DIR, exist_ok=True)
+    os.makedirs(obj_dir, exist_ok=True)
+    os.makedirs(os.path.dirname(out), exist_ok=True)
 
     def compile_one(unit):
-        obj = os.path.join(OBJ_DIR, unit[:-3] + ".o")
+        obj = os.path.join(obj_dir, unit[:-3] + ".o")
         cmd = [nvcc] + NVCC_FLAGS + list(extra_flags) + ["-c", os.path.join(CSRC, unit), "-o", obj]
         if verbose:
             cmd += ["-Xptxas", "-v"]
@@ -80,15 +84,15 @@ def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
 
     with ThreadPoolExecutor(max_workers=max(1, min(len(units), os.cpu_count() or 4))) as ex:
         objs = list(ex.map(compile_one, units))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = out + f".tmp{os.getpid()}"
     cmd = [nvcc] + ARCH + ["-shared", "--cudart", "static", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, out)
     with open(stamp, "w") as f:
         f.write(digest + "\n")
-    return LIB
+    return out
 
 
 if __name__ == "__main__":

@@ -37,8 +37,14 @@ namespace {
 
 // Fraction of L2 a B column panel may occupy; panels are only used when B
 // itself exceeds PANEL_TRIGGER of L2.
-constexpr double PANEL_FRACTION = 0.5;
-constexpr double PANEL_TRIGGER = 0.75;
+#ifndef SPMM_PANEL_FRACTION
+#define SPMM_PANEL_FRACTION 0.5
+#endif
+#ifndef SPMM_PANEL_TRIGGER
+#define SPMM_PANEL_TRIGGER 3.0
+#endif
+constexpr double PANEL_FRACTION = SPMM_PANEL_FRACTION;
+constexpr double PANEL_TRIGGER = SPMM_PANEL_TRIGGER;
 // Rows at least this long go to the CTA-split kernel.
 constexpr int LONG_MIN_ROW = 1024;
 // Long-row grid: CTAs per SM.
@@ -135,7 +141,7 @@ Plan make_plan(const spmm_handle_s* h, int64_t k, int64_t n, const T* B, int64_t
     }
     // bin thresholds
     const int bytes_per_entry = P.geo.R * W * es;
-    const int U = std::min(8, std::max(1, 128 / bytes_per_entry));
+    const int U = std::min(SPMM_BATCH_MAX, std::max(1, SPMM_BATCH_BYTES / bytes_per_entry));
     const int CH = std::max(P.geo.G, U);
     P.long_min = LONG_MIN_ROW;
     P.short_max = (P.geo.G == 32) ? P.long_min - 1 : std::min(P.long_min - 1, 2 * CH);

@@ -34,8 +34,18 @@ constexpr int LONG_THREADS = 512;
 constexpr int LONG_WARPS = LONG_THREADS / 32;
 constexpr int LONG_MIN_SEGMENT = 2048;   // smallest per-CTA share of long-row entries
 
-// Rows kernel block size.
+// Rows kernel block size and minimum resident blocks per SM (a register cap).
 constexpr int ROWS_THREADS = 256;
+#ifndef SPMM_ROWS_MIN_BLOCKS
+#define SPMM_ROWS_MIN_BLOCKS 4
+#endif
+// B bytes each lane keeps in flight per gather batch, and the batch cap.
+#ifndef SPMM_BATCH_BYTES
+#define SPMM_BATCH_BYTES 64
+#endif
+#ifndef SPMM_BATCH_MAX
+#define SPMM_BATCH_MAX 8
+#endif
 
 struct BinScratch {
     int* rowlist;       // [m]  short rows, then medium rows, then long rows (each ascending)

@@ -13,11 +13,17 @@
 // shuffle and every lane gathers a 16-byte vector of the B row, so each B row
 // segment is fetched with full-sector, coalesced requests.
 //
+// The kernels are bound by the latency of dependent memory round trips
+// (row list -> row_ptr -> col_idx/values -> B), so each warp works through a
+// contiguous range of rows with the stream software-pipelined: the row
+// descriptors of 32 rows are loaded at once, and the (col_idx, value) pairs of
+// the next step are in flight while the current step's B gathers are issued
+// and consumed.
+//
 // Entry distribution: in each step a group takes CH = max(G, U) consecutive
-// entries; lane g of the group loads entries g, g + G, ... of the step
-// (coalesced), then the group walks them in batches of U, broadcasting
-// (col, value) from the owning lane and issuing U * R independent B gathers
-// before the FMAs, so that every lane keeps U * R loads in flight.
+// entries; lane g of the group holds entries g, g + G, ... of the step, and
+// the group walks them in batches of U, broadcasting (col, value) from the
+// owning lane and issuing U * R independent B gathers before the FMAs.
 #pragma once
 
 #include "spmm_device.cuh"
@@ -29,84 +35,82 @@ struct Cfg {
     static_assert(G >= 1 && G <= 32 && (G & (G - 1)) == 0, "G must be a power of two <= 32");
     static constexpr int SLOTS = G * R;                       // vectors per column pass
     static constexpr int BYTES_PER_ENTRY = R * W * (int)sizeof(T);
-    static constexpr int U0 = 128 / BYTES_PER_ENTRY;          // ~128 B of loads in flight/lane
-    static constexpr int U = U0 < 1 ? 1 : (U0 > 8 ? 8 : U0);  // entries per batch
+    static constexpr int U0 = SPMM_BATCH_BYTES / BYTES_PER_ENTRY;   // B bytes in flight/lane
+    static constexpr int U = U0 < 1 ? 1 : (U0 > SPMM_BATCH_MAX ? SPMM_BATCH_MAX : U0);
     static constexpr int CH = G > U ? G : U;                  // entries per group per step
     static constexpr int Q = CH / G;                          // (col, value) loads per lane per step
-    static constexpr int RPW = 32 / G;                        // groups (rows) per warp
+    static constexpr int RPW = 32 / G;                        // groups per warp
 };
 
-// Accumulate entries [e0, e0 + len) of A into acc, for the column pass whose
-// first vector is vbase, in a panel of pw columns starting at c0.
-//   MEDIUM == false: each group walks its own row (e0, len per group); the
-//                    step loop runs to the longest row in the warp.
-//   MEDIUM == true : the whole warp shares one entry range; group gi takes
-//                    entries [s + gi*CH, s + gi*CH + CH) of each warp step of
-//                    RPW*CH entries.  The caller combines the groups.
-template <typename T, int W, int G, int R, bool MEDIUM>
-__device__ __forceinline__ void accumulate(T (&acc)[R][W], const int* __restrict__ col_idx,
-                                           const T* __restrict__ values,
-                                           const T* __restrict__ Bp, int64_t ldb, int e0,
-                                           int len, int vbase, int pw, uint64_t pol_b,
-                                           uint64_t pol_s) {
-    using C = Cfg<T, W, G, R>;
-    const int lane = threadIdx.x & 31;
-    const int g = lane & (G - 1);
-    const int gi = lane / G;
-    const int step = MEDIUM ? C::RPW * C::CH : C::CH;
-    const int goff = MEDIUM ? gi * C::CH : 0;
-    const int span = MEDIUM ? len : __reduce_max_sync(FULL, len);   // warp-uniform
+template <typename T, int W, int R>
+__device__ __forceinline__ void zero_acc(T (&acc)[R][W]) {
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int e = 0; e < W; ++e) acc[r][e] = T(0);
+}
 
-    for (int s = 0; s < span; s += step) {
-        // load this step's (col, value) pairs: lane g holds entries g + G*q
-        int colr[C::Q];
-        T valr[C::Q];
+// Lane g of a group loads entries first + g + G*q (q < Q) that lie below `limit`.
+template <typename T, int G, int Q>
+__device__ __forceinline__ void load_entries(int (&col)[Q], T (&val)[Q],
+                                             const int* __restrict__ col_idx,
+                                             const T* __restrict__ values, int first, int limit,
+                                             uint64_t pol_s) {
+    const int g = (threadIdx.x & 31) & (G - 1);
 #pragma unroll
-        for (int q = 0; q < C::Q; ++q) {
-            const int j = s + goff + g + G * q;
-            colr[q] = 0;
-            valr[q] = T(0);
-            if (j < len) {
-                colr[q] = ld_stream(col_idx + e0 + j, pol_s);
-                valr[q] = ld_stream(values + e0 + j, pol_s);
-            }
+    for (int q = 0; q < Q; ++q) {
+        const int j = first + g + G * q;
+        col[q] = 0;
+        val[q] = T(0);
+        if (j < limit) {
+            col[q] = ld_stream(col_idx + j, pol_s);
+            val[q] = ld_stream(values + j, pol_s);
         }
-        const int cnt = min(C::CH, len - s - goff);   // valid entries for this group (may be <= 0)
-        const int cmax = min(C::CH, span - s);          // warp-uniform bound
+    }
+}
+
+// One step: the group consumes its `cnt` (<= CH) entries held in (col, val),
+// in batches of U; `cmax` is a warp-uniform upper bound on every group's cnt.
+template <typename T, int W, int G, int R>
+__device__ __forceinline__ void consume_step(T (&acc)[R][W], const int (&col)[Cfg<T, W, G, R>::Q],
+                                             const T (&val)[Cfg<T, W, G, R>::Q], int cnt,
+                                             int cmax, const T* __restrict__ Bp, int64_t ldb,
+                                             int vbase, int pw) {
+    using C = Cfg<T, W, G, R>;
+    const int g = (threadIdx.x & 31) & (G - 1);
 #pragma unroll
-        for (int j0 = 0; j0 < C::CH; j0 += C::U) {
-            if (j0 >= cmax) break;                      // uniform
-            T bv[C::U][R][W];
-            T av[C::U];
+    for (int j0 = 0; j0 < C::CH; j0 += C::U) {
+        if (j0 >= cmax) break;                          // warp-uniform
+        T bv[C::U][R][W];
+        T av[C::U];
 #pragma unroll
-            for (int u = 0; u < C::U; ++u) {
-                const int j = j0 + u;                   // compile-time after unrolling
-                const int q = (j / G) % C::Q;
-                const int src = j % G;
-                const int cj = __shfl_sync(FULL, colr[q], src, G);
-                const T aj = __shfl_sync(FULL, valr[q], src, G);
-                const bool ok = (j < C::CH) && (j < cnt);
-                av[u] = ok ? aj : T(0);
-                const T* brow = Bp + (int64_t)cj * ldb;
+        for (int u = 0; u < C::U; ++u) {
+            const int j = j0 + u;                       // compile-time after unrolling
+            const int q = j / G;
+            const int src = j % G;
+            const int cj = __shfl_sync(FULL, col[q], src, G);
+            const T aj = __shfl_sync(FULL, val[q], src, G);
+            const bool ok = j < cnt;
+            av[u] = ok ? aj : T(0);
+            const T* brow = Bp + (int64_t)cj * ldb;
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const int col = (vbase + g + G * r) * W;
-                    if (ok && col < pw) {
-                        if (col + W <= pw) BLoad<T, W>::run(brow + col, bv[u][r], pol_b);
-                        else load_b_partial<T, W>(brow + col, pw - col, bv[u][r], pol_b);
-                    } else {
+            for (int r = 0; r < R; ++r) {
+                const int c = (vbase + g + G * r) * W;
+                if (ok && c < pw) {
+                    if (c + W <= pw) BLoad<T, W>::run(brow + c, bv[u][r]);
+                    else load_b_partial<T, W>(brow + c, pw - c, bv[u][r]);
+                } else {
 #pragma unroll
-                        for (int e = 0; e < W; ++e) bv[u][r][e] = T(0);
-                    }
+                    for (int e = 0; e < W; ++e) bv[u][r][e] = T(0);
                 }
             }
-#pragma unroll
-            for (int u = 0; u < C::U; ++u)
-#pragma unroll
-                for (int r = 0; r < R; ++r)
-#pragma unroll
-                    for (int e = 0; e < W; ++e) acc[r][e] = fma(av[u], bv[u][r][e], acc[r][e]);
         }
+#pragma unroll
+        for (int u = 0; u < C::U; ++u)
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int e = 0; e < W; ++e) acc[r][e] = fma(av[u], bv[u][r][e], acc[r][e]);
     }
 }
 
@@ -133,71 +137,153 @@ __device__ __forceinline__ void write_row(T* __restrict__ Crow, const T (&acc)[R
 }
 
 // ---------------------------------------------------------------------------
-// Short and medium rows.  One persistent launch walks warp items, panel-major:
-// per panel, first the short items (RPW rows each, one per lane group), then
-// the medium rows (one warp each, groups split the entries).
+// A warp works through rows list[r0 .. r1) of one bin, for the panel of pw
+// columns starting at c0.
+//   MEDIUM == false (short rows): group gi takes rows gi, gi + RPW, ... of
+//     every 32-row block; each group walks its own row CH entries per step.
+//   MEDIUM == true (medium rows): the whole warp takes one row at a time;
+//     group gi takes entries [s + gi*CH, s + gi*CH + CH) of each warp step of
+//     RPW*CH entries, and the groups are combined at the end of the row.
 // ---------------------------------------------------------------------------
-template <typename T, int W, int G, int R>
-__global__ void __launch_bounds__(ROWS_THREADS)
-rows_kernel(SpmmParams<T> p) {
+template <typename T, int W, int G, int R, bool MEDIUM>
+__device__ __forceinline__ void process_rows(const SpmmParams<T>& p, const int* __restrict__ list,
+                                             int r0, int r1, int c0, int pw, uint64_t pol_s,
+                                             bool read_c) {
     using C = Cfg<T, W, G, R>;
+    constexpr int Q = C::Q;
     const int lane = threadIdx.x & 31;
     const int gi = lane / G;
-    const uint64_t pol_b = policy_evict_last();
+    constexpr int TSTEP = MEDIUM ? 1 : C::RPW;              // row-slot advance per row
+    constexpr int ESTEP = MEDIUM ? C::RPW * C::CH : C::CH;  // entry advance per step
+    const int goff = MEDIUM ? gi * C::CH : 0;
+    const int nvec = (pw + W - 1) / W;
+    const T* Bp = p.B + c0;
+
+    for (int sub = r0; sub < r1; sub += 32) {
+        const int nrows = min(32, r1 - sub);
+        int my_row = -1, my_e0 = 0, my_len = 0;
+        if (lane < nrows) {
+            my_row = list[sub + lane];
+            my_e0 = p.row_ptr[my_row];
+            my_len = p.row_ptr[my_row + 1] - my_e0;
+        }
+        for (int vbase = 0; vbase < nvec; vbase += C::SLOTS) {
+            int t = MEDIUM ? 0 : gi;
+            int row = __shfl_sync(FULL, my_row, t & 31);
+            int e0 = __shfl_sync(FULL, my_e0, t & 31);
+            const int len0 = __shfl_sync(FULL, my_len, t & 31);
+            int len = t < nrows ? len0 : 0;
+            int s = 0;
+            T acc[R][W];
+            zero_acc<T, W, R>(acc);
+            int colc[Q];
+            T valc[Q];
+            load_entries<T, G, Q>(colc, valc, p.col_idx, p.values, e0 + goff, e0 + len, pol_s);
+
+            while (__any_sync(FULL, t < nrows)) {
+                const bool active = t < nrows;
+                // next position of this group, and its entries (prefetch)
+                int t2 = t, s2 = s + ESTEP;
+                if (s2 >= len) {
+                    t2 = t + TSTEP;
+                    s2 = 0;
+                }
+                const int row2 = __shfl_sync(FULL, my_row, t2 & 31);
+                const int e02 = __shfl_sync(FULL, my_e0, t2 & 31);
+                const int lraw = __shfl_sync(FULL, my_len, t2 & 31);
+                const int len2 = t2 < nrows ? lraw : 0;
+                int coln[Q];
+                T valn[Q];
+                load_entries<T, G, Q>(coln, valn, p.col_idx, p.values, e02 + s2 + goff,
+                                      e02 + len2, pol_s);
+
+                // consume the current step
+                const int cnt = active ? min(C::CH, len - s - goff) : 0;
+                const int cmax = MEDIUM ? min(C::CH, len - s)
+                                        : (int)__reduce_max_sync(FULL, (unsigned)max(cnt, 0));
+                consume_step<T, W, G, R>(acc, colc, valc, cnt, cmax, Bp, p.ldb, vbase, pw);
+
+                if (s + ESTEP >= len) {                     // row finished (uniform if MEDIUM)
+                    if (MEDIUM) {
+                        combine_groups<T, W, G, R>(acc);
+                        if (gi == 0 && active)
+                            write_row<T, W, G, R>(p.C + (int64_t)row * p.ldc + c0, acc, vbase, pw,
+                                                  p.alpha, p.beta, read_c);
+                    } else if (active) {
+                        write_row<T, W, G, R>(p.C + (int64_t)row * p.ldc + c0, acc, vbase, pw,
+                                              p.alpha, p.beta, read_c);
+                    }
+                    zero_acc<T, W, R>(acc);
+                }
+                t = t2;
+                s = s2;
+                row = row2;
+                e0 = e02;
+                len = len2;
+#pragma unroll
+                for (int q = 0; q < Q; ++q) {
+                    colc[q] = coln[q];
+                    valc[q] = valn[q];
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Short and medium rows.  Persistent launch: for each panel (in order), warp w
+// takes the w-th of nwarps equal contiguous ranges of the short list, then of
+// the medium list.
+// ---------------------------------------------------------------------------
+template <typename T, int W, int G, int R>
+__global__ void __launch_bounds__(ROWS_THREADS, SPMM_ROWS_MIN_BLOCKS)
+rows_kernel(SpmmParams<T> p) {
     const uint64_t pol_s = policy_evict_first();
     const int n_short = p.hdr[HDR_COUNT_SHORT];
     const int n_med = p.hdr[HDR_COUNT_MEDIUM];
-    const int64_t items_short = (n_short + C::RPW - 1) / C::RPW;
-    const int64_t items_panel = items_short + n_med;
-    const int64_t total = items_panel * p.npanels;
     const int64_t nwarps = (int64_t)gridDim.x * (ROWS_THREADS / 32);
+    const int64_t w = (int64_t)blockIdx.x * (ROWS_THREADS / 32) + (threadIdx.x >> 5);
     const bool read_c = p.beta != T(0);
-
-    for (int64_t it = (int64_t)blockIdx.x * (ROWS_THREADS / 32) + (threadIdx.x >> 5); it < total;
-         it += nwarps) {
-        const int panel = (int)(it / items_panel);
-        const int64_t item = it - (int64_t)panel * items_panel;
+    const int s0 = (int)(w * n_short / nwarps), s1 = (int)((w + 1) * n_short / nwarps);
+    const int m0 = (int)(w * n_med / nwarps), m1 = (int)((w + 1) * n_med / nwarps);
+    for (int panel = 0; panel < p.npanels; ++panel) {
         const int c0 = panel * p.panel_cols;
         const int pw = min(p.panel_cols, p.n - c0);
-        const int nvec = (pw + W - 1) / W;
-        const T* Bp = p.B + c0;
-        if (item < items_short) {
-            const int64_t idx = item * C::RPW + gi;
-            const int row = idx < n_short ? p.rowlist[idx] : -1;
-            int e0 = 0, len = 0;
-            if (row >= 0) {
-                e0 = p.row_ptr[row];
-                len = p.row_ptr[row + 1] - e0;
-            }
-            for (int vbase = 0; vbase < nvec; vbase += C::SLOTS) {
-                T acc[R][W];
+        if (s1 > s0)
+            process_rows<T, W, G, R, false>(p, p.rowlist, s0, s1, c0, pw, pol_s, read_c);
+        if (m1 > m0)
+            process_rows<T, W, G, R, true>(p, p.rowlist + n_short, m0, m1, c0, pw, pol_s, read_c);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Accumulate the entries [a, b) of one row, whole warp (groups interleaved as
+// in the medium-row mode), with the next step's entries prefetched.  The
+// caller combines the groups.
+// ---------------------------------------------------------------------------
+template <typename T, int W, int G, int R>
+__device__ __forceinline__ void accumulate_range(T (&acc)[R][W], const SpmmParams<T>& p, int a,
+                                                 int b, const T* __restrict__ Bp, int vbase,
+                                                 int pw, uint64_t pol_s) {
+    using C = Cfg<T, W, G, R>;
+    constexpr int Q = C::Q;
+    constexpr int ESTEP = C::RPW * C::CH;
+    const int gi = (threadIdx.x & 31) / G;
+    const int goff = gi * C::CH;
+    int colc[Q];
+    T valc[Q];
+    load_entries<T, G, Q>(colc, valc, p.col_idx, p.values, a + goff, b, pol_s);
+    for (int s = a; s < b; s += ESTEP) {
+        int coln[Q];
+        T valn[Q];
+        load_entries<T, G, Q>(coln, valn, p.col_idx, p.values, s + ESTEP + goff, b, pol_s);
+        const int cnt = min(C::CH, b - s - goff);
+        const int cmax = min(C::CH, b - s);
+        consume_step<T, W, G, R>(acc, colc, valc, cnt, cmax, Bp, p.ldb, vbase, pw);
 #pragma unroll
-                for (int r = 0; r < R; ++r)
-#pragma unroll
-                    for (int e = 0; e < W; ++e) acc[r][e] = T(0);
-                accumulate<T, W, G, R, false>(acc, p.col_idx, p.values, Bp, p.ldb, e0, len, vbase,
-                                              pw, pol_b, pol_s);
-                if (row >= 0)
-                    write_row<T, W, G, R>(p.C + (int64_t)row * p.ldc + c0, acc, vbase, pw,
-                                          p.alpha, p.beta, read_c);
-            }
-        } else {
-            const int row = p.rowlist[n_short + (item - items_short)];
-            const int e0 = p.row_ptr[row];
-            const int len = p.row_ptr[row + 1] - e0;
-            for (int vbase = 0; vbase < nvec; vbase += C::SLOTS) {
-                T acc[R][W];
-#pragma unroll
-                for (int r = 0; r < R; ++r)
-#pragma unroll
-                    for (int e = 0; e < W; ++e) acc[r][e] = T(0);
-                accumulate<T, W, G, R, true>(acc, p.col_idx, p.values, Bp, p.ldb, e0, len, vbase,
-                                             pw, pol_b, pol_s);
-                combine_groups<T, W, G, R>(acc);
-                if (gi == 0)
-                    write_row<T, W, G, R>(p.C + (int64_t)row * p.ldc + c0, acc, vbase, pw,
-                                          p.alpha, p.beta, read_c);
-            }
+        for (int q = 0; q < Q; ++q) {
+            colc[q] = coln[q];
+            valc[q] = valn[q];
         }
     }
 }
@@ -235,7 +321,6 @@ long_kernel(SpmmParams<T> p) {
     const int s1 = (int)min((int64_t)s0 + seg, (int64_t)total);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane & (G - 1), gi = lane / G;
-    const uint64_t pol_b = policy_evict_last();
     const uint64_t pol_s = policy_evict_first();
     const bool read_c = p.beta != T(0);
     const int* lrows = p.rowlist + p.hdr[HDR_COUNT_SHORT] + p.hdr[HDR_COUNT_MEDIUM];
@@ -267,12 +352,8 @@ long_kernel(SpmmParams<T> p) {
             const int slot = (r == r0) ? 0 : 1;
             for (int vbase = 0; vbase < nvec; vbase += C::SLOTS) {
                 T acc[R][W];
-#pragma unroll
-                for (int q = 0; q < R; ++q)
-#pragma unroll
-                    for (int e = 0; e < W; ++e) acc[q][e] = T(0);
-                accumulate<T, W, G, R, true>(acc, p.col_idx, p.values, Bp, p.ldb, wl, wh - wl,
-                                             vbase, pw, pol_b, pol_s);
+                zero_acc<T, W, R>(acc);
+                accumulate_range<T, W, G, R>(acc, p, wl, wh, Bp, vbase, pw, pol_s);
                 combine_groups<T, W, G, R>(acc);
                 if (gi == 0) {
 #pragma unroll

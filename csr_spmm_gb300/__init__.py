@@ -16,12 +16,13 @@ from __future__ import annotations
 from ._lib import (EXPORTED, SPMM_ERR_ALLOC, SPMM_ERR_CUDA, SPMM_ERR_DIMENSION_MISMATCH,
                    SPMM_ERR_INVALID_ARGUMENT, SPMM_ERR_INVALID_CSR, SPMM_ERR_NULL_POINTER,
                    SPMM_ERR_UNSUPPORTED_DEVICE, SPMM_OK, SpmmError, library, spmm_create,
-                   spmm_csr_check, spmm_csr_f32, spmm_csr_f64, spmm_destroy, spmm_get_profile,
+                   spmm_csr_check, spmm_csr_f32, spmm_csr_f32_noalloc, spmm_csr_f64,
+                   spmm_destroy, spmm_get_profile,
                    spmm_reserve, spmm_set_profiling, status_string)
 
 __all__ = ["Handle", "spmm", "csr_check", "SpmmError", "library", "spmm_create", "spmm_destroy",
            "spmm_reserve", "spmm_csr_f32", "spmm_csr_f64", "spmm_csr_check", "status_string",
-           "spmm_set_profiling", "spmm_get_profile", "EXPORTED"]
+           "spmm_set_profiling", "spmm_get_profile", "spmm_csr_f32_noalloc", "EXPORTED"]
 
 
 class Handle:

@@ -22,10 +22,12 @@ SPMM_ERR_UNSUPPORTED_DEVICE = 4
 SPMM_ERR_ALLOC = 5
 SPMM_ERR_CUDA = 6
 SPMM_ERR_INVALID_CSR = 7
+SPMM_ERR_TOO_LARGE = 8
 
 # every symbol include/csr_spmm.h declares
 EXPORTED = ("spmm_create", "spmm_destroy", "spmm_reserve", "spmm_csr_f32", "spmm_csr_f64",
-            "spmm_csr_check", "spmm_set_profiling", "spmm_get_profile", "spmm_status_string")
+            "spmm_csr_check", "spmm_set_profiling", "spmm_get_profile", "spmm_csr_f32_noalloc",
+            "spmm_status_string")
 
 
 class SpmmProfile(ctypes.Structure):
@@ -83,6 +85,9 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.spmm_set_profiling.restype = st
     lib.spmm_get_profile.argtypes = [vp, ctypes.POINTER(SpmmProfile)]
     lib.spmm_get_profile.restype = st
+    lib.spmm_csr_f32_noalloc.argtypes = [ctypes.c_float, vp, vp, vp, i64, i64, vp, i64, i64,
+                                         ctypes.c_float, vp, i64, vp]
+    lib.spmm_csr_f32_noalloc.restype = st
     lib.spmm_status_string.argtypes = [ctypes.c_int]
     lib.spmm_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -146,3 +151,14 @@ def spmm_get_profile(handle) -> dict:
     prof = SpmmProfile()
     _check(library().spmm_get_profile(handle, ctypes.byref(prof)), "spmm_get_profile")
     return prof.as_dict()
+
+
+def spmm_csr_f32_noalloc(alpha, row_ptr, col_idx, values, m, k, B, ldb, n, beta, C, ldc,
+                         stream=0, check=True) -> int:
+    """The handle-free binary32 product whose scratch is a fixed device array
+    inside the library (for callers that cannot allocate device memory)."""
+    s = library().spmm_csr_f32_noalloc(float(alpha), row_ptr, col_idx, values, m, k, B, ldb, n,
+                                       float(beta), C, ldc, stream or None)
+    if check:
+        _check(s, "spmm_csr_f32_noalloc")
+    return s

@@ -432,6 +432,8 @@ const char* spmm_status_string(spmm_status_t s) {
         case SPMM_ERR_ALLOC: return "SPMM_ERR_ALLOC: scratch allocation failed";
         case SPMM_ERR_CUDA: return "SPMM_ERR_CUDA: CUDA runtime or launch error";
         case SPMM_ERR_INVALID_CSR: return "SPMM_ERR_INVALID_CSR: malformed CSR structure";
+        case SPMM_ERR_TOO_LARGE:
+            return "SPMM_ERR_TOO_LARGE: m or n beyond the static scratch of spmm_csr_f32_noalloc";
     }
     return "unknown spmm status";
 }

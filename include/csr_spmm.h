@@ -64,7 +64,8 @@ typedef enum {
     SPMM_ERR_UNSUPPORTED_DEVICE = 4, /* device is not compute capability 10.x / sm_103 family */
     SPMM_ERR_ALLOC = 5,              /* scratch allocation failed */
     SPMM_ERR_CUDA = 6,               /* a CUDA runtime call or kernel launch failed */
-    SPMM_ERR_INVALID_CSR = 7         /* spmm_csr_check found a malformed CSR structure */
+    SPMM_ERR_INVALID_CSR = 7,        /* spmm_csr_check found a malformed CSR structure */
+    SPMM_ERR_TOO_LARGE = 8           /* beyond the fixed limits of spmm_csr_f32_noalloc */
 } spmm_status_t;
 
 typedef struct spmm_handle_s *spmm_handle_t;
@@ -145,6 +146,34 @@ spmm_status_t spmm_set_profiling(spmm_handle_t h, int enable);
  * profiled product has been issued.  Only the epilogue-only path ran when
  * launches == 1 and rows_ms == 0. */
 spmm_status_t spmm_get_profile(spmm_handle_t h, spmm_profile_t *out);
+
+/* C = alpha * A * B + beta * C in binary32 without allocating anything.
+ *
+ * For callers that cannot call cudaMalloc: code running under a fixed or
+ * capped memory budget, inside an allocator or a host framework that owns all
+ * device memory, or on a path that must never stall on an allocation.  The
+ * reference pages have no counterpart; this is an addition of this library.
+ *
+ * Same operation, conventions, arguments (minus the handle) and results as
+ * spmm_csr_f32, on the same kernels.  The scratch they need (row bins, long-row
+ * partial sums) is one fixed device array inside the library, about 5.5 MB,
+ * held by every GPU that loads the library until the process exits.  Limits:
+ * m <= 524288 and n <= 512; larger products return SPMM_ERR_TOO_LARGE and do
+ * nothing.  The call never calls cudaMalloc, cudaFree or any allocating
+ * routine.
+ *
+ * The first call on a device (with that device current) looks up the array's
+ * device address and the device's SM count and L2 size; make that first call
+ * before capturing any stream into a CUDA graph.  Every call on a device shares
+ * the one array, which keeps the last call's contents: calls whose work
+ * overlaps on the GPU (different streams, or different host threads) race and
+ * must be serialised by the caller.  Nothing in the array needs to start at
+ * zero.  Asynchronous on `stream`, like spmm_csr_f32. */
+spmm_status_t spmm_csr_f32_noalloc(float alpha,
+                                   const int32_t *row_ptr, const int32_t *col_idx,
+                                   const float *values, int64_t m, int64_t k,
+                                   const float *B, int64_t ldb, int64_t n,
+                                   float beta, float *C, int64_t ldc, void *stream);
 
 /* Static, human-readable name of a status code (never NULL). */
 const char *spmm_status_string(spmm_status_t s);

@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in range(8):
+    for code in range(9):
         s = cs.status_string(code)
         assert s.startswith("SPMM_")
     assert "unknown" in cs.status_string(99)

@@ -48,7 +48,7 @@ constexpr double PANEL_TRIGGER = SPMM_PANEL_TRIGGER;
 // Rows at least this long go to the CTA-split kernel.
 constexpr int LONG_MIN_ROW = 1024;
 // Long-row grid: CTAs per SM.
-constexpr int LONG_CTAS_PER_SM = 2;
+constexpr int LONG_CTAS_PER_SM = 4;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -59,7 +59,7 @@ inline int next_pow2(int x) {
 }
 
 struct ScratchLayout {
-    size_t hdr, tile_counts, tile_offsets, rowlist, long_pre, partials, total;
+    size_t hdr, tile_counts, tile_offsets, rowlist, med_pre, long_pre, partials, total;
 };
 
 ScratchLayout layout_for(int64_t m, int64_t n, int es, int long_grid) {
@@ -67,9 +67,10 @@ ScratchLayout layout_for(int64_t m, int64_t n, int es, int long_grid) {
     const int64_t tiles = (m + BIN_TILE - 1) / BIN_TILE;
     size_t off = 0;
     L.hdr = off;          off = align_up(off + sizeof(int) * HDR_WORDS, 256);
-    L.tile_counts = off;  off = align_up(off + sizeof(int) * 4 * (size_t)std::max<int64_t>(tiles, 1), 256);
-    L.tile_offsets = off; off = align_up(off + sizeof(int) * 4 * (size_t)std::max<int64_t>(tiles, 1), 256);
+    L.tile_counts = off;  off = align_up(off + sizeof(int) * BIN_REC * (size_t)std::max<int64_t>(tiles, 1), 256);
+    L.tile_offsets = off; off = align_up(off + sizeof(int) * BIN_REC * (size_t)std::max<int64_t>(tiles, 1), 256);
     L.rowlist = off;      off = align_up(off + sizeof(int) * (size_t)std::max<int64_t>(m, 1), 256);
+    L.med_pre = off;      off = align_up(off + sizeof(int) * (size_t)(m + 1), 256);
     L.long_pre = off;     off = align_up(off + sizeof(int) * (size_t)(m + 1), 256);
     L.partials = off;     off = align_up(off + (size_t)es * 2 * long_grid * (size_t)std::max<int64_t>(n, 1), 256);
     L.total = off;
@@ -141,7 +142,8 @@ Plan make_plan(const spmm_handle_s* h, int64_t k, int64_t n, const T* B, int64_t
     }
     // bin thresholds
     const int bytes_per_entry = P.geo.R * W * es;
-    const int U = std::min(SPMM_BATCH_MAX, std::max(1, SPMM_BATCH_BYTES / bytes_per_entry));
+    const int batch_bytes = es == 8 ? SPMM_BATCH_BYTES_F64 : SPMM_BATCH_BYTES;
+    const int U = std::min(SPMM_BATCH_MAX, std::max(1, batch_bytes / bytes_per_entry));
     const int CH = std::max(P.geo.G, U);
     P.long_min = LONG_MIN_ROW;
     P.short_max = (P.geo.G == 32) ? P.long_min - 1 : std::min(P.long_min - 1, 2 * CH);
@@ -212,6 +214,7 @@ spmm_status_t spmm_csr_impl(spmm_handle_t h, T alpha, const int32_t* row_ptr,
     bs.tile_counts = reinterpret_cast<int*>(base + L.tile_counts);
     bs.tile_offsets = reinterpret_cast<int*>(base + L.tile_offsets);
     bs.rowlist = reinterpret_cast<int*>(base + L.rowlist);
+    bs.med_pre = reinterpret_cast<int*>(base + L.med_pre);
     bs.long_pre = reinterpret_cast<int*>(base + L.long_pre);
     bs.tiles = (int)((m + BIN_TILE - 1) / BIN_TILE);
 
@@ -235,6 +238,7 @@ spmm_status_t spmm_csr_impl(spmm_handle_t h, T alpha, const int32_t* row_ptr,
     p.panel_cols = P.panel_cols;
     p.npanels = P.npanels;
     p.rowlist = bs.rowlist;
+    p.med_pre = bs.med_pre;
     p.long_pre = bs.long_pre;
     p.hdr = bs.hdr;
     p.partials = reinterpret_cast<T*>(base + L.partials);

@@ -1,18 +1,23 @@
 // Row-binning pre-pass: a stable partition of the rows of A by length into
-// short / medium / long lists, plus the exclusive prefix of long-row lengths
-// that the long-row CTA split works from.
+// short / medium / long lists, plus the exclusive prefix of the medium-row and
+// long-row lengths (the medium prefix balances medium rows across warps by
+// entries; the long prefix drives the long-row CTA split).
 //
-// Three launches, all reading row_ptr only:
-//   bin_count   per 2048-row tile: rows per bin and entries in long rows
-//   bin_scan    one CTA: exclusive scans of the tile counts, bin totals
+// Reads row_ptr only.  For m <= 2048 (one tile) a single CTA does everything
+// in one launch; otherwise three launches:
+//   bin_count   per 2048-row tile: rows per bin, entries in medium and long rows
+//   bin_scan    one CTA: exclusive scans of the tile records, bin totals
 //   bin_scatter per tile: stable ranks (warp ballots + per-warp prefix),
-//               writes rowlist and long_pre
+//               writes rowlist, med_pre and long_pre
 // Ranks come from ballots in ascending row order, never from atomics, so the
 // lists (and everything computed from them) are identical on every call.
 #include "spmm_internal.h"
 
 namespace spmm {
 namespace {
+
+// tile record words
+enum { R_SHORT = 0, R_MED = 1, R_LONG = 2, R_LONG_NNZ = 3, R_MED_NNZ = 4, R_USED = 5 };
 
 __device__ __forceinline__ int classify(int len, int short_max, int long_min) {
     return len <= short_max ? BIN_SHORT : (len < long_min ? BIN_MEDIUM : BIN_LONG);
@@ -22,120 +27,50 @@ __device__ __forceinline__ int row_len(const int* row_ptr, int row, int m) {
     return row < m ? __ldg(row_ptr + row + 1) - __ldg(row_ptr + row) : -1;
 }
 
-__global__ void __launch_bounds__(BIN_THREADS)
-bin_count_kernel(const int* __restrict__ row_ptr, int m, int short_max, int long_min,
-                 int* __restrict__ tile_counts) {
-    __shared__ int s_cnt[4];
-    if (threadIdx.x < 4) s_cnt[threadIdx.x] = 0;
-    __syncthreads();
-    const int lane = threadIdx.x & 31;
-    int c[3] = {0, 0, 0};
-    int long_nnz = 0;
-    const int base = blockIdx.x * BIN_TILE;
+// Per-warp totals of one tile's record into s_part[warp][word]; the caller
+// synchronises and adds the warps in order (tile_total).
+__device__ __forceinline__ void tile_record(const int* __restrict__ row_ptr, int m, int short_max,
+                                            int long_min, int tile, int (*s_part)[R_USED]) {
+    int c[R_USED] = {0, 0, 0, 0, 0};
+    const int base = tile * BIN_TILE;
 #pragma unroll
     for (int j = 0; j < BIN_ITEMS; ++j) {
         const int row = base + j * BIN_THREADS + threadIdx.x;
         const int len = row_len(row_ptr, row, m);
-        if (len >= 0) {
-            const int b = classify(len, short_max, long_min);
-            c[b] += 1;
-            if (b == BIN_LONG) long_nnz += len;
-        }
+        const int b = len >= 0 ? classify(len, short_max, long_min) : -1;
+        c[R_SHORT] += b == BIN_SHORT;
+        c[R_MED] += b == BIN_MEDIUM;
+        c[R_LONG] += b == BIN_LONG;
+        c[R_LONG_NNZ] += b == BIN_LONG ? len : 0;
+        c[R_MED_NNZ] += b == BIN_MEDIUM ? len : 0;
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        c[0] += __shfl_xor_sync(FULL, c[0], off);
-        c[1] += __shfl_xor_sync(FULL, c[1], off);
-        c[2] += __shfl_xor_sync(FULL, c[2], off);
-        long_nnz += __shfl_xor_sync(FULL, long_nnz, off);
-    }
-    if (lane == 0) {
-        atomicAdd(&s_cnt[0], c[0]);   // integer counts: order-independent
-        atomicAdd(&s_cnt[1], c[1]);
-        atomicAdd(&s_cnt[2], c[2]);
-        atomicAdd(&s_cnt[3], long_nnz);
-    }
-    __syncthreads();
-    if (threadIdx.x < 4) tile_counts[blockIdx.x * 4 + threadIdx.x] = s_cnt[threadIdx.x];
+    for (int w = 0; w < R_USED; ++w)
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) c[w] += __shfl_xor_sync(FULL, c[w], off);
+    if ((threadIdx.x & 31) == 0)
+#pragma unroll
+        for (int w = 0; w < R_USED; ++w) s_part[threadIdx.x >> 5][w] = c[w];
 }
 
-// Exclusive scan of the 4-word tile records over all tiles, by one CTA.
-constexpr int SCAN_THREADS = 1024;
-
-__global__ void __launch_bounds__(SCAN_THREADS)
-bin_scan_kernel(const int* __restrict__ tile_counts, int tiles, int* __restrict__ tile_offsets,
-                int* __restrict__ hdr, int* __restrict__ long_pre) {
-    __shared__ int s_warp[32][4];
-    __shared__ int s_carry[4];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (threadIdx.x < 4) s_carry[threadIdx.x] = 0;
-    __syncthreads();
-    for (int t0 = 0; t0 < tiles; t0 += SCAN_THREADS) {
-        const int t = t0 + threadIdx.x;
-        int v[4];
+__device__ __forceinline__ int tile_total(const int (*s_part)[R_USED], int word) {
+    int t = 0;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) v[c] = t < tiles ? tile_counts[t * 4 + c] : 0;
-        int incl[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            int x = v[c];
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                int y = __shfl_up_sync(FULL, x, off);
-                if (lane >= off) x += y;
-            }
-            incl[c] = x;
-            if (lane == 31) s_warp[warp][c] = x;
-        }
-        __syncthreads();
-        if (warp == 0) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                int x = s_warp[lane][c];
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    int y = __shfl_up_sync(FULL, x, off);
-                    if (lane >= off) x += y;
-                }
-                s_warp[lane][c] = x;   // inclusive over warps
-            }
-        }
-        __syncthreads();
-        int carry_next[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int warp_excl = warp > 0 ? s_warp[warp - 1][c] : 0;
-            const int excl = s_carry[c] + warp_excl + incl[c] - v[c];
-            if (t < tiles) tile_offsets[t * 4 + c] = excl;
-            carry_next[c] = s_carry[c] + s_warp[31][c];
-        }
-        __syncthreads();
-        if (threadIdx.x < 4) s_carry[threadIdx.x] = carry_next[threadIdx.x];
-        __syncthreads();
-    }
-    if (threadIdx.x == 0) {
-        hdr[HDR_COUNT_SHORT] = s_carry[0];
-        hdr[HDR_COUNT_MEDIUM] = s_carry[1];
-        hdr[HDR_COUNT_LONG] = s_carry[2];
-        hdr[HDR_LONG_NNZ] = s_carry[3];
-        long_pre[s_carry[2]] = s_carry[3];     // closing entry of the prefix
-    }
+    for (int w = 0; w < BIN_THREADS / 32; ++w) t += s_part[w][word];
+    return t;
 }
 
-__global__ void __launch_bounds__(BIN_THREADS)
-bin_scatter_kernel(const int* __restrict__ row_ptr, int m, int short_max, int long_min,
-                   const int* __restrict__ tile_offsets, const int* __restrict__ hdr,
-                   int* __restrict__ rowlist, int* __restrict__ long_pre) {
+// Stable scatter of one tile.  run[] holds the tile's offsets within each bin
+// (and within the medium / long length prefixes); bin_base the list offsets.
+__device__ __forceinline__ void tile_scatter(const int* __restrict__ row_ptr, int m, int short_max,
+                                             int long_min, int tile, int (&run)[R_USED],
+                                             const int (&bin_base)[3], int* __restrict__ rowlist,
+                                             int* __restrict__ med_pre, int* __restrict__ long_pre,
+                                             int (*s_wc)[R_USED]) {
     constexpr int NW = BIN_THREADS / 32;
-    __shared__ int s_wc[NW][4];            // per warp: counts of the 3 bins + long nnz
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const unsigned lt_mask = (1u << lane) - 1u;
-    const int base = blockIdx.x * BIN_TILE;
-    int run[4];                            // running tile-local offsets
-#pragma unroll
-    for (int c = 0; c < 4; ++c) run[c] = tile_offsets[blockIdx.x * 4 + c];
-    const int bin_base[3] = {0, hdr[HDR_COUNT_SHORT], hdr[HDR_COUNT_SHORT] + hdr[HDR_COUNT_MEDIUM]};
-
+    const int base = tile * BIN_TILE;
     for (int j = 0; j < BIN_ITEMS; ++j) {
         const int row = base + j * BIN_THREADS + threadIdx.x;
         const int len = row_len(row_ptr, row, m);
@@ -147,26 +82,32 @@ bin_scatter_kernel(const int* __restrict__ row_ptr, int m, int short_max, int lo
             mask[c] = __ballot_sync(FULL, b == c);
             rank[c] = __popc(mask[c] & lt_mask);
         }
-        // inclusive warp scan of long-row lengths
+        // inclusive warp scans of long-row and medium-row lengths
         const int llen = b == BIN_LONG ? len : 0;
-        int lincl = llen;
+        const int mlen = b == BIN_MEDIUM ? len : 0;
+        int lincl = llen, mincl = mlen;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            int y = __shfl_up_sync(FULL, lincl, off);
-            if (lane >= off) lincl += y;
+            const int y = __shfl_up_sync(FULL, lincl, off);
+            const int z = __shfl_up_sync(FULL, mincl, off);
+            if (lane >= off) {
+                lincl += y;
+                mincl += z;
+            }
         }
         if (lane == 31) {
-            s_wc[warp][0] = __popc(mask[0]);
-            s_wc[warp][1] = __popc(mask[1]);
-            s_wc[warp][2] = __popc(mask[2]);
-            s_wc[warp][3] = lincl;
+            s_wc[warp][R_SHORT] = __popc(mask[0]);
+            s_wc[warp][R_MED] = __popc(mask[1]);
+            s_wc[warp][R_LONG] = __popc(mask[2]);
+            s_wc[warp][R_LONG_NNZ] = lincl;
+            s_wc[warp][R_MED_NNZ] = mincl;
         }
         __syncthreads();
-        int wpre[4] = {0, 0, 0, 0}, tot[4] = {0, 0, 0, 0};
+        int wpre[R_USED] = {0, 0, 0, 0, 0}, tot[R_USED] = {0, 0, 0, 0, 0};
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < R_USED; ++c) {
                 const int x = s_wc[w][c];
                 if (w < warp) wpre[c] += x;
                 tot[c] += x;
@@ -175,12 +116,127 @@ bin_scatter_kernel(const int* __restrict__ row_ptr, int m, int short_max, int lo
         if (b >= 0) {
             const int pos_in_bin = run[b] + wpre[b] + rank[b];
             rowlist[bin_base[b] + pos_in_bin] = row;
-            if (b == BIN_LONG) long_pre[pos_in_bin] = run[3] + wpre[3] + lincl - llen;
+            if (b == BIN_LONG) long_pre[pos_in_bin] = run[R_LONG_NNZ] + wpre[R_LONG_NNZ] + lincl - llen;
+            if (b == BIN_MEDIUM) med_pre[pos_in_bin] = run[R_MED_NNZ] + wpre[R_MED_NNZ] + mincl - mlen;
         }
 #pragma unroll
-        for (int c = 0; c < 4; ++c) run[c] += tot[c];
+        for (int c = 0; c < R_USED; ++c) run[c] += tot[c];
         __syncthreads();   // s_wc is rewritten by the next sub-tile
     }
+}
+
+__device__ __forceinline__ void write_header(const int (&total)[R_USED], int* __restrict__ hdr,
+                                             int* __restrict__ med_pre, int* __restrict__ long_pre) {
+    hdr[HDR_COUNT_SHORT] = total[R_SHORT];
+    hdr[HDR_COUNT_MEDIUM] = total[R_MED];
+    hdr[HDR_COUNT_LONG] = total[R_LONG];
+    hdr[HDR_LONG_NNZ] = total[R_LONG_NNZ];
+    hdr[HDR_MED_NNZ] = total[R_MED_NNZ];
+    long_pre[total[R_LONG]] = total[R_LONG_NNZ];   // closing entries of the prefixes
+    med_pre[total[R_MED]] = total[R_MED_NNZ];
+}
+
+// ---- one tile (m <= BIN_TILE): the whole pre-pass in one CTA ----
+__global__ void __launch_bounds__(BIN_THREADS)
+bin_single_kernel(const int* __restrict__ row_ptr, int m, int short_max, int long_min,
+                  int* __restrict__ hdr, int* __restrict__ rowlist, int* __restrict__ med_pre,
+                  int* __restrict__ long_pre) {
+    __shared__ int s_part[BIN_THREADS / 32][R_USED];
+    __shared__ int s_wc[BIN_THREADS / 32][R_USED];
+    tile_record(row_ptr, m, short_max, long_min, 0, s_part);
+    __syncthreads();
+    int total[R_USED];
+#pragma unroll
+    for (int c = 0; c < R_USED; ++c) total[c] = tile_total(s_part, c);
+    if (threadIdx.x == 0) write_header(total, hdr, med_pre, long_pre);
+    int run[R_USED] = {0, 0, 0, 0, 0};
+    const int bin_base[3] = {0, total[R_SHORT], total[R_SHORT] + total[R_MED]};
+    tile_scatter(row_ptr, m, short_max, long_min, 0, run, bin_base, rowlist, med_pre, long_pre,
+                 s_wc);
+}
+
+// ---- many tiles ----
+__global__ void __launch_bounds__(BIN_THREADS)
+bin_count_kernel(const int* __restrict__ row_ptr, int m, int short_max, int long_min,
+                 int* __restrict__ tile_counts) {
+    __shared__ int s_part[BIN_THREADS / 32][R_USED];
+    tile_record(row_ptr, m, short_max, long_min, blockIdx.x, s_part);
+    __syncthreads();
+    if (threadIdx.x < BIN_REC) tile_counts[blockIdx.x * BIN_REC + threadIdx.x] =
+        threadIdx.x < R_USED ? tile_total(s_part, threadIdx.x) : 0;
+}
+
+// Exclusive scan of the tile records over all tiles, by one CTA.
+constexpr int SCAN_THREADS = 1024;
+
+__global__ void __launch_bounds__(SCAN_THREADS)
+bin_scan_kernel(const int* __restrict__ tile_counts, int tiles, int* __restrict__ tile_offsets,
+                int* __restrict__ hdr, int* __restrict__ med_pre, int* __restrict__ long_pre) {
+    __shared__ int s_warp[32][R_USED];
+    __shared__ int s_carry[R_USED];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x < R_USED) s_carry[threadIdx.x] = 0;
+    __syncthreads();
+    for (int t0 = 0; t0 < tiles; t0 += SCAN_THREADS) {
+        const int t = t0 + threadIdx.x;
+        int v[R_USED], incl[R_USED];
+#pragma unroll
+        for (int c = 0; c < R_USED; ++c) {
+            v[c] = t < tiles ? tile_counts[t * BIN_REC + c] : 0;
+            int x = v[c];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(FULL, x, off);
+                if (lane >= off) x += y;
+            }
+            incl[c] = x;
+            if (lane == 31) s_warp[warp][c] = x;
+        }
+        __syncthreads();
+        if (warp == 0) {
+#pragma unroll
+            for (int c = 0; c < R_USED; ++c) {
+                int x = s_warp[lane][c];
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int y = __shfl_up_sync(FULL, x, off);
+                    if (lane >= off) x += y;
+                }
+                s_warp[lane][c] = x;   // inclusive over warps
+            }
+        }
+        __syncthreads();
+        int carry_next[R_USED];
+#pragma unroll
+        for (int c = 0; c < R_USED; ++c) {
+            const int warp_excl = warp > 0 ? s_warp[warp - 1][c] : 0;
+            if (t < tiles) tile_offsets[t * BIN_REC + c] = s_carry[c] + warp_excl + incl[c] - v[c];
+            carry_next[c] = s_carry[c] + s_warp[31][c];
+        }
+        __syncthreads();
+        if (threadIdx.x < R_USED) s_carry[threadIdx.x] = carry_next[threadIdx.x];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        int total[R_USED];
+#pragma unroll
+        for (int c = 0; c < R_USED; ++c) total[c] = s_carry[c];
+        write_header(total, hdr, med_pre, long_pre);
+    }
+}
+
+__global__ void __launch_bounds__(BIN_THREADS)
+bin_scatter_kernel(const int* __restrict__ row_ptr, int m, int short_max, int long_min,
+                   const int* __restrict__ tile_offsets, const int* __restrict__ hdr,
+                   int* __restrict__ rowlist, int* __restrict__ med_pre,
+                   int* __restrict__ long_pre) {
+    __shared__ int s_wc[BIN_THREADS / 32][R_USED];
+    int run[R_USED];
+#pragma unroll
+    for (int c = 0; c < R_USED; ++c) run[c] = tile_offsets[blockIdx.x * BIN_REC + c];
+    const int bin_base[3] = {0, hdr[HDR_COUNT_SHORT], hdr[HDR_COUNT_SHORT] + hdr[HDR_COUNT_MEDIUM]};
+    tile_scatter(row_ptr, m, short_max, long_min, blockIdx.x, run, bin_base, rowlist, med_pre,
+                 long_pre, s_wc);
 }
 
 }  // namespace
@@ -188,13 +244,18 @@ bin_scatter_kernel(const int* __restrict__ row_ptr, int m, int short_max, int lo
 cudaError_t launch_binning(const int* row_ptr, int m, int short_max, int long_min,
                            const BinScratch& s, cudaStream_t st) {
     if (m <= 0) return cudaSuccess;
+    if (s.tiles == 1) {
+        bin_single_kernel<<<1, BIN_THREADS, 0, st>>>(row_ptr, m, short_max, long_min, s.hdr,
+                                                     s.rowlist, s.med_pre, s.long_pre);
+        return cudaGetLastError();
+    }
     bin_count_kernel<<<s.tiles, BIN_THREADS, 0, st>>>(row_ptr, m, short_max, long_min,
                                                       s.tile_counts);
     bin_scan_kernel<<<1, SCAN_THREADS, 0, st>>>(s.tile_counts, s.tiles, s.tile_offsets, s.hdr,
-                                                s.long_pre);
+                                                s.med_pre, s.long_pre);
     bin_scatter_kernel<<<s.tiles, BIN_THREADS, 0, st>>>(row_ptr, m, short_max, long_min,
                                                         s.tile_offsets, s.hdr, s.rowlist,
-                                                        s.long_pre);
+                                                        s.med_pre, s.long_pre);
     return cudaGetLastError();
 }
 

@@ -141,4 +141,49 @@ __device__ __forceinline__ void store_c(T* c, int cnt, const T (&acc)[W], T alph
     }
 }
 
+// C elements [0, cnt) of a vector slot, streaming load (the rest stay zero).
+template <typename T, int W>
+__device__ __forceinline__ void load_c(const T* c, int cnt, T (&v)[W]) {
+    if (cnt == W && (W * sizeof(T)) % 16 == 0) {
+        constexpr int PER = 16 / sizeof(T);
+#pragma unroll
+        for (int h = 0; h < W; h += PER) {
+            if constexpr (sizeof(T) == 4) {
+                const float4 x = __ldcs(reinterpret_cast<const float4*>(c + h));
+                v[h] = x.x; v[h + 1] = x.y; v[h + 2] = x.z; v[h + 3] = x.w;
+            } else {
+                const double2 x = __ldcs(reinterpret_cast<const double2*>(c + h));
+                v[h] = x.x; v[h + 1] = x.y;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < W; ++e)
+            if (e < cnt) v[e] = __ldcs(c + e);
+    }
+}
+
+// C = alpha * acc + beta * c0 with c0 already loaded.
+template <typename T, int W>
+__device__ __forceinline__ void store_c_pre(T* c, int cnt, const T (&acc)[W], const T (&c0)[W],
+                                            T alpha, T beta) {
+    T o[W];
+#pragma unroll
+    for (int e = 0; e < W; ++e) o[e] = epi<T>(alpha, acc[e], beta, c0[e]);
+    if (cnt == W && (W * sizeof(T)) % 16 == 0) {
+        constexpr int PER = 16 / sizeof(T);
+#pragma unroll
+        for (int h = 0; h < W; h += PER) {
+            if constexpr (sizeof(T) == 4)
+                __stcs(reinterpret_cast<float4*>(c + h), make_float4(o[h], o[h + 1], o[h + 2], o[h + 3]));
+            else
+                __stcs(reinterpret_cast<double2*>(c + h), make_double2(o[h], o[h + 1]));
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < W; ++e)
+            if (e < cnt) __stcs(c + e, o[e]);
+    }
+}
+
 }  // namespace spmm

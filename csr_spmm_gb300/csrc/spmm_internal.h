@@ -21,6 +21,7 @@ enum HeaderWord {
     HDR_COUNT_MEDIUM = 1,
     HDR_COUNT_LONG = 2,
     HDR_LONG_NNZ = 3,   // total entries in long rows
+    HDR_MED_NNZ = 4,    // total entries in medium rows
     HDR_WORDS = 8
 };
 
@@ -28,9 +29,10 @@ enum HeaderWord {
 constexpr int BIN_THREADS = 256;
 constexpr int BIN_ITEMS = 8;
 constexpr int BIN_TILE = BIN_THREADS * BIN_ITEMS;
+constexpr int BIN_REC = 8;    // int32 words per tile record
 
 // Long-row kernel geometry.
-constexpr int LONG_THREADS = 512;
+constexpr int LONG_THREADS = 256;
 constexpr int LONG_WARPS = LONG_THREADS / 32;
 constexpr int LONG_MIN_SEGMENT = 2048;   // smallest per-CTA share of long-row entries
 
@@ -39,9 +41,18 @@ constexpr int ROWS_THREADS = 256;
 #ifndef SPMM_ROWS_MIN_BLOCKS
 #define SPMM_ROWS_MIN_BLOCKS 4
 #endif
+#ifndef SPMM_ROWS_MIN_BLOCKS_F64
+#define SPMM_ROWS_MIN_BLOCKS_F64 6
+#endif
 // B bytes each lane keeps in flight per gather batch, and the batch cap.
 #ifndef SPMM_BATCH_BYTES
 #define SPMM_BATCH_BYTES 64
+#endif
+#ifndef SPMM_BATCH_BYTES_F64
+#define SPMM_BATCH_BYTES_F64 16
+#endif
+#ifndef SPMM_LONG_MIN_BLOCKS
+#define SPMM_LONG_MIN_BLOCKS 4
 #endif
 #ifndef SPMM_BATCH_MAX
 #define SPMM_BATCH_MAX 8
@@ -49,9 +60,10 @@ constexpr int ROWS_THREADS = 256;
 
 struct BinScratch {
     int* rowlist;       // [m]  short rows, then medium rows, then long rows (each ascending)
+    int* med_pre;       // [m + 1] exclusive prefix of medium-row lengths (stable order)
     int* long_pre;      // [m + 1] exclusive prefix of long-row lengths (stable order)
-    int* tile_counts;   // [tiles * 4]  per tile: short, medium, long counts, long nnz
-    int* tile_offsets;  // [tiles * 4]  exclusive scans of the above over tiles
+    int* tile_counts;   // [tiles * BIN_REC] per tile: bin counts, long nnz, medium nnz
+    int* tile_offsets;  // [tiles * BIN_REC] exclusive scans of the above over tiles
     int* hdr;           // [HDR_WORDS]
     int tiles;
 };
@@ -73,6 +85,7 @@ struct SpmmParams {
     int npanels;
     // bins
     const int* rowlist;
+    const int* med_pre;
     const int* long_pre;
     const int* hdr;
     // long-row partial sums: [2 * long_grid, n]

@@ -35,7 +35,8 @@ struct Cfg {
     static_assert(G >= 1 && G <= 32 && (G & (G - 1)) == 0, "G must be a power of two <= 32");
     static constexpr int SLOTS = G * R;                       // vectors per column pass
     static constexpr int BYTES_PER_ENTRY = R * W * (int)sizeof(T);
-    static constexpr int U0 = SPMM_BATCH_BYTES / BYTES_PER_ENTRY;   // B bytes in flight/lane
+    static constexpr int BATCH_BYTES = sizeof(T) == 8 ? SPMM_BATCH_BYTES_F64 : SPMM_BATCH_BYTES;
+    static constexpr int U0 = BATCH_BYTES / BYTES_PER_ENTRY;        // B bytes in flight/lane
     static constexpr int U = U0 < 1 ? 1 : (U0 > SPMM_BATCH_MAX ? SPMM_BATCH_MAX : U0);
     static constexpr int CH = G > U ? G : U;                  // entries per group per step
     static constexpr int Q = CH / G;                          // (col, value) loads per lane per step
@@ -136,6 +137,33 @@ __device__ __forceinline__ void write_row(T* __restrict__ Crow, const T (&acc)[R
     }
 }
 
+// The C row a lane group will update (beta != 0), loaded when the group
+// starts the row so that the load overlaps the row's gathers.
+template <typename T, int W, int G, int R>
+__device__ __forceinline__ void load_c_row(T (&c0)[R][W], const T* __restrict__ Crow, int vbase,
+                                           int pw) {
+    const int g = (threadIdx.x & 31) & (G - 1);
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int col = (vbase + g + G * r) * W;
+#pragma unroll
+        for (int e = 0; e < W; ++e) c0[r][e] = T(0);
+        if (col < pw) load_c<T, W>(Crow + col, min(W, pw - col), c0[r]);
+    }
+}
+
+template <typename T, int W, int G, int R>
+__device__ __forceinline__ void write_row_c0(T* __restrict__ Crow, const T (&acc)[R][W],
+                                             const T (&c0)[R][W], int vbase, int pw, T alpha,
+                                             T beta) {
+    const int g = (threadIdx.x & 31) & (G - 1);
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int col = (vbase + g + G * r) * W;
+        if (col < pw) store_c_pre<T, W>(Crow + col, min(W, pw - col), acc[r], c0[r], alpha, beta);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // A warp works through rows list[r0 .. r1) of one bin, for the panel of pw
 // columns starting at c0.
@@ -145,10 +173,9 @@ __device__ __forceinline__ void write_row(T* __restrict__ Crow, const T (&acc)[R
 //     group gi takes entries [s + gi*CH, s + gi*CH + CH) of each warp step of
 //     RPW*CH entries, and the groups are combined at the end of the row.
 // ---------------------------------------------------------------------------
-template <typename T, int W, int G, int R, bool MEDIUM>
+template <typename T, int W, int G, int R, bool MEDIUM, bool READ_C>
 __device__ __forceinline__ void process_rows(const SpmmParams<T>& p, const int* __restrict__ list,
-                                             int r0, int r1, int c0, int pw, uint64_t pol_s,
-                                             bool read_c) {
+                                             int r0, int r1, int c0col, int pw, uint64_t pol_s) {
     using C = Cfg<T, W, G, R>;
     constexpr int Q = C::Q;
     const int lane = threadIdx.x & 31;
@@ -157,7 +184,7 @@ __device__ __forceinline__ void process_rows(const SpmmParams<T>& p, const int* 
     constexpr int ESTEP = MEDIUM ? C::RPW * C::CH : C::CH;  // entry advance per step
     const int goff = MEDIUM ? gi * C::CH : 0;
     const int nvec = (pw + W - 1) / W;
-    const T* Bp = p.B + c0;
+    const T* Bp = p.B + c0col;
 
     for (int sub = r0; sub < r1; sub += 32) {
         const int nrows = min(32, r1 - sub);
@@ -176,6 +203,11 @@ __device__ __forceinline__ void process_rows(const SpmmParams<T>& p, const int* 
             int s = 0;
             T acc[R][W];
             zero_acc<T, W, R>(acc);
+            T c0[R][W];
+            zero_acc<T, W, R>(c0);
+            const bool loads_c = READ_C && (!MEDIUM || gi == 0);
+            if (loads_c && t < nrows)
+                load_c_row<T, W, G, R>(c0, p.C + (int64_t)row * p.ldc + c0col, vbase, pw);
             int colc[Q];
             T valc[Q];
             load_entries<T, G, Q>(colc, valc, p.col_idx, p.values, e0 + goff, e0 + len, pol_s);
@@ -204,16 +236,17 @@ __device__ __forceinline__ void process_rows(const SpmmParams<T>& p, const int* 
                 consume_step<T, W, G, R>(acc, colc, valc, cnt, cmax, Bp, p.ldb, vbase, pw);
 
                 if (s + ESTEP >= len) {                     // row finished (uniform if MEDIUM)
-                    if (MEDIUM) {
-                        combine_groups<T, W, G, R>(acc);
-                        if (gi == 0 && active)
-                            write_row<T, W, G, R>(p.C + (int64_t)row * p.ldc + c0, acc, vbase, pw,
-                                                  p.alpha, p.beta, read_c);
-                    } else if (active) {
-                        write_row<T, W, G, R>(p.C + (int64_t)row * p.ldc + c0, acc, vbase, pw,
-                                              p.alpha, p.beta, read_c);
+                    if (MEDIUM) combine_groups<T, W, G, R>(acc);
+                    if (active && (!MEDIUM || gi == 0)) {
+                        T* Crow = p.C + (int64_t)row * p.ldc + c0col;
+                        if constexpr (READ_C)
+                            write_row_c0<T, W, G, R>(Crow, acc, c0, vbase, pw, p.alpha, p.beta);
+                        else
+                            write_row<T, W, G, R>(Crow, acc, vbase, pw, p.alpha, p.beta, false);
                     }
                     zero_acc<T, W, R>(acc);
+                    if (loads_c && t2 < nrows)
+                        load_c_row<T, W, G, R>(c0, p.C + (int64_t)row2 * p.ldc + c0col, vbase, pw);
                 }
                 t = t2;
                 s = s2;
@@ -235,24 +268,48 @@ __device__ __forceinline__ void process_rows(const SpmmParams<T>& p, const int* 
 // takes the w-th of nwarps equal contiguous ranges of the short list, then of
 // the medium list.
 // ---------------------------------------------------------------------------
-template <typename T, int W, int G, int R>
-__global__ void __launch_bounds__(ROWS_THREADS, SPMM_ROWS_MIN_BLOCKS)
+// First medium row whose entries start at or after `target` (lower bound in
+// the medium-length prefix).
+__device__ __forceinline__ int medium_lower_bound(const int* __restrict__ med_pre, int n_med,
+                                                  int64_t target) {
+    int lo = 0, hi = n_med;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if ((int64_t)med_pre[mid] < target) lo = mid + 1; else hi = mid;
+    }
+    return lo;
+}
+
+template <typename T>
+struct RowsOccupancy {
+    static constexpr int MIN_BLOCKS = sizeof(T) == 8 ? SPMM_ROWS_MIN_BLOCKS_F64 : SPMM_ROWS_MIN_BLOCKS;
+};
+
+// READ_C: beta != 0 (C is read, and prefetched at each row start).
+template <typename T, int W, int G, int R, bool READ_C>
+__global__ void __launch_bounds__(ROWS_THREADS, RowsOccupancy<T>::MIN_BLOCKS)
 rows_kernel(SpmmParams<T> p) {
     const uint64_t pol_s = policy_evict_first();
     const int n_short = p.hdr[HDR_COUNT_SHORT];
     const int n_med = p.hdr[HDR_COUNT_MEDIUM];
+    const int64_t med_nnz = p.hdr[HDR_MED_NNZ];
     const int64_t nwarps = (int64_t)gridDim.x * (ROWS_THREADS / 32);
     const int64_t w = (int64_t)blockIdx.x * (ROWS_THREADS / 32) + (threadIdx.x >> 5);
-    const bool read_c = p.beta != T(0);
+    // short rows: equal counts per warp; medium rows: equal entries per warp
     const int s0 = (int)(w * n_short / nwarps), s1 = (int)((w + 1) * n_short / nwarps);
-    const int m0 = (int)(w * n_med / nwarps), m1 = (int)((w + 1) * n_med / nwarps);
+    int m0 = 0, m1 = 0;
+    if (n_med > 0) {
+        m0 = medium_lower_bound(p.med_pre, n_med, w * med_nnz / nwarps);
+        m1 = medium_lower_bound(p.med_pre, n_med, (w + 1) * med_nnz / nwarps);
+        if (w == nwarps - 1) m1 = n_med;
+    }
     for (int panel = 0; panel < p.npanels; ++panel) {
         const int c0 = panel * p.panel_cols;
         const int pw = min(p.panel_cols, p.n - c0);
         if (s1 > s0)
-            process_rows<T, W, G, R, false>(p, p.rowlist, s0, s1, c0, pw, pol_s, read_c);
+            process_rows<T, W, G, R, false, READ_C>(p, p.rowlist, s0, s1, c0, pw, pol_s);
         if (m1 > m0)
-            process_rows<T, W, G, R, true>(p, p.rowlist + n_short, m0, m1, c0, pw, pol_s, read_c);
+            process_rows<T, W, G, R, true, READ_C>(p, p.rowlist + n_short, m0, m1, c0, pw, pol_s);
     }
 }
 
@@ -307,7 +364,7 @@ __device__ __forceinline__ int long_segment(int total, int long_grid) {
 }
 
 template <typename T, int W, int G, int R>
-__global__ void __launch_bounds__(LONG_THREADS)
+__global__ void __launch_bounds__(LONG_THREADS, SPMM_LONG_MIN_BLOCKS)
 long_kernel(SpmmParams<T> p) {
     using C = Cfg<T, W, G, R>;
     extern __shared__ __align__(16) unsigned char smem_raw[];

@@ -25,20 +25,21 @@ namespace {
 // Limits of the static scratch (see include/csr_spmm.h).
 constexpr int64_t NOALLOC_MAX_ROWS = 1 << 19;      // m <= 524,288
 constexpr int64_t NOALLOC_MAX_COLS = 512;          // n <= 512
-constexpr int NOALLOC_LONG_GRID_MAX = 320;         // 2 CTAs per SM for up to 160 SMs
+constexpr int NOALLOC_LONG_GRID_MAX = 640;         // 4 CTAs per SM for up to 160 SMs
 
 constexpr size_t al256(size_t x) { return (x + 255) / 256 * 256; }
 constexpr int64_t NOALLOC_TILES = (NOALLOC_MAX_ROWS + BIN_TILE - 1) / BIN_TILE;
 constexpr size_t OFF_HDR = 0;
 constexpr size_t OFF_TILE_COUNTS = al256(OFF_HDR + sizeof(int) * HDR_WORDS);
-constexpr size_t OFF_TILE_OFFSETS = al256(OFF_TILE_COUNTS + sizeof(int) * 4 * NOALLOC_TILES);
-constexpr size_t OFF_ROWLIST = al256(OFF_TILE_OFFSETS + sizeof(int) * 4 * NOALLOC_TILES);
-constexpr size_t OFF_LONG_PRE = al256(OFF_ROWLIST + sizeof(int) * NOALLOC_MAX_ROWS);
+constexpr size_t OFF_TILE_OFFSETS = al256(OFF_TILE_COUNTS + sizeof(int) * BIN_REC * NOALLOC_TILES);
+constexpr size_t OFF_ROWLIST = al256(OFF_TILE_OFFSETS + sizeof(int) * BIN_REC * NOALLOC_TILES);
+constexpr size_t OFF_MED_PRE = al256(OFF_ROWLIST + sizeof(int) * NOALLOC_MAX_ROWS);
+constexpr size_t OFF_LONG_PRE = al256(OFF_MED_PRE + sizeof(int) * (NOALLOC_MAX_ROWS + 1));
 constexpr size_t OFF_PARTIALS = al256(OFF_LONG_PRE + sizeof(int) * (NOALLOC_MAX_ROWS + 1));
 constexpr size_t NOALLOC_BYTES =
     al256(OFF_PARTIALS + sizeof(float) * 2 * NOALLOC_LONG_GRID_MAX * NOALLOC_MAX_COLS);
 
-// The scratch itself (about 5.5 MB on every device that loads this library).
+// The scratch itself (about 8.9 MB on every device that loads this library).
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_BYTES];
 
 // Per-device set-up, done once on the first call made with that device current.
@@ -157,13 +158,14 @@ extern "C" spmm_status_t spmm_csr_f32_noalloc(float alpha, const int32_t* row_pt
     const int CH = std::max(geo.G, U);
     const int long_min = 1024;
     const int short_max = geo.G == 32 ? long_min - 1 : std::min(long_min - 1, 2 * CH);
-    const int long_grid = std::min(2 * ds->num_sms, NOALLOC_LONG_GRID_MAX);
+    const int long_grid = std::min(4 * ds->num_sms, NOALLOC_LONG_GRID_MAX);
 
     BinScratch bs{};
     bs.hdr = reinterpret_cast<int*>(ds->scratch + OFF_HDR);
     bs.tile_counts = reinterpret_cast<int*>(ds->scratch + OFF_TILE_COUNTS);
     bs.tile_offsets = reinterpret_cast<int*>(ds->scratch + OFF_TILE_OFFSETS);
     bs.rowlist = reinterpret_cast<int*>(ds->scratch + OFF_ROWLIST);
+    bs.med_pre = reinterpret_cast<int*>(ds->scratch + OFF_MED_PRE);
     bs.long_pre = reinterpret_cast<int*>(ds->scratch + OFF_LONG_PRE);
     bs.tiles = (int)((m + BIN_TILE - 1) / BIN_TILE);
     if (launch_binning(row_ptr, (int)m, short_max, long_min, bs, st) != cudaSuccess)
@@ -184,6 +186,7 @@ extern "C" spmm_status_t spmm_csr_f32_noalloc(float alpha, const int32_t* row_pt
     p.panel_cols = panel_cols;
     p.npanels = npanels;
     p.rowlist = bs.rowlist;
+    p.med_pre = bs.med_pre;
     p.long_pre = bs.long_pre;
     p.hdr = bs.hdr;
     p.partials = reinterpret_cast<float*>(ds->scratch + OFF_PARTIALS);
@@ -194,3 +197,5 @@ extern "C" spmm_status_t spmm_csr_f32_noalloc(float alpha, const int32_t* row_pt
     if (launch_fixup<float>(p, st) != cudaSuccess) return SPMM_ERR_CUDA;
     return SPMM_OK;
 }
+
+static_assert(NOALLOC_BYTES < 9u * 1024 * 1024, "static scratch grew past its stated size");

@@ -8,7 +8,10 @@ template <>
 cudaError_t launch_rows<float>(const SpmmParams<float>& p, const Geometry& g, int grid,
                                cudaStream_t st) {
     return dispatch_geometry<float>(g, [&]<int W, int G, int R>() -> cudaError_t {
-        rows_kernel<float, W, G, R><<<grid, ROWS_THREADS, 0, st>>>(p);
+        if (p.beta != float(0))
+            rows_kernel<float, W, G, R, true><<<grid, ROWS_THREADS, 0, st>>>(p);
+        else
+            rows_kernel<float, W, G, R, false><<<grid, ROWS_THREADS, 0, st>>>(p);
         return cudaGetLastError();
     });
 }
@@ -17,8 +20,8 @@ template <>
 int rows_blocks_per_sm<float>(const Geometry& g) {
     int blocks = 0;
     cudaError_t e = dispatch_geometry<float>(g, [&]<int W, int G, int R>() -> cudaError_t {
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, rows_kernel<float, W, G, R>,
-                                                             ROWS_THREADS, 0);
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &blocks, rows_kernel<float, W, G, R, false>, ROWS_THREADS, 0);
     });
     return (e == cudaSuccess && blocks > 0) ? blocks : 1;
 }

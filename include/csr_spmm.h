@@ -156,7 +156,7 @@ spmm_status_t spmm_get_profile(spmm_handle_t h, spmm_profile_t *out);
  *
  * Same operation, conventions, arguments (minus the handle) and results as
  * spmm_csr_f32, on the same kernels.  The scratch they need (row bins, long-row
- * partial sums) is one fixed device array inside the library, about 5.5 MB,
+ * partial sums) is one fixed device array inside the library, about 9 MB,
  * held by every GPU that loads the library until the process exits.  Limits:
  * m <= 524288 and n <= 512; larger products return SPMM_ERR_TOO_LARGE and do
  * nothing.  The call never calls cudaMalloc, cudaFree or any allocating

@@ -61,13 +61,17 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+ROWS_KERNEL_SOURCES = ("spmm_kernels.cuh", "spmm_device.cuh", "spmm_internal.h",
+                       "spmm_dispatch.cuh", "spmm_rows_f32.cu", "spmm_rows_f64.cu")
+
+
 def source_digest():
+    """sha256 over the sources that define rows_kernel (the kernel the roofline covers)."""
     csrc = os.path.join(ROOT, "csr_spmm_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in ROWS_KERNEL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()
 
 

@@ -43,6 +43,9 @@ namespace {
 #ifndef SPMM_PANEL_TRIGGER
 #define SPMM_PANEL_TRIGGER 3.0
 #endif
+#ifndef SPMM_PANEL_COLS
+#define SPMM_PANEL_COLS 0     // > 0 forces the panel width (tuning experiments)
+#endif
 constexpr double PANEL_FRACTION = SPMM_PANEL_FRACTION;
 constexpr double PANEL_TRIGGER = SPMM_PANEL_TRIGGER;
 // Rows at least this long go to the CTA-split kernel.
@@ -129,6 +132,7 @@ Plan make_plan(const spmm_handle_s* h, int64_t k, int64_t n, const T* B, int64_t
         panel = (n + np - 1) / np;
         panel = (panel + W - 1) / W * W;
     }
+    if (SPMM_PANEL_COLS > 0) panel = (SPMM_PANEL_COLS + W - 1) / W * W;
     P.panel_cols = (int)std::min<int64_t>(panel, n);
     P.npanels = (int)((n + P.panel_cols - 1) / P.panel_cols);
 

@@ -1,7 +1,7 @@
 // Host driver behind the C ABI in include/csr_spmm.h: argument validation,
 // the handle and its scratch, the column-panel / geometry plan, and the
 // launch sequence
-//   pre-pass (row bins) -> short/medium rows -> long-row CTA split -> fixup.
+//   pre-pass (row bins) -> short/medium rows -> long-row CTA split (+ fixup).
 // No step synchronises the stream; no device value is read back.
 #include <algorithm>
 #include <climits>
@@ -62,7 +62,7 @@ inline int next_pow2(int x) {
 }
 
 struct ScratchLayout {
-    size_t hdr, tile_counts, tile_offsets, rowlist, med_pre, long_pre, partials, total;
+    size_t hdr, tile_counts, tile_offsets, rowlist, med_pre, long_pre, long_cnt, partials, total;
 };
 
 ScratchLayout layout_for(int64_t m, int64_t n, int es, int long_grid) {
@@ -75,6 +75,7 @@ ScratchLayout layout_for(int64_t m, int64_t n, int es, int long_grid) {
     L.rowlist = off;      off = align_up(off + sizeof(int) * (size_t)std::max<int64_t>(m, 1), 256);
     L.med_pre = off;      off = align_up(off + sizeof(int) * (size_t)(m + 1), 256);
     L.long_pre = off;     off = align_up(off + sizeof(int) * (size_t)(m + 1), 256);
+    L.long_cnt = off;     off = align_up(off + sizeof(int) * (size_t)std::max<int64_t>(m, 1), 256);
     L.partials = off;     off = align_up(off + (size_t)es * 2 * long_grid * (size_t)std::max<int64_t>(n, 1), 256);
     L.total = off;
     return L;
@@ -220,10 +221,13 @@ spmm_status_t spmm_csr_impl(spmm_handle_t h, T alpha, const int32_t* row_ptr,
     bs.rowlist = reinterpret_cast<int*>(base + L.rowlist);
     bs.med_pre = reinterpret_cast<int*>(base + L.med_pre);
     bs.long_pre = reinterpret_cast<int*>(base + L.long_pre);
-    bs.tiles = (int)((m + BIN_TILE - 1) / BIN_TILE);
+    bs.long_cnt = reinterpret_cast<int*>(base + L.long_cnt);
+    bin_geometry(m, &bs.items, &bs.tiles);
 
+    // overlap launches only when no profiling events sit between the kernels
+    const bool overlap = SPMM_PDL && !h->profiling;
     mark(h, 0, st);
-    if (launch_binning(row_ptr, (int)m, P.short_max, P.long_min, bs, st) != cudaSuccess)
+    if (launch_binning(row_ptr, (int)m, P.short_max, P.long_min, bs, st, overlap) != cudaSuccess)
         return SPMM_ERR_CUDA;
     mark(h, 1, st);
 
@@ -244,20 +248,20 @@ spmm_status_t spmm_csr_impl(spmm_handle_t h, T alpha, const int32_t* row_ptr,
     p.rowlist = bs.rowlist;
     p.med_pre = bs.med_pre;
     p.long_pre = bs.long_pre;
+    p.long_cnt = bs.long_cnt;
     p.hdr = bs.hdr;
     p.partials = reinterpret_cast<T*>(base + L.partials);
     p.long_grid = lg;
 
-    if (launch_rows<T>(p, P.geo, rows_grid(h, (int)sizeof(T), P.geo), st) != cudaSuccess)
+    if (launch_rows<T>(p, P.geo, rows_grid(h, (int)sizeof(T), P.geo), st, overlap) != cudaSuccess)
         return SPMM_ERR_CUDA;
     mark(h, 2, st);
-    if (launch_long<T>(p, P.geo, st) != cudaSuccess) return SPMM_ERR_CUDA;
+    if (launch_long<T>(p, P.geo, st, overlap) != cudaSuccess) return SPMM_ERR_CUDA;
     mark(h, 3, st);
-    if (launch_fixup<T>(p, st) != cudaSuccess) return SPMM_ERR_CUDA;
-    mark(h, 4, st);
+    mark(h, 4, st);               // the fixup runs inside the long-row launch
     if (h->profiling) {
         h->prof = spmm_profile_t{};
-        h->prof.launches = 6;
+        h->prof.launches = (m <= BIN_SINGLE_ROWS ? 1 : 3) + 2;
         h->prof.panels = P.npanels;
         h->prof.panel_cols = P.panel_cols;
         h->prof.vec_elems = P.geo.W;

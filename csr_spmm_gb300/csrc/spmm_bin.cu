@@ -3,12 +3,15 @@
 // long-row lengths (the medium prefix balances medium rows across warps by
 // entries; the long prefix drives the long-row CTA split).
 //
-// Reads row_ptr only.  For m <= 2048 (one tile) a single CTA does everything
-// in one launch; otherwise three launches:
-//   bin_count   per 2048-row tile: rows per bin, entries in medium and long rows
+// Reads row_ptr only.  For m <= 2048 a single CTA does everything in one
+// launch; otherwise three launches:
+//   bin_count   per tile (512, 1024 or 2048 rows, the smallest that keeps the
+//               tile count within about one wave): rows per bin, entries in
+//               medium and long rows
 //   bin_scan    one CTA: exclusive scans of the tile records, bin totals
 //   bin_scatter per tile: stable ranks (warp ballots + per-warp prefix),
-//               writes rowlist, med_pre and long_pre
+//               writes rowlist, med_pre and long_pre, and zeroes the
+//               per-long-row counters of the long-row kernel
 // Ranks come from ballots in ascending row order, never from atomics, so the
 // lists (and everything computed from them) are identical on every call.
 #include "spmm_internal.h"
@@ -27,14 +30,15 @@ __device__ __forceinline__ int row_len(const int* row_ptr, int row, int m) {
     return row < m ? __ldg(row_ptr + row + 1) - __ldg(row_ptr + row) : -1;
 }
 
-// Per-warp totals of one tile's record into s_part[warp][word]; the caller
-// synchronises and adds the warps in order (tile_total).
+// Per-warp totals of one tile (ITEMS rows per thread) into s_part[warp][word];
+// the caller synchronises and adds the warps in order (tile_total).
+template <int ITEMS>
 __device__ __forceinline__ void tile_record(const int* __restrict__ row_ptr, int m, int short_max,
                                             int long_min, int tile, int (*s_part)[R_USED]) {
     int c[R_USED] = {0, 0, 0, 0, 0};
-    const int base = tile * BIN_TILE;
+    const int base = tile * BIN_THREADS * ITEMS;
 #pragma unroll
-    for (int j = 0; j < BIN_ITEMS; ++j) {
+    for (int j = 0; j < ITEMS; ++j) {
         const int row = base + j * BIN_THREADS + threadIdx.x;
         const int len = row_len(row_ptr, row, m);
         const int b = len >= 0 ? classify(len, short_max, long_min) : -1;
@@ -62,16 +66,17 @@ __device__ __forceinline__ int tile_total(const int (*s_part)[R_USED], int word)
 
 // Stable scatter of one tile.  run[] holds the tile's offsets within each bin
 // (and within the medium / long length prefixes); bin_base the list offsets.
+template <int ITEMS>
 __device__ __forceinline__ void tile_scatter(const int* __restrict__ row_ptr, int m, int short_max,
                                              int long_min, int tile, int (&run)[R_USED],
                                              const int (&bin_base)[3], int* __restrict__ rowlist,
                                              int* __restrict__ med_pre, int* __restrict__ long_pre,
-                                             int (*s_wc)[R_USED]) {
+                                             int* __restrict__ long_cnt, int (*s_wc)[R_USED]) {
     constexpr int NW = BIN_THREADS / 32;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const unsigned lt_mask = (1u << lane) - 1u;
-    const int base = tile * BIN_TILE;
-    for (int j = 0; j < BIN_ITEMS; ++j) {
+    const int base = tile * BIN_THREADS * ITEMS;
+    for (int j = 0; j < ITEMS; ++j) {
         const int row = base + j * BIN_THREADS + threadIdx.x;
         const int len = row_len(row_ptr, row, m);
         const int b = len >= 0 ? classify(len, short_max, long_min) : -1;
@@ -116,7 +121,10 @@ __device__ __forceinline__ void tile_scatter(const int* __restrict__ row_ptr, in
         if (b >= 0) {
             const int pos_in_bin = run[b] + wpre[b] + rank[b];
             rowlist[bin_base[b] + pos_in_bin] = row;
-            if (b == BIN_LONG) long_pre[pos_in_bin] = run[R_LONG_NNZ] + wpre[R_LONG_NNZ] + lincl - llen;
+            if (b == BIN_LONG) {
+                long_pre[pos_in_bin] = run[R_LONG_NNZ] + wpre[R_LONG_NNZ] + lincl - llen;
+                long_cnt[pos_in_bin] = 0;
+            }
             if (b == BIN_MEDIUM) med_pre[pos_in_bin] = run[R_MED_NNZ] + wpre[R_MED_NNZ] + mincl - mlen;
         }
 #pragma unroll
@@ -136,14 +144,15 @@ __device__ __forceinline__ void write_header(const int (&total)[R_USED], int* __
     med_pre[total[R_MED]] = total[R_MED_NNZ];
 }
 
-// ---- one tile (m <= BIN_TILE): the whole pre-pass in one CTA ----
+// ---- m <= BIN_SINGLE_ROWS: the whole pre-pass in one CTA ----
 __global__ void __launch_bounds__(BIN_THREADS)
 bin_single_kernel(const int* __restrict__ row_ptr, int m, int short_max, int long_min,
                   int* __restrict__ hdr, int* __restrict__ rowlist, int* __restrict__ med_pre,
-                  int* __restrict__ long_pre) {
+                  int* __restrict__ long_pre, int* __restrict__ long_cnt) {
     __shared__ int s_part[BIN_THREADS / 32][R_USED];
     __shared__ int s_wc[BIN_THREADS / 32][R_USED];
-    tile_record(row_ptr, m, short_max, long_min, 0, s_part);
+    allow_successor();
+    tile_record<BIN_SINGLE_ITEMS>(row_ptr, m, short_max, long_min, 0, s_part);
     __syncthreads();
     int total[R_USED];
 #pragma unroll
@@ -151,16 +160,18 @@ bin_single_kernel(const int* __restrict__ row_ptr, int m, int short_max, int lon
     if (threadIdx.x == 0) write_header(total, hdr, med_pre, long_pre);
     int run[R_USED] = {0, 0, 0, 0, 0};
     const int bin_base[3] = {0, total[R_SHORT], total[R_SHORT] + total[R_MED]};
-    tile_scatter(row_ptr, m, short_max, long_min, 0, run, bin_base, rowlist, med_pre, long_pre,
-                 s_wc);
+    tile_scatter<BIN_SINGLE_ITEMS>(row_ptr, m, short_max, long_min, 0, run, bin_base, rowlist,
+                                   med_pre, long_pre, long_cnt, s_wc);
 }
 
 // ---- many tiles ----
+template <int ITEMS>
 __global__ void __launch_bounds__(BIN_THREADS)
 bin_count_kernel(const int* __restrict__ row_ptr, int m, int short_max, int long_min,
                  int* __restrict__ tile_counts) {
     __shared__ int s_part[BIN_THREADS / 32][R_USED];
-    tile_record(row_ptr, m, short_max, long_min, blockIdx.x, s_part);
+    allow_successor();
+    tile_record<ITEMS>(row_ptr, m, short_max, long_min, blockIdx.x, s_part);
     __syncthreads();
     if (threadIdx.x < BIN_REC) tile_counts[blockIdx.x * BIN_REC + threadIdx.x] =
         threadIdx.x < R_USED ? tile_total(s_part, threadIdx.x) : 0;
@@ -174,6 +185,8 @@ bin_scan_kernel(const int* __restrict__ tile_counts, int tiles, int* __restrict_
                 int* __restrict__ hdr, int* __restrict__ med_pre, int* __restrict__ long_pre) {
     __shared__ int s_warp[32][R_USED];
     __shared__ int s_carry[R_USED];
+    wait_for_predecessor();
+    allow_successor();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (threadIdx.x < R_USED) s_carry[threadIdx.x] = 0;
     __syncthreads();
@@ -225,38 +238,47 @@ bin_scan_kernel(const int* __restrict__ tile_counts, int tiles, int* __restrict_
     }
 }
 
+template <int ITEMS>
 __global__ void __launch_bounds__(BIN_THREADS)
 bin_scatter_kernel(const int* __restrict__ row_ptr, int m, int short_max, int long_min,
                    const int* __restrict__ tile_offsets, const int* __restrict__ hdr,
                    int* __restrict__ rowlist, int* __restrict__ med_pre,
-                   int* __restrict__ long_pre) {
+                   int* __restrict__ long_pre, int* __restrict__ long_cnt) {
     __shared__ int s_wc[BIN_THREADS / 32][R_USED];
+    wait_for_predecessor();
+    allow_successor();
     int run[R_USED];
 #pragma unroll
     for (int c = 0; c < R_USED; ++c) run[c] = tile_offsets[blockIdx.x * BIN_REC + c];
     const int bin_base[3] = {0, hdr[HDR_COUNT_SHORT], hdr[HDR_COUNT_SHORT] + hdr[HDR_COUNT_MEDIUM]};
-    tile_scatter(row_ptr, m, short_max, long_min, blockIdx.x, run, bin_base, rowlist, med_pre,
-                 long_pre, s_wc);
+    tile_scatter<ITEMS>(row_ptr, m, short_max, long_min, blockIdx.x, run, bin_base, rowlist,
+                            med_pre, long_pre, long_cnt, s_wc);
 }
 
 }  // namespace
 
 cudaError_t launch_binning(const int* row_ptr, int m, int short_max, int long_min,
-                           const BinScratch& s, cudaStream_t st) {
+                           const BinScratch& s, cudaStream_t st, bool overlap) {
     if (m <= 0) return cudaSuccess;
-    if (s.tiles == 1) {
-        bin_single_kernel<<<1, BIN_THREADS, 0, st>>>(row_ptr, m, short_max, long_min, s.hdr,
-                                                     s.rowlist, s.med_pre, s.long_pre);
-        return cudaGetLastError();
-    }
-    bin_count_kernel<<<s.tiles, BIN_THREADS, 0, st>>>(row_ptr, m, short_max, long_min,
-                                                      s.tile_counts);
-    bin_scan_kernel<<<1, SCAN_THREADS, 0, st>>>(s.tile_counts, s.tiles, s.tile_offsets, s.hdr,
-                                                s.med_pre, s.long_pre);
-    bin_scatter_kernel<<<s.tiles, BIN_THREADS, 0, st>>>(row_ptr, m, short_max, long_min,
-                                                        s.tile_offsets, s.hdr, s.rowlist,
-                                                        s.med_pre, s.long_pre);
-    return cudaGetLastError();
+    const dim3 blk(BIN_THREADS);
+    if (m <= BIN_SINGLE_ROWS)
+        return launch_chained(bin_single_kernel, dim3(1), blk, 0, st, false, row_ptr, m,
+                              short_max, long_min, s.hdr, s.rowlist, s.med_pre, s.long_pre,
+                              s.long_cnt);
+    auto count = s.items == 8 ? bin_count_kernel<8> : s.items == 4 ? bin_count_kernel<4>
+                                                                      : bin_count_kernel<2>;
+    auto scatter = s.items == 8 ? bin_scatter_kernel<8> : s.items == 4 ? bin_scatter_kernel<4>
+                                                                        : bin_scatter_kernel<2>;
+    cudaError_t e = launch_chained(count, dim3(s.tiles), blk, 0, st, false, row_ptr, m,
+                                   short_max, long_min, s.tile_counts);
+    if (e != cudaSuccess) return e;
+    e = launch_chained(bin_scan_kernel, dim3(1), dim3(SCAN_THREADS), 0, st, overlap,
+                       (const int*)s.tile_counts, s.tiles, s.tile_offsets, s.hdr, s.med_pre,
+                       s.long_pre);
+    if (e != cudaSuccess) return e;
+    return launch_chained(scatter, dim3(s.tiles), blk, 0, st, overlap, row_ptr, m,
+                          short_max, long_min, (const int*)s.tile_offsets, (const int*)s.hdr,
+                          s.rowlist, s.med_pre, s.long_pre, s.long_cnt);
 }
 
 }  // namespace spmm

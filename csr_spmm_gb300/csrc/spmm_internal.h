@@ -25,16 +25,24 @@ enum HeaderWord {
     HDR_WORDS = 8
 };
 
-// Rows per pre-pass tile: 256 threads x 8 rows.
+// Pre-pass geometry: 256 threads; tiles of 512 rows, or one CTA for m <= 2048.
 constexpr int BIN_THREADS = 256;
-constexpr int BIN_ITEMS = 8;
-constexpr int BIN_TILE = BIN_THREADS * BIN_ITEMS;
+constexpr int BIN_ITEMS = 2;                            // fewest rows per thread, many-tile path
+constexpr int BIN_TILE = BIN_THREADS * BIN_ITEMS;       // smallest tile (bounds the tile count)
+constexpr int BIN_WAVE_TILES = 1216;                    // tiles kept within about one wave
+constexpr int BIN_SINGLE_ITEMS = 8;                     // rows per thread, one-CTA path
+constexpr int BIN_SINGLE_ROWS = BIN_THREADS * BIN_SINGLE_ITEMS;   // m up to this: one launch
 constexpr int BIN_REC = 8;    // int32 words per tile record
 
 // Long-row kernel geometry.
 constexpr int LONG_THREADS = 256;
 constexpr int LONG_WARPS = LONG_THREADS / 32;
 constexpr int LONG_MIN_SEGMENT = 2048;   // smallest per-CTA share of long-row entries
+
+// Programmatic dependent launch between the kernels of one call.
+#ifndef SPMM_PDL
+#define SPMM_PDL 1
+#endif
 
 // Rows kernel block size and minimum resident blocks per SM (a register cap).
 constexpr int ROWS_THREADS = 256;
@@ -58,14 +66,25 @@ constexpr int ROWS_THREADS = 256;
 #define SPMM_BATCH_MAX 8
 #endif
 
+// Rows per thread (2, 4 or 8) and tile count of the many-tile pre-pass for m
+// rows: the smallest tiles that keep the count within about one wave.
+inline void bin_geometry(int64_t m, int* items, int* tiles) {
+    int it = BIN_ITEMS;
+    while (it < 8 && (m + BIN_THREADS * it - 1) / (BIN_THREADS * it) > BIN_WAVE_TILES) it *= 2;
+    *items = it;
+    *tiles = (int)((m + BIN_THREADS * it - 1) / (BIN_THREADS * it));
+}
+
 struct BinScratch {
     int* rowlist;       // [m]  short rows, then medium rows, then long rows (each ascending)
     int* med_pre;       // [m + 1] exclusive prefix of medium-row lengths (stable order)
     int* long_pre;      // [m + 1] exclusive prefix of long-row lengths (stable order)
+    int* long_cnt;      // [m] per long row: CTAs that have added their partial (zeroed here)
     int* tile_counts;   // [tiles * BIN_REC] per tile: bin counts, long nnz, medium nnz
     int* tile_offsets;  // [tiles * BIN_REC] exclusive scans of the above over tiles
     int* hdr;           // [HDR_WORDS]
-    int tiles;
+    int tiles;          // many-tile path: tiles of BIN_THREADS * items rows
+    int items;
 };
 
 template <typename T>
@@ -87,6 +106,7 @@ struct SpmmParams {
     const int* rowlist;
     const int* med_pre;
     const int* long_pre;
+    int* long_cnt;
     const int* hdr;
     // long-row partial sums: [2 * long_grid, n]
     T* partials;
@@ -101,16 +121,17 @@ struct Geometry {
 };
 
 // ---- pre-pass (spmm_bin.cu) ----
+// `overlap`: launch the dependent kernels of the chain with programmatic
+// dependent launch (the first kernel of a call always waits for the stream).
 cudaError_t launch_binning(const int* row_ptr, int m, int short_max, int long_min,
-                           const BinScratch& s, cudaStream_t st);
+                           const BinScratch& s, cudaStream_t st, bool overlap);
 
 // ---- per-bin kernels (spmm_rows_*.cu, spmm_long_*.cu) ----
 template <typename T>
-cudaError_t launch_rows(const SpmmParams<T>& p, const Geometry& g, int grid, cudaStream_t st);
+cudaError_t launch_rows(const SpmmParams<T>& p, const Geometry& g, int grid, cudaStream_t st,
+                        bool overlap);
 template <typename T>
-cudaError_t launch_long(const SpmmParams<T>& p, const Geometry& g, cudaStream_t st);
-template <typename T>
-cudaError_t launch_fixup(const SpmmParams<T>& p, cudaStream_t st);
+cudaError_t launch_long(const SpmmParams<T>& p, const Geometry& g, cudaStream_t st, bool overlap);
 
 // ---- epilogue-only and checking kernels (spmm_misc.cu) ----
 template <typename T>
@@ -121,5 +142,42 @@ cudaError_t launch_csr_check(const int* row_ptr, const int* col_idx, int64_t m, 
 // Blocks per SM the rows kernel reaches for this geometry (occupancy query).
 template <typename T>
 int rows_blocks_per_sm(const Geometry& g);
+
+}  // namespace spmm
+
+namespace spmm {
+
+// Programmatic dependent launch: a kernel of the chain may be launched while
+// its predecessor drains; it waits here before touching the predecessor's
+// output (a no-op when launched without the attribute).
+__device__ __forceinline__ void wait_for_predecessor() {
+#if defined(__CUDA_ARCH__)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+}
+// Let the next kernel of the chain be scheduled now.
+__device__ __forceinline__ void allow_successor() {
+#if defined(__CUDA_ARCH__)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+}
+
+// Launch `kernel` on `st`, overlapping its launch with the previous kernel
+// of the stream when `overlap` is set.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                  cudaStream_t st, bool overlap, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = overlap ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 }  // namespace spmm

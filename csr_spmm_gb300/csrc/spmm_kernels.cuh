@@ -289,6 +289,8 @@ struct RowsOccupancy {
 template <typename T, int W, int G, int R, bool READ_C>
 __global__ void __launch_bounds__(ROWS_THREADS, RowsOccupancy<T>::MIN_BLOCKS)
 rows_kernel(SpmmParams<T> p) {
+    wait_for_predecessor();
+    allow_successor();
     const uint64_t pol_s = policy_evict_first();
     const int n_short = p.hdr[HDR_COUNT_SHORT];
     const int n_med = p.hdr[HDR_COUNT_MEDIUM];
@@ -355,9 +357,27 @@ __device__ __forceinline__ void accumulate_range(T (&acc)[R][W], const SpmmParam
 // added in warp order through shared memory.  A row lying wholly inside the
 // range is finished here (epilogue to C).  Otherwise the CTA stores a partial
 // sum: slot 0 for the row containing the range's first entry, slot 1 for the
-// row containing its last; the fixup kernel adds the partials of each split
-// row in CTA order.
+// row containing its last; the last CTA to finish a split row adds its
+// partials in CTA order (the fixup pass, in the same launch).
 // ---------------------------------------------------------------------------
+// Sum the partials of split long row r in CTA order (cf's slot, then slot 0
+// of cf+1 .. cl) and apply the epilogue; every thread of the CTA takes
+// columns threadIdx.x, threadIdx.x + blockDim.x, ...  Partials were written by
+// other SMs, so they are read from L2 (ld.cg), never from a stale L1 line.
+template <typename T>
+__device__ __forceinline__ void finish_split_row(const SpmmParams<T>& p, const int* lrows, int r,
+                                                 int seg, bool read_c) {
+    const int pre_r = p.long_pre[r], pre_r1 = p.long_pre[r + 1];
+    const int cf = pre_r / seg, cl = (pre_r1 - 1) / seg;
+    const int slot_first = (pre_r == cf * seg) ? 0 : 1;
+    T* Crow = p.C + (int64_t)lrows[r] * p.ldc;
+    for (int col = threadIdx.x; col < p.n; col += blockDim.x) {
+        T s = __ldcg(p.partials + ((int64_t)cf * 2 + slot_first) * p.n + col);
+        for (int c = cf + 1; c <= cl; ++c) s += __ldcg(p.partials + ((int64_t)c * 2) * p.n + col);
+        Crow[col] = read_c ? p.alpha * s + p.beta * Crow[col] : p.alpha * s;
+    }
+}
+
 __device__ __forceinline__ int long_segment(int total, int long_grid) {
     const int s = (int)(((int64_t)total + long_grid - 1) / long_grid);
     return s > LONG_MIN_SEGMENT ? s : LONG_MIN_SEGMENT;
@@ -369,6 +389,7 @@ long_kernel(SpmmParams<T> p) {
     using C = Cfg<T, W, G, R>;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     T* red = reinterpret_cast<T*>(smem_raw);      // [LONG_WARPS][SLOTS * W]
+    wait_for_predecessor();
     const int nl = p.hdr[HDR_COUNT_LONG];
     const int total = p.hdr[HDR_LONG_NNZ];
     if (nl == 0 || total == 0) return;
@@ -449,32 +470,38 @@ long_kernel(SpmmParams<T> p) {
             }
         }
     }
-}
 
-// Adds the partial sums of every long row that spans more than one CTA, in
-// CTA order, and applies the epilogue.  One CTA per row (grid-stride).
-template <typename T>
-__global__ void __launch_bounds__(256)
-fixup_kernel(SpmmParams<T> p) {
-    const int nl = p.hdr[HDR_COUNT_LONG];
-    const int total = p.hdr[HDR_LONG_NNZ];
-    if (nl == 0 || total == 0) return;
-    const int seg = long_segment(total, p.long_grid);
-    const int* lrows = p.rowlist + p.hdr[HDR_COUNT_SHORT] + p.hdr[HDR_COUNT_MEDIUM];
-    const bool read_c = p.beta != T(0);
-    for (int r = blockIdx.x; r < nl; r += gridDim.x) {
-        const int pre_r = p.long_pre[r], pre_r1 = p.long_pre[r + 1];
-        const int cf = pre_r / seg, cl = (pre_r1 - 1) / seg;
-        if (cf == cl) continue;                              // finished by its CTA
-        const int slot_first = (pre_r == cf * seg) ? 0 : 1;
-        const int row = lrows[r];
-        T* Crow = p.C + (int64_t)row * p.ldc;
-        for (int col = threadIdx.x; col < p.n; col += blockDim.x) {
-            T s = p.partials[((int64_t)cf * 2 + slot_first) * p.n + col];
-            for (int c = cf + 1; c <= cl; ++c) s += p.partials[((int64_t)c * 2) * p.n + col];
-            const T o = read_c ? p.alpha * s + p.beta * Crow[col] : p.alpha * s;
-            Crow[col] = o;
+    // Split rows.  This CTA holds a partial of r0 (slot 0) unless r0 lies wholly
+    // inside its range, and of its last row (slot 1) if that row runs past the
+    // range.  Each CTA sharing a row counts its partial once; the CTA whose
+    // count completes the row sums every partial of it in CTA order (a fixed
+    // order, whichever CTA finishes last) and applies the epilogue.
+    __shared__ int s_finish[2];
+    int lo1 = r0, hi1 = nl - 1;                   // last row: largest r with long_pre[r] < s1
+    while (lo1 < hi1) {
+        const int mid = (lo1 + hi1 + 1) >> 1;
+        if (p.long_pre[mid] < s1) lo1 = mid; else hi1 = mid - 1;
+    }
+    const int rlast = lo1;
+    __threadfence();                              // partial writes before the counters
+    __syncthreads();
+    if (threadIdx.x < 2) {
+        const int r = threadIdx.x == 0 ? r0 : rlast;
+        int fin = 0;
+        if (threadIdx.x == 0 || rlast != r0) {
+            const int pre_r = p.long_pre[r], pre_r1 = p.long_pre[r + 1];
+            if (!(pre_r >= s0 && pre_r1 <= s1)) {
+                const int cf = pre_r / seg, cl = (pre_r1 - 1) / seg;
+                fin = atomicAdd(p.long_cnt + r, 1) == cl - cf;
+            }
         }
+        s_finish[threadIdx.x] = fin;
+    }
+    __syncthreads();
+    for (int which = 0; which < 2; ++which) {
+        if (!s_finish[which]) continue;           // uniform per CTA
+        __threadfence();
+        finish_split_row<T>(p, lrows, which == 0 ? r0 : rlast, seg, read_c);
     }
 }
 

@@ -9,7 +9,8 @@
 // The array is a single buffer per device, shared by every call: calls that
 // overlap on the GPU (two streams, or a second call before the first has run)
 // race on it.  Nothing in it has to start at zero: each call's pre-pass writes
-// every word a later kernel of the same call reads.
+// every word a later kernel of the same call reads (it also zeroes the
+// long-row counters before the long-row kernel counts on them).
 #include <algorithm>
 #include <climits>
 #include <cstdint>
@@ -35,11 +36,12 @@ constexpr size_t OFF_TILE_OFFSETS = al256(OFF_TILE_COUNTS + sizeof(int) * BIN_RE
 constexpr size_t OFF_ROWLIST = al256(OFF_TILE_OFFSETS + sizeof(int) * BIN_REC * NOALLOC_TILES);
 constexpr size_t OFF_MED_PRE = al256(OFF_ROWLIST + sizeof(int) * NOALLOC_MAX_ROWS);
 constexpr size_t OFF_LONG_PRE = al256(OFF_MED_PRE + sizeof(int) * (NOALLOC_MAX_ROWS + 1));
-constexpr size_t OFF_PARTIALS = al256(OFF_LONG_PRE + sizeof(int) * (NOALLOC_MAX_ROWS + 1));
+constexpr size_t OFF_LONG_CNT = al256(OFF_LONG_PRE + sizeof(int) * (NOALLOC_MAX_ROWS + 1));
+constexpr size_t OFF_PARTIALS = al256(OFF_LONG_CNT + sizeof(int) * NOALLOC_MAX_ROWS);
 constexpr size_t NOALLOC_BYTES =
     al256(OFF_PARTIALS + sizeof(float) * 2 * NOALLOC_LONG_GRID_MAX * NOALLOC_MAX_COLS);
 
-// The scratch itself (about 8.9 MB on every device that loads this library).
+// The scratch itself (about 11.1 MB on every device that loads this library).
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_BYTES];
 
 // Per-device set-up, done once on the first call made with that device current.
@@ -166,9 +168,10 @@ extern "C" spmm_status_t spmm_csr_f32_noalloc(float alpha, const int32_t* row_pt
     bs.tile_offsets = reinterpret_cast<int*>(ds->scratch + OFF_TILE_OFFSETS);
     bs.rowlist = reinterpret_cast<int*>(ds->scratch + OFF_ROWLIST);
     bs.med_pre = reinterpret_cast<int*>(ds->scratch + OFF_MED_PRE);
+    bs.long_cnt = reinterpret_cast<int*>(ds->scratch + OFF_LONG_CNT);
     bs.long_pre = reinterpret_cast<int*>(ds->scratch + OFF_LONG_PRE);
-    bs.tiles = (int)((m + BIN_TILE - 1) / BIN_TILE);
-    if (launch_binning(row_ptr, (int)m, short_max, long_min, bs, st) != cudaSuccess)
+    bin_geometry(m, &bs.items, &bs.tiles);
+    if (launch_binning(row_ptr, (int)m, short_max, long_min, bs, st, SPMM_PDL) != cudaSuccess)
         return SPMM_ERR_CUDA;
 
     SpmmParams<float> p{};
@@ -187,15 +190,15 @@ extern "C" spmm_status_t spmm_csr_f32_noalloc(float alpha, const int32_t* row_pt
     p.npanels = npanels;
     p.rowlist = bs.rowlist;
     p.med_pre = bs.med_pre;
+    p.long_cnt = bs.long_cnt;
     p.long_pre = bs.long_pre;
     p.hdr = bs.hdr;
     p.partials = reinterpret_cast<float*>(ds->scratch + OFF_PARTIALS);
     p.long_grid = long_grid;
     const int grid = rows_blocks_per_sm<float>(geo) * ds->num_sms;
-    if (launch_rows<float>(p, geo, grid, st) != cudaSuccess) return SPMM_ERR_CUDA;
-    if (launch_long<float>(p, geo, st) != cudaSuccess) return SPMM_ERR_CUDA;
-    if (launch_fixup<float>(p, st) != cudaSuccess) return SPMM_ERR_CUDA;
+    if (launch_rows<float>(p, geo, grid, st, SPMM_PDL) != cudaSuccess) return SPMM_ERR_CUDA;
+    if (launch_long<float>(p, geo, st, SPMM_PDL) != cudaSuccess) return SPMM_ERR_CUDA;
     return SPMM_OK;
 }
 
-static_assert(NOALLOC_BYTES < 9u * 1024 * 1024, "static scratch grew past its stated size");
+static_assert(NOALLOC_BYTES < 11u * 1024 * 1024, "static scratch grew past its stated size");

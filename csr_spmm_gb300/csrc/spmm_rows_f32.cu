@@ -6,13 +6,13 @@ namespace spmm {
 
 template <>
 cudaError_t launch_rows<float>(const SpmmParams<float>& p, const Geometry& g, int grid,
-                               cudaStream_t st) {
+                               cudaStream_t st, bool overlap) {
     return dispatch_geometry<float>(g, [&]<int W, int G, int R>() -> cudaError_t {
         if (p.beta != float(0))
-            rows_kernel<float, W, G, R, true><<<grid, ROWS_THREADS, 0, st>>>(p);
-        else
-            rows_kernel<float, W, G, R, false><<<grid, ROWS_THREADS, 0, st>>>(p);
-        return cudaGetLastError();
+            return launch_chained(rows_kernel<float, W, G, R, true>, dim3(grid), dim3(ROWS_THREADS),
+                                  0, st, overlap, p);
+        return launch_chained(rows_kernel<float, W, G, R, false>, dim3(grid), dim3(ROWS_THREADS), 0,
+                              st, overlap, p);
     });
 }
 

@@ -127,7 +127,7 @@ typedef struct {
     float prepass_ms;      /* row-binning pre-pass (3 launches) */
     float rows_ms;         /* short + medium rows kernel (1 launch) */
     float long_ms;         /* long-row CTA split (1 launch) */
-    float fixup_ms;        /* long-row fixup (1 launch) */
+    float fixup_ms;        /* 0: the long-row fixup runs inside the long-row launch */
     float total_ms;        /* first event to last event */
     int32_t launches;      /* kernels the product launched */
     int32_t rows_short, rows_medium, rows_long;  /* rows per bin */
@@ -156,7 +156,7 @@ spmm_status_t spmm_get_profile(spmm_handle_t h, spmm_profile_t *out);
  *
  * Same operation, conventions, arguments (minus the handle) and results as
  * spmm_csr_f32, on the same kernels.  The scratch they need (row bins, long-row
- * partial sums) is one fixed device array inside the library, about 9 MB,
+ * partial sums) is one fixed device array inside the library, about 11 MB,
  * held by every GPU that loads the library until the process exits.  Limits:
  * m <= 524288 and n <= 512; larger products return SPMM_ERR_TOO_LARGE and do
  * nothing.  The call never calls cudaMalloc, cudaFree or any allocating

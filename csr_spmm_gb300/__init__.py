@@ -17,12 +17,14 @@ from ._lib import (EXPORTED, SPMM_ERR_ALLOC, SPMM_ERR_CUDA, SPMM_ERR_DIMENSION_M
                    SPMM_ERR_INVALID_ARGUMENT, SPMM_ERR_INVALID_CSR, SPMM_ERR_NULL_POINTER,
                    SPMM_ERR_UNSUPPORTED_DEVICE, SPMM_OK, SpmmError, library, spmm_create,
                    spmm_csr_check, spmm_csr_f32, spmm_csr_f32_noalloc, spmm_csr_f64,
-                   spmm_destroy, spmm_get_profile,
+                   spmm_destroy, spmm_get_profile, spmm_plan_create, spmm_plan_csr_f32,
+                   spmm_plan_csr_f64, spmm_plan_destroy,
                    spmm_reserve, spmm_set_profiling, status_string)
 
 __all__ = ["Handle", "spmm", "csr_check", "SpmmError", "library", "spmm_create", "spmm_destroy",
            "spmm_reserve", "spmm_csr_f32", "spmm_csr_f64", "spmm_csr_check", "status_string",
-           "spmm_set_profiling", "spmm_get_profile", "spmm_csr_f32_noalloc", "EXPORTED"]
+           "spmm_set_profiling", "spmm_get_profile", "spmm_csr_f32_noalloc", "spmm_plan_create",
+           "spmm_plan_destroy", "spmm_plan_csr_f32", "spmm_plan_csr_f64", "Plan", "EXPORTED"]
 
 
 class Handle:
@@ -88,6 +90,41 @@ def spmm(handle: Handle, alpha: float, row_ptr, col_idx, values, k: int, B, beta
         spmm_csr_f64(*args)
     else:
         raise TypeError("values must be float32 or float64")
+
+
+class Plan:
+    """The row bins of one sparsity structure, reused by repeated products."""
+
+    def __init__(self, handle: Handle, row_ptr, k: int, n: int, dtype, stream=None):
+        import torch
+        self.handle = handle
+        self.m = int(row_ptr.numel()) - 1
+        self.k, self.n = int(k), int(n)
+        self.dtype = dtype
+        es = 4 if dtype == torch.float32 else 8
+        st = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+        self.ptr = spmm_plan_create(handle.ptr, _ptr(row_ptr), self.m, self.k, self.n, es, st)
+
+    def __call__(self, alpha, row_ptr, col_idx, values, B, beta, C, stream=None) -> None:
+        """C <- alpha * A * B + beta * C with A's structure from the plan."""
+        import torch
+        st = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+        ldb = B.stride(0) if B.shape[0] > 1 else max(1, self.n)
+        ldc = C.stride(0) if C.shape[0] > 1 else max(1, self.n)
+        fn = spmm_plan_csr_f32 if values.dtype == torch.float32 else spmm_plan_csr_f64
+        fn(self.ptr, alpha, _ptr(row_ptr), _ptr(col_idx), _ptr(values), _ptr(B), ldb, beta,
+           _ptr(C), ldc, st)
+
+    def close(self) -> None:
+        if self.ptr:
+            spmm_plan_destroy(self.ptr)
+            self.ptr = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def csr_check(handle: Handle, row_ptr, col_idx, k: int, stream=None) -> int:

@@ -27,6 +27,7 @@ SPMM_ERR_TOO_LARGE = 8
 # every symbol include/csr_spmm.h declares
 EXPORTED = ("spmm_create", "spmm_destroy", "spmm_reserve", "spmm_csr_f32", "spmm_csr_f64",
             "spmm_csr_check", "spmm_set_profiling", "spmm_get_profile", "spmm_csr_f32_noalloc",
+            "spmm_plan_create", "spmm_plan_destroy", "spmm_plan_csr_f32", "spmm_plan_csr_f64",
             "spmm_status_string")
 
 
@@ -88,6 +89,16 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.spmm_csr_f32_noalloc.argtypes = [ctypes.c_float, vp, vp, vp, i64, i64, vp, i64, i64,
                                          ctypes.c_float, vp, i64, vp]
     lib.spmm_csr_f32_noalloc.restype = st
+    lib.spmm_plan_create.argtypes = [vp, ctypes.POINTER(vp), vp, i64, i64, i64, ctypes.c_int, vp]
+    lib.spmm_plan_create.restype = st
+    lib.spmm_plan_destroy.argtypes = [vp]
+    lib.spmm_plan_destroy.restype = st
+    lib.spmm_plan_csr_f32.argtypes = [vp, ctypes.c_float, vp, vp, vp, vp, i64, ctypes.c_float, vp,
+                                      i64, vp]
+    lib.spmm_plan_csr_f32.restype = st
+    lib.spmm_plan_csr_f64.argtypes = [vp, ctypes.c_double, vp, vp, vp, vp, i64, ctypes.c_double,
+                                      vp, i64, vp]
+    lib.spmm_plan_csr_f64.restype = st
     lib.spmm_status_string.argtypes = [ctypes.c_int]
     lib.spmm_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -161,4 +172,34 @@ def spmm_csr_f32_noalloc(alpha, row_ptr, col_idx, values, m, k, B, ldb, n, beta,
                                        float(beta), C, ldc, stream or None)
     if check:
         _check(s, "spmm_csr_f32_noalloc")
+    return s
+
+
+def spmm_plan_create(handle, row_ptr, m, k, n, elem_size, stream=0) -> int:
+    """Analyse a sparsity structure once; returns the plan pointer."""
+    plan = ctypes.c_void_p()
+    _check(library().spmm_plan_create(handle, ctypes.byref(plan), row_ptr, m, k, n, elem_size,
+                                      stream or None), "spmm_plan_create")
+    return plan.value
+
+
+def spmm_plan_destroy(plan) -> None:
+    _check(library().spmm_plan_destroy(plan), "spmm_plan_destroy")
+
+
+def spmm_plan_csr_f32(plan, alpha, row_ptr, col_idx, values, B, ldb, beta, C, ldc, stream=0,
+                      check=True) -> int:
+    s = library().spmm_plan_csr_f32(plan, float(alpha), row_ptr, col_idx, values, B, ldb,
+                                    float(beta), C, ldc, stream or None)
+    if check:
+        _check(s, "spmm_plan_csr_f32")
+    return s
+
+
+def spmm_plan_csr_f64(plan, alpha, row_ptr, col_idx, values, B, ldb, beta, C, ldc, stream=0,
+                      check=True) -> int:
+    s = library().spmm_plan_csr_f64(plan, float(alpha), row_ptr, col_idx, values, B, ldb,
+                                    float(beta), C, ldc, stream or None)
+    if check:
+        _check(s, "spmm_plan_csr_f64")
     return s

@@ -33,6 +33,23 @@ struct spmm_handle_s {
     const int* prof_hdr = nullptr;     // device header of the last profiled call
 };
 
+// An analysed sparsity structure: the row bins of one row_ptr, computed once
+// and reused by every product issued on the plan.
+struct spmm_plan_s {
+    spmm_handle_s* h = nullptr;
+    int64_t m = 0, k = 0, n = 0;
+    int es = 0;
+    int long_grid = 0;
+    void* scratch = nullptr;          // bins, counters, partials (plan-owned)
+    int* hdr = nullptr;
+    int* rowlist = nullptr;
+    int* med_pre = nullptr;
+    int* long_pre = nullptr;
+    int* long_cnt = nullptr;
+    void* partials = nullptr;
+    int hdr_host[HDR_WORDS] = {};     // bin counts, read back once
+};
+
 namespace {
 
 // Fraction of L2 a B column panel may occupy; panels are only used when B
@@ -111,12 +128,10 @@ struct Plan {
     int long_min;
 };
 
-template <typename T>
-Plan make_plan(const spmm_handle_s* h, int64_t k, int64_t n, const T* B, int64_t ldb, const T* C,
-               int64_t ldc) {
-    const int es = (int)sizeof(T);
+// Geometry for a product with k x n B of element size es; `vec` when B and C
+// allow 16-byte accesses (base pointers and leading dimensions).
+Plan make_plan_es(const spmm_handle_s* h, int64_t k, int64_t n, int es, bool vec) {
     const int WV = 16 / es;
-    const bool vec = aligned(B, 16) && aligned(C, 16) && ldb % WV == 0 && ldc % WV == 0;
     Plan P{};
     P.geo.W = vec ? WV : 1;
     const int W = P.geo.W;
@@ -153,6 +168,14 @@ Plan make_plan(const spmm_handle_s* h, int64_t k, int64_t n, const T* B, int64_t
     P.long_min = LONG_MIN_ROW;
     P.short_max = (P.geo.G == 32) ? P.long_min - 1 : std::min(P.long_min - 1, 2 * CH);
     return P;
+}
+
+template <typename T>
+Plan make_plan(const spmm_handle_s* h, int64_t k, int64_t n, const T* B, int64_t ldb, const T* C,
+               int64_t ldc) {
+    const int WV = 16 / (int)sizeof(T);
+    const bool vec = aligned(B, 16) && aligned(C, 16) && ldb % WV == 0 && ldc % WV == 0;
+    return make_plan_es(h, k, n, (int)sizeof(T), vec);
 }
 
 int rows_grid(spmm_handle_s* h, int es, const Geometry& g) {
@@ -270,6 +293,85 @@ spmm_status_t spmm_csr_impl(spmm_handle_t h, T alpha, const int32_t* row_ptr,
         h->prof.short_max = P.short_max;
         h->prof.long_min = P.long_min;
         h->prof_hdr = bs.hdr;
+        h->have_profile = true;
+    }
+    return SPMM_OK;
+}
+
+template <typename T>
+spmm_status_t spmm_plan_impl(spmm_plan_t pl, T alpha, const int32_t* row_ptr,
+                             const int32_t* col_idx, const T* values, const T* B, int64_t ldb,
+                             T beta, T* C, int64_t ldc, void* stream) {
+    if (!pl || pl->es != (int)sizeof(T)) return SPMM_ERR_INVALID_ARGUMENT;
+    spmm_handle_s* h = pl->h;
+    const int64_t m = pl->m, k = pl->k, n = pl->n;
+    if (ldb < std::max<int64_t>(1, n) || ldc < std::max<int64_t>(1, n))
+        return SPMM_ERR_DIMENSION_MISMATCH;
+    if (m == 0 || n == 0) return SPMM_OK;
+    if (!C) return SPMM_ERR_NULL_POINTER;
+    const bool uses_a = alpha != T(0) && k > 0;
+    if (uses_a && (!row_ptr || !col_idx || !values || !B)) return SPMM_ERR_NULL_POINTER;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device) {
+        cudaGetLastError();
+        return SPMM_ERR_INVALID_ARGUMENT;
+    }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (!uses_a) {
+        if (h->profiling) {
+            h->prof = spmm_profile_t{};
+            h->prof.launches = 1;
+            h->prof_hdr = nullptr;
+            for (int i = 0; i < 5; ++i) mark(h, i, st);
+            h->have_profile = true;
+        }
+        return launch_scale<T>(C, ldc, (int)m, (int)n, beta, h->num_sms * 8, st) == cudaSuccess
+                   ? SPMM_OK : SPMM_ERR_CUDA;
+    }
+    const Plan P = make_plan<T>(h, k, n, B, ldb, C, ldc);
+    SpmmParams<T> p{};
+    p.row_ptr = row_ptr;
+    p.col_idx = col_idx;
+    p.values = values;
+    p.B = B;
+    p.ldb = ldb;
+    p.C = C;
+    p.ldc = ldc;
+    p.m = (int)m;
+    p.n = (int)n;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.panel_cols = P.panel_cols;
+    p.npanels = P.npanels;
+    p.rowlist = pl->rowlist;
+    p.med_pre = pl->med_pre;
+    p.long_pre = pl->long_pre;
+    p.long_cnt = pl->long_cnt;
+    p.hdr = pl->hdr;
+    p.partials = static_cast<T*>(pl->partials);
+    p.long_grid = pl->long_grid;
+    const bool overlap = SPMM_PDL && !h->profiling;
+    const bool has_long = pl->hdr_host[HDR_COUNT_LONG] > 0;
+    mark(h, 0, st);
+    mark(h, 1, st);                       // no pre-pass: the plan holds the bins
+    // the first kernel of the call waits for the stream (no launch overlap)
+    if (launch_rows<T>(p, P.geo, rows_grid(h, (int)sizeof(T), P.geo), st, false) != cudaSuccess)
+        return SPMM_ERR_CUDA;
+    mark(h, 2, st);
+    if (has_long && launch_long<T>(p, P.geo, st, overlap) != cudaSuccess) return SPMM_ERR_CUDA;
+    mark(h, 3, st);
+    mark(h, 4, st);
+    if (h->profiling) {
+        h->prof = spmm_profile_t{};
+        h->prof.launches = has_long ? 2 : 1;
+        h->prof.panels = P.npanels;
+        h->prof.panel_cols = P.panel_cols;
+        h->prof.vec_elems = P.geo.W;
+        h->prof.group_lanes = P.geo.G;
+        h->prof.slots = P.geo.R;
+        h->prof.short_max = P.short_max;
+        h->prof.long_min = P.long_min;
+        h->prof_hdr = pl->hdr;
         h->have_profile = true;
     }
     return SPMM_OK;
@@ -430,6 +532,92 @@ spmm_status_t spmm_get_profile(spmm_handle_t h, spmm_profile_t* out) {
     }
     *out = p;
     return SPMM_OK;
+}
+
+spmm_status_t spmm_plan_create(spmm_handle_t h, spmm_plan_t* out, const int32_t* row_ptr,
+                               int64_t m, int64_t k, int64_t n, int elem_size, void* stream) {
+    if (!out) return SPMM_ERR_NULL_POINTER;
+    *out = nullptr;
+    if (!h || m < 0 || k < 0 || n < 0 || (elem_size != 4 && elem_size != 8))
+        return SPMM_ERR_INVALID_ARGUMENT;
+    if (m > (int64_t)INT_MAX - BIN_TILE || k > (int64_t)INT_MAX || n > (int64_t)INT_MAX)
+        return SPMM_ERR_INVALID_ARGUMENT;
+    if (m > 0 && !row_ptr) return SPMM_ERR_NULL_POINTER;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device) {
+        cudaGetLastError();
+        return SPMM_ERR_INVALID_ARGUMENT;
+    }
+    spmm_plan_s* pl = new (std::nothrow) spmm_plan_s();
+    if (!pl) return SPMM_ERR_ALLOC;
+    pl->h = h;
+    pl->m = m;
+    pl->k = k;
+    pl->n = n;
+    pl->es = elem_size;
+    pl->long_grid = long_grid_of(h);
+    const ScratchLayout L = layout_for(m, n, elem_size, pl->long_grid);
+    if (cudaMalloc(&pl->scratch, L.total) != cudaSuccess) {
+        cudaGetLastError();
+        delete pl;
+        return SPMM_ERR_ALLOC;
+    }
+    char* base = static_cast<char*>(pl->scratch);
+    BinScratch bs{};
+    bs.hdr = pl->hdr = reinterpret_cast<int*>(base + L.hdr);
+    bs.tile_counts = reinterpret_cast<int*>(base + L.tile_counts);
+    bs.tile_offsets = reinterpret_cast<int*>(base + L.tile_offsets);
+    bs.rowlist = pl->rowlist = reinterpret_cast<int*>(base + L.rowlist);
+    bs.med_pre = pl->med_pre = reinterpret_cast<int*>(base + L.med_pre);
+    bs.long_pre = pl->long_pre = reinterpret_cast<int*>(base + L.long_pre);
+    bs.long_cnt = pl->long_cnt = reinterpret_cast<int*>(base + L.long_cnt);
+    pl->partials = base + L.partials;
+    bin_geometry(m, &bs.items, &bs.tiles);
+    // bins for 16-byte-aligned operands (the usual case); products issued with
+    // other alignments use the same bins, which are valid for any geometry
+    const Plan P = make_plan_es(h, k, n, elem_size, true);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (m > 0 && n > 0 && k > 0) {
+        if (launch_binning(row_ptr, (int)m, P.short_max, P.long_min, bs, st, SPMM_PDL) !=
+                cudaSuccess ||
+            cudaMemcpyAsync(pl->hdr_host, pl->hdr, sizeof(pl->hdr_host), cudaMemcpyDeviceToHost,
+                            st) != cudaSuccess ||
+            cudaStreamSynchronize(st) != cudaSuccess) {
+            cudaGetLastError();
+            cudaFree(pl->scratch);
+            delete pl;
+            return SPMM_ERR_CUDA;
+        }
+    }
+    *out = pl;
+    return SPMM_OK;
+}
+
+spmm_status_t spmm_plan_destroy(spmm_plan_t pl) {
+    if (!pl) return SPMM_OK;
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != pl->h->device) cudaSetDevice(pl->h->device);
+    cudaDeviceSynchronize();
+    cudaFree(pl->scratch);
+    if (cur >= 0 && cur != pl->h->device) cudaSetDevice(cur);
+    cudaGetLastError();
+    delete pl;
+    return SPMM_OK;
+}
+
+spmm_status_t spmm_plan_csr_f32(spmm_plan_t plan, float alpha, const int32_t* row_ptr,
+                                const int32_t* col_idx, const float* values, const float* B,
+                                int64_t ldb, float beta, float* C, int64_t ldc, void* stream) {
+    return spmm_plan_impl<float>(plan, alpha, row_ptr, col_idx, values, B, ldb, beta, C, ldc,
+                                 stream);
+}
+
+spmm_status_t spmm_plan_csr_f64(spmm_plan_t plan, double alpha, const int32_t* row_ptr,
+                                const int32_t* col_idx, const double* values, const double* B,
+                                int64_t ldb, double beta, double* C, int64_t ldc, void* stream) {
+    return spmm_plan_impl<double>(plan, alpha, row_ptr, col_idx, values, B, ldb, beta, C, ldc,
+                                  stream);
 }
 
 const char* spmm_status_string(spmm_status_t s) {

@@ -165,8 +165,8 @@ __device__ __forceinline__ void write_row_c0(T* __restrict__ Crow, const T (&acc
 }
 
 // ---------------------------------------------------------------------------
-// A warp works through rows list[r0 .. r1) of one bin, for the panel of pw
-// columns starting at c0.
+// A warp works through rows list[first + i * stride], i < count, of one bin,
+// for the panel of pw columns starting at c0col.
 //   MEDIUM == false (short rows): group gi takes rows gi, gi + RPW, ... of
 //     every 32-row block; each group walks its own row CH entries per step.
 //   MEDIUM == true (medium rows): the whole warp takes one row at a time;
@@ -175,7 +175,8 @@ __device__ __forceinline__ void write_row_c0(T* __restrict__ Crow, const T (&acc
 // ---------------------------------------------------------------------------
 template <typename T, int W, int G, int R, bool MEDIUM, bool READ_C>
 __device__ __forceinline__ void process_rows(const SpmmParams<T>& p, const int* __restrict__ list,
-                                             int r0, int r1, int c0col, int pw, uint64_t pol_s) {
+                                             int first, int count, int stride, int c0col, int pw,
+                                             uint64_t pol_s) {
     using C = Cfg<T, W, G, R>;
     constexpr int Q = C::Q;
     const int lane = threadIdx.x & 31;
@@ -186,11 +187,11 @@ __device__ __forceinline__ void process_rows(const SpmmParams<T>& p, const int* 
     const int nvec = (pw + W - 1) / W;
     const T* Bp = p.B + c0col;
 
-    for (int sub = r0; sub < r1; sub += 32) {
-        const int nrows = min(32, r1 - sub);
+    for (int sub = 0; sub < count; sub += 32) {
+        const int nrows = min(32, count - sub);
         int my_row = -1, my_e0 = 0, my_len = 0;
         if (lane < nrows) {
-            my_row = list[sub + lane];
+            my_row = list[first + (int64_t)(sub + lane) * stride];
             my_e0 = p.row_ptr[my_row];
             my_len = p.row_ptr[my_row + 1] - my_e0;
         }
@@ -280,6 +281,10 @@ __device__ __forceinline__ int medium_lower_bound(const int* __restrict__ med_pr
     return lo;
 }
 
+#ifndef SPMM_SHORT_INTERLEAVE
+#define SPMM_SHORT_INTERLEAVE 1
+#endif
+
 template <typename T>
 struct RowsOccupancy {
     static constexpr int MIN_BLOCKS = sizeof(T) == 8 ? SPMM_ROWS_MIN_BLOCKS_F64 : SPMM_ROWS_MIN_BLOCKS;
@@ -298,7 +303,19 @@ rows_kernel(SpmmParams<T> p) {
     const int64_t nwarps = (int64_t)gridDim.x * (ROWS_THREADS / 32);
     const int64_t w = (int64_t)blockIdx.x * (ROWS_THREADS / 32) + (threadIdx.x >> 5);
     // short rows: equal counts per warp; medium rows: equal entries per warp
-    const int s0 = (int)(w * n_short / nwarps), s1 = (int)((w + 1) * n_short / nwarps);
+    // short rows: each CTA takes an equal contiguous range of the short list and
+    // its warps interleave over it (warp j: rows j, j + 8, ...), so rows that
+    // sit next to each other in the list run at the same time on the same SM
+    constexpr int WPB = ROWS_THREADS / 32;
+    const int64_t nblk = gridDim.x;
+    const int cs0 = (int)((int64_t)blockIdx.x * n_short / nblk);
+    const int cs1 = (int)((int64_t)(blockIdx.x + 1) * n_short / nblk);
+    const int wib = threadIdx.x >> 5;
+    const int s_first = SPMM_SHORT_INTERLEAVE ? cs0 + wib : (int)(w * n_short / nwarps);
+    const int s_count = SPMM_SHORT_INTERLEAVE
+                            ? max(0, (cs1 - cs0 - wib + WPB - 1) / WPB)
+                            : (int)((w + 1) * n_short / nwarps) - (int)(w * n_short / nwarps);
+    const int s_stride = SPMM_SHORT_INTERLEAVE ? WPB : 1;
     int m0 = 0, m1 = 0;
     if (n_med > 0) {
         m0 = medium_lower_bound(p.med_pre, n_med, w * med_nnz / nwarps);
@@ -308,10 +325,12 @@ rows_kernel(SpmmParams<T> p) {
     for (int panel = 0; panel < p.npanels; ++panel) {
         const int c0 = panel * p.panel_cols;
         const int pw = min(p.panel_cols, p.n - c0);
-        if (s1 > s0)
-            process_rows<T, W, G, R, false, READ_C>(p, p.rowlist, s0, s1, c0, pw, pol_s);
+        if (s_count > 0)
+            process_rows<T, W, G, R, false, READ_C>(p, p.rowlist, s_first, s_count, s_stride, c0,
+                                                    pw, pol_s);
         if (m1 > m0)
-            process_rows<T, W, G, R, true, READ_C>(p, p.rowlist + n_short, m0, m1, c0, pw, pol_s);
+            process_rows<T, W, G, R, true, READ_C>(p, p.rowlist + n_short, m0, m1 - m0, 1, c0, pw,
+                                                   pol_s);
     }
 }
 
@@ -501,7 +520,11 @@ long_kernel(SpmmParams<T> p) {
     for (int which = 0; which < 2; ++which) {
         if (!s_finish[which]) continue;           // uniform per CTA
         __threadfence();
-        finish_split_row<T>(p, lrows, which == 0 ? r0 : rlast, seg, read_c);
+        const int r = which == 0 ? r0 : rlast;
+        finish_split_row<T>(p, lrows, r, seg, read_c);
+        // every sharer has counted: leave the counter at zero for the next
+        // product that reuses these bins (an analysed plan)
+        if (threadIdx.x == 0) p.long_cnt[r] = 0;
     }
 }
 

@@ -119,6 +119,43 @@ spmm_status_t spmm_csr_check(spmm_handle_t h, const int32_t *row_ptr, const int3
                              int64_t m, int64_t k, int64_t nnz, void *stream,
                              int32_t *host_status);
 
+/* ---- Analysis reuse: plans ------------------------------------------------
+ * A plan holds the row bins of one sparsity structure (row_ptr of an m x k
+ * matrix) for products with n columns, so that repeated products with the same
+ * structure -- new values, new B, new C, as in an iterative solver that applies
+ * one kernel matrix every iteration -- skip the row-binning pre-pass.  The
+ * product is the same operation with the same conventions and bitwise the same
+ * results as spmm_csr_f32/f64 on the same handle.  The plan owns device
+ * scratch, allocated when it is created. */
+typedef struct spmm_plan_s *spmm_plan_t;
+
+/* Analyse row_ptr (device, m + 1 entries) on `stream` and create a plan for
+ * m x k matrices with that structure and n-column products of elem_size (4 or
+ * 8) byte elements.  Synchronises `stream` (it reads the bin counts back once).
+ * The handle must outlive the plan and serve one stream at a time, as for
+ * direct products.  CSR validity is the caller's precondition, as everywhere. */
+spmm_status_t spmm_plan_create(spmm_handle_t h, spmm_plan_t *plan, const int32_t *row_ptr,
+                               int64_t m, int64_t k, int64_t n, int elem_size, void *stream);
+
+/* Release a plan (synchronises its device).  NULL is accepted and ignored. */
+spmm_status_t spmm_plan_destroy(spmm_plan_t plan);
+
+/* C = alpha * A * B + beta * C with A's structure taken from the plan.
+ * row_ptr must hold the structure the plan analysed (same values); col_idx,
+ * values, B and C may change from call to call.  Same argument rules as
+ * spmm_csr_f32 (m, k, n come from the plan).  SPMM_ERR_INVALID_ARGUMENT if the
+ * plan was made for the other element size.  Asynchronous on `stream`. */
+spmm_status_t spmm_plan_csr_f32(spmm_plan_t plan, float alpha,
+                                const int32_t *row_ptr, const int32_t *col_idx,
+                                const float *values, const float *B, int64_t ldb,
+                                float beta, float *C, int64_t ldc, void *stream);
+
+/* Same in binary64. */
+spmm_status_t spmm_plan_csr_f64(spmm_plan_t plan, double alpha,
+                                const int32_t *row_ptr, const int32_t *col_idx,
+                                const double *values, const double *B, int64_t ldb,
+                                double beta, double *C, int64_t ldc, void *stream);
+
 /* Per-stage record of the most recent product issued on a handle with
  * profiling enabled (a tracing aid; the pages have no counterpart).  Times are
  * GPU durations between CUDA events recorded on the call's stream around each

@@ -18,13 +18,14 @@ from ._lib import (EXPORTED, SPMM_ERR_ALLOC, SPMM_ERR_CUDA, SPMM_ERR_DIMENSION_M
                    SPMM_ERR_UNSUPPORTED_DEVICE, SPMM_OK, SpmmError, library, spmm_create,
                    spmm_csr_check, spmm_csr_f32, spmm_csr_f32_noalloc, spmm_csr_f64,
                    spmm_destroy, spmm_get_profile, spmm_plan_create, spmm_plan_csr_f32,
-                   spmm_plan_csr_f64, spmm_plan_destroy,
+                   spmm_plan_csr_f64, spmm_plan_destroy, spmm_set_l2_persistence,
                    spmm_reserve, spmm_set_profiling, status_string)
 
 __all__ = ["Handle", "spmm", "csr_check", "SpmmError", "library", "spmm_create", "spmm_destroy",
            "spmm_reserve", "spmm_csr_f32", "spmm_csr_f64", "spmm_csr_check", "status_string",
            "spmm_set_profiling", "spmm_get_profile", "spmm_csr_f32_noalloc", "spmm_plan_create",
-           "spmm_plan_destroy", "spmm_plan_csr_f32", "spmm_plan_csr_f64", "Plan", "EXPORTED"]
+           "spmm_plan_destroy", "spmm_set_l2_persistence", "spmm_plan_csr_f32",
+           "spmm_plan_csr_f64", "Plan", "EXPORTED"]
 
 
 class Handle:

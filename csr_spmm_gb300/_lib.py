@@ -27,7 +27,7 @@ SPMM_ERR_TOO_LARGE = 8
 # every symbol include/csr_spmm.h declares
 EXPORTED = ("spmm_create", "spmm_destroy", "spmm_reserve", "spmm_csr_f32", "spmm_csr_f64",
             "spmm_csr_check", "spmm_set_profiling", "spmm_get_profile", "spmm_csr_f32_noalloc",
-            "spmm_plan_create", "spmm_plan_destroy", "spmm_plan_csr_f32", "spmm_plan_csr_f64",
+            "spmm_set_l2_persistence", "spmm_plan_create", "spmm_plan_destroy", "spmm_plan_csr_f32", "spmm_plan_csr_f64",
             "spmm_status_string")
 
 
@@ -89,6 +89,8 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.spmm_csr_f32_noalloc.argtypes = [ctypes.c_float, vp, vp, vp, i64, i64, vp, i64, i64,
                                          ctypes.c_float, vp, i64, vp]
     lib.spmm_csr_f32_noalloc.restype = st
+    lib.spmm_set_l2_persistence.argtypes = [vp, i64]
+    lib.spmm_set_l2_persistence.restype = st
     lib.spmm_plan_create.argtypes = [vp, ctypes.POINTER(vp), vp, i64, i64, i64, ctypes.c_int, vp]
     lib.spmm_plan_create.restype = st
     lib.spmm_plan_destroy.argtypes = [vp]
@@ -203,3 +205,8 @@ def spmm_plan_csr_f64(plan, alpha, row_ptr, col_idx, values, B, ldb, beta, C, ld
     if check:
         _check(s, "spmm_plan_csr_f64")
     return s
+
+
+def spmm_set_l2_persistence(handle, nbytes) -> None:
+    """Persisting L2 set-aside for B (0: off, < 0: device maximum)."""
+    _check(library().spmm_set_l2_persistence(handle, int(nbytes)), "spmm_set_l2_persistence")

@@ -18,6 +18,10 @@ struct spmm_handle_s {
     int device = 0;
     int num_sms = 0;
     int64_t l2_bytes = 0;
+    int64_t persist_max = 0;          // largest persisting L2 set-aside
+    int64_t window_max = 0;           // largest access-policy window
+    int64_t persist_bytes = 0;        // set-aside this handle asked for (0: off)
+    size_t persist_prev = 0;          // the limit before, restored on destroy
     void* scratch = nullptr;
     size_t scratch_bytes = 0;
     int* check_status = nullptr;
@@ -178,6 +182,23 @@ Plan make_plan(const spmm_handle_s* h, int64_t k, int64_t n, const T* B, int64_t
     return make_plan_es(h, k, n, (int)sizeof(T), vec);
 }
 
+// Access-policy window over the B rows a product gathers, when the handle
+// holds a persisting L2 set-aside and B's span fits in it: B's lines then
+// persist, and the A and C streams cannot evict them.  A B larger than the
+// set-aside gets no window (measured on GB300: persisting a fraction of a
+// larger B slowed the product by 5-10%).
+template <typename T>
+const L2Window* b_window(const spmm_handle_s* h, const T* B, int64_t k, int64_t ldb, int64_t n,
+                         L2Window* w) {
+    if (h->persist_bytes <= 0 || k <= 0 || n <= 0) return nullptr;
+    const double span = ((double)(k - 1) * (double)ldb + (double)n) * sizeof(T);
+    if (span > (double)h->persist_bytes || span > (double)h->window_max) return nullptr;
+    w->base = B;
+    w->bytes = (size_t)span;
+    w->hit_ratio = 1.0f;
+    return w;
+}
+
 int rows_grid(spmm_handle_s* h, int es, const Geometry& g) {
     for (int i = 0; i < h->nocc; ++i) {
         const auto& e = h->occ[i];
@@ -276,10 +297,13 @@ spmm_status_t spmm_csr_impl(spmm_handle_t h, T alpha, const int32_t* row_ptr,
     p.partials = reinterpret_cast<T*>(base + L.partials);
     p.long_grid = lg;
 
-    if (launch_rows<T>(p, P.geo, rows_grid(h, (int)sizeof(T), P.geo), st, overlap) != cudaSuccess)
+    L2Window wbuf;
+    const L2Window* win = b_window(h, B, k, ldb, n, &wbuf);
+    if (launch_rows<T>(p, P.geo, rows_grid(h, (int)sizeof(T), P.geo), st, overlap, win) !=
+        cudaSuccess)
         return SPMM_ERR_CUDA;
     mark(h, 2, st);
-    if (launch_long<T>(p, P.geo, st, overlap) != cudaSuccess) return SPMM_ERR_CUDA;
+    if (launch_long<T>(p, P.geo, st, overlap, win) != cudaSuccess) return SPMM_ERR_CUDA;
     mark(h, 3, st);
     mark(h, 4, st);               // the fixup runs inside the long-row launch
     if (h->profiling) {
@@ -355,10 +379,14 @@ spmm_status_t spmm_plan_impl(spmm_plan_t pl, T alpha, const int32_t* row_ptr,
     mark(h, 0, st);
     mark(h, 1, st);                       // no pre-pass: the plan holds the bins
     // the first kernel of the call waits for the stream (no launch overlap)
-    if (launch_rows<T>(p, P.geo, rows_grid(h, (int)sizeof(T), P.geo), st, false) != cudaSuccess)
+    L2Window wbuf;
+    const L2Window* win = b_window(h, B, k, ldb, n, &wbuf);
+    if (launch_rows<T>(p, P.geo, rows_grid(h, (int)sizeof(T), P.geo), st, false, win) !=
+        cudaSuccess)
         return SPMM_ERR_CUDA;
     mark(h, 2, st);
-    if (has_long && launch_long<T>(p, P.geo, st, overlap) != cudaSuccess) return SPMM_ERR_CUDA;
+    if (has_long && launch_long<T>(p, P.geo, st, overlap, win) != cudaSuccess)
+        return SPMM_ERR_CUDA;
     mark(h, 3, st);
     mark(h, 4, st);
     if (h->profiling) {
@@ -405,6 +433,13 @@ spmm_status_t spmm_create(spmm_handle_t* out, int device) {
     h->device = device;
     h->num_sms = sms;
     h->l2_bytes = l2;
+    int pmax = 0, wmax = 0;
+    if (cudaDeviceGetAttribute(&pmax, cudaDevAttrMaxPersistingL2CacheSize, device) == cudaSuccess &&
+        cudaDeviceGetAttribute(&wmax, cudaDevAttrMaxAccessPolicyWindowSize, device) == cudaSuccess) {
+        h->persist_max = pmax;
+        h->window_max = wmax;
+    }
+    cudaGetLastError();
     *out = h;
     return SPMM_OK;
 }
@@ -419,6 +454,10 @@ spmm_status_t spmm_destroy(spmm_handle_t h) {
         if (e) cudaEventDestroy(e);
     if (h->scratch) cudaFree(h->scratch);
     if (h->check_status) cudaFree(h->check_status);
+    if (h->persist_bytes > 0) {
+        cudaCtxResetPersistingL2Cache();
+        cudaDeviceSetLimit(cudaLimitPersistingL2CacheSize, h->persist_prev);
+    }
     if (cur >= 0 && cur != h->device) cudaSetDevice(cur);
     cudaGetLastError();
     delete h;
@@ -618,6 +657,40 @@ spmm_status_t spmm_plan_csr_f64(spmm_plan_t plan, double alpha, const int32_t* r
                                 int64_t ldb, double beta, double* C, int64_t ldc, void* stream) {
     return spmm_plan_impl<double>(plan, alpha, row_ptr, col_idx, values, B, ldb, beta, C, ldc,
                                   stream);
+}
+
+spmm_status_t spmm_set_l2_persistence(spmm_handle_t h, int64_t bytes) {
+    if (!h) return SPMM_ERR_INVALID_ARGUMENT;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device) {
+        cudaGetLastError();
+        return SPMM_ERR_INVALID_ARGUMENT;
+    }
+    if (bytes == 0) {
+        if (h->persist_bytes > 0) {
+            cudaError_t e1 = cudaCtxResetPersistingL2Cache();
+            cudaError_t e2 = cudaDeviceSetLimit(cudaLimitPersistingL2CacheSize, h->persist_prev);
+            h->persist_bytes = 0;
+            if (e1 != cudaSuccess || e2 != cudaSuccess) {
+                cudaGetLastError();
+                return SPMM_ERR_CUDA;
+            }
+        }
+        return SPMM_OK;
+    }
+    if (h->persist_max <= 0 || h->window_max <= 0) return SPMM_ERR_UNSUPPORTED_DEVICE;
+    const int64_t want = bytes < 0 ? h->persist_max : std::min(bytes, h->persist_max);
+    if (h->persist_bytes == 0 &&
+        cudaDeviceGetLimit(&h->persist_prev, cudaLimitPersistingL2CacheSize) != cudaSuccess) {
+        cudaGetLastError();
+        return SPMM_ERR_CUDA;
+    }
+    if (cudaDeviceSetLimit(cudaLimitPersistingL2CacheSize, (size_t)want) != cudaSuccess) {
+        cudaGetLastError();
+        return SPMM_ERR_CUDA;
+    }
+    h->persist_bytes = want;
+    return SPMM_OK;
 }
 
 const char* spmm_status_string(spmm_status_t s) {

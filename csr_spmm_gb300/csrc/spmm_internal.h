@@ -52,9 +52,18 @@ constexpr int ROWS_THREADS = 256;
 #ifndef SPMM_ROWS_MIN_BLOCKS_F64
 #define SPMM_ROWS_MIN_BLOCKS_F64 6
 #endif
+// binary32 rows kernels with 16-byte vectors and lane groups narrower than a
+// warp (n <= 64 columns per panel): twice the gathers in flight per lane, at
+// one resident block fewer (measured faster on power-law and wide-N inputs)
+#ifndef SPMM_ROWS_MIN_BLOCKS_NARROW
+#define SPMM_ROWS_MIN_BLOCKS_NARROW 3
+#endif
 // B bytes each lane keeps in flight per gather batch, and the batch cap.
 #ifndef SPMM_BATCH_BYTES
 #define SPMM_BATCH_BYTES 64
+#endif
+#ifndef SPMM_BATCH_BYTES_NARROW
+#define SPMM_BATCH_BYTES_NARROW 128
 #endif
 #ifndef SPMM_BATCH_BYTES_F64
 #define SPMM_BATCH_BYTES_F64 16
@@ -120,6 +129,14 @@ struct Geometry {
     int R;        // vector slots per lane per column pass (1..4)
 };
 
+// An L2 access-policy window for one launch: accesses to [base, base + bytes)
+// are marked persisting with probability hit_ratio (the rest are normal).
+struct L2Window {
+    const void* base;
+    size_t bytes;
+    float hit_ratio;
+};
+
 // ---- pre-pass (spmm_bin.cu) ----
 // `overlap`: launch the dependent kernels of the chain with programmatic
 // dependent launch (the first kernel of a call always waits for the stream).
@@ -129,9 +146,10 @@ cudaError_t launch_binning(const int* row_ptr, int m, int short_max, int long_mi
 // ---- per-bin kernels (spmm_rows_*.cu, spmm_long_*.cu) ----
 template <typename T>
 cudaError_t launch_rows(const SpmmParams<T>& p, const Geometry& g, int grid, cudaStream_t st,
-                        bool overlap);
+                        bool overlap, const L2Window* win = nullptr);
 template <typename T>
-cudaError_t launch_long(const SpmmParams<T>& p, const Geometry& g, cudaStream_t st, bool overlap);
+cudaError_t launch_long(const SpmmParams<T>& p, const Geometry& g, cudaStream_t st, bool overlap,
+                        const L2Window* win = nullptr);
 
 // ---- epilogue-only and checking kernels (spmm_misc.cu) ----
 template <typename T>
@@ -163,21 +181,43 @@ __device__ __forceinline__ void allow_successor() {
 }
 
 // Launch `kernel` on `st`, overlapping its launch with the previous kernel
-// of the stream when `overlap` is set.
+// of the stream when `overlap` is set, with an L2 access-policy window on
+// this launch alone when `win` is given (the stream's attributes are left
+// untouched).
 template <typename... KArgs, typename... Args>
-inline cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                                  cudaStream_t st, bool overlap, Args... args) {
+inline cudaError_t launch_windowed(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                   cudaStream_t st, bool overlap, const L2Window* win,
+                                   Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (overlap) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (win && win->bytes > 0) {
+        attr[n].id = cudaLaunchAttributeAccessPolicyWindow;
+        attr[n].val.accessPolicyWindow.base_ptr = const_cast<void*>(win->base);
+        attr[n].val.accessPolicyWindow.num_bytes = win->bytes;
+        attr[n].val.accessPolicyWindow.hitRatio = win->hit_ratio;
+        attr[n].val.accessPolicyWindow.hitProp = cudaAccessPropertyPersisting;
+        attr[n].val.accessPolicyWindow.missProp = cudaAccessPropertyNormal;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = overlap ? 1 : 0;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                  cudaStream_t st, bool overlap, Args... args) {
+    return launch_windowed(kernel, grid, block, smem, st, overlap, nullptr, args...);
 }
 
 }  // namespace spmm

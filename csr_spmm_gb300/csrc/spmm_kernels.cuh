@@ -30,17 +30,26 @@
 
 namespace spmm {
 
-template <typename T, int W, int G, int R>
+// binary32, 16-byte vectors, lane groups narrower than a warp
+template <typename T, int W, int G>
+constexpr bool narrow_f32() { return sizeof(T) == 4 && W * (int)sizeof(T) == 16 && G < 32; }
+
+// ROWS: the short/medium-row kernel (narrow binary32 groups take the larger
+// batch there; the long-row kernel keeps the general one).
+template <typename T, int W, int G, int R, bool ROWS = false>
 struct Cfg {
     static_assert(G >= 1 && G <= 32 && (G & (G - 1)) == 0, "G must be a power of two <= 32");
     static constexpr int SLOTS = G * R;                       // vectors per column pass
     static constexpr int BYTES_PER_ENTRY = R * W * (int)sizeof(T);
-    static constexpr int BATCH_BYTES = sizeof(T) == 8 ? SPMM_BATCH_BYTES_F64 : SPMM_BATCH_BYTES;
+    static constexpr int BATCH_BYTES = sizeof(T) == 8 ? SPMM_BATCH_BYTES_F64
+                                       : (ROWS && narrow_f32<T, W, G>()) ? SPMM_BATCH_BYTES_NARROW
+                                                               : SPMM_BATCH_BYTES;
     static constexpr int U0 = BATCH_BYTES / BYTES_PER_ENTRY;        // B bytes in flight/lane
     static constexpr int U = U0 < 1 ? 1 : (U0 > SPMM_BATCH_MAX ? SPMM_BATCH_MAX : U0);
     static constexpr int CH = G > U ? G : U;                  // entries per group per step
     static constexpr int Q = CH / G;                          // (col, value) loads per lane per step
     static constexpr int RPW = 32 / G;                        // groups per warp
+    static_assert(CH % U == 0, "a step must hold whole batches");
 };
 
 template <typename T, int W, int R>
@@ -72,12 +81,13 @@ __device__ __forceinline__ void load_entries(int (&col)[Q], T (&val)[Q],
 
 // One step: the group consumes its `cnt` (<= CH) entries held in (col, val),
 // in batches of U; `cmax` is a warp-uniform upper bound on every group's cnt.
-template <typename T, int W, int G, int R>
-__device__ __forceinline__ void consume_step(T (&acc)[R][W], const int (&col)[Cfg<T, W, G, R>::Q],
-                                             const T (&val)[Cfg<T, W, G, R>::Q], int cnt,
+template <typename T, int W, int G, int R, bool ROWS = false>
+__device__ __forceinline__ void consume_step(T (&acc)[R][W],
+                                             const int (&col)[Cfg<T, W, G, R, ROWS>::Q],
+                                             const T (&val)[Cfg<T, W, G, R, ROWS>::Q], int cnt,
                                              int cmax, const T* __restrict__ Bp, int64_t ldb,
                                              int vbase, int pw) {
-    using C = Cfg<T, W, G, R>;
+    using C = Cfg<T, W, G, R, ROWS>;
     const int g = (threadIdx.x & 31) & (G - 1);
 #pragma unroll
     for (int j0 = 0; j0 < C::CH; j0 += C::U) {
@@ -177,7 +187,7 @@ template <typename T, int W, int G, int R, bool MEDIUM, bool READ_C>
 __device__ __forceinline__ void process_rows(const SpmmParams<T>& p, const int* __restrict__ list,
                                              int first, int count, int stride, int c0col, int pw,
                                              uint64_t pol_s) {
-    using C = Cfg<T, W, G, R>;
+    using C = Cfg<T, W, G, R, true>;
     constexpr int Q = C::Q;
     const int lane = threadIdx.x & 31;
     const int gi = lane / G;
@@ -234,7 +244,7 @@ __device__ __forceinline__ void process_rows(const SpmmParams<T>& p, const int* 
                 const int cnt = active ? min(C::CH, len - s - goff) : 0;
                 const int cmax = MEDIUM ? min(C::CH, len - s)
                                         : (int)__reduce_max_sync(FULL, (unsigned)max(cnt, 0));
-                consume_step<T, W, G, R>(acc, colc, valc, cnt, cmax, Bp, p.ldb, vbase, pw);
+                consume_step<T, W, G, R, true>(acc, colc, valc, cnt, cmax, Bp, p.ldb, vbase, pw);
 
                 if (s + ESTEP >= len) {                     // row finished (uniform if MEDIUM)
                     if (MEDIUM) combine_groups<T, W, G, R>(acc);
@@ -285,14 +295,16 @@ __device__ __forceinline__ int medium_lower_bound(const int* __restrict__ med_pr
 #define SPMM_SHORT_INTERLEAVE 1
 #endif
 
-template <typename T>
+template <typename T, int W, int G>
 struct RowsOccupancy {
-    static constexpr int MIN_BLOCKS = sizeof(T) == 8 ? SPMM_ROWS_MIN_BLOCKS_F64 : SPMM_ROWS_MIN_BLOCKS;
+    static constexpr int MIN_BLOCKS = sizeof(T) == 8 ? SPMM_ROWS_MIN_BLOCKS_F64
+                                      : narrow_f32<T, W, G>() ? SPMM_ROWS_MIN_BLOCKS_NARROW
+                                                              : SPMM_ROWS_MIN_BLOCKS;
 };
 
 // READ_C: beta != 0 (C is read, and prefetched at each row start).
 template <typename T, int W, int G, int R, bool READ_C>
-__global__ void __launch_bounds__(ROWS_THREADS, RowsOccupancy<T>::MIN_BLOCKS)
+__global__ void __launch_bounds__(ROWS_THREADS, RowsOccupancy<T, W, G>::MIN_BLOCKS)
 rows_kernel(SpmmParams<T> p) {
     wait_for_predecessor();
     allow_successor();

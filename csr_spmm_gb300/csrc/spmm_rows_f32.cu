@@ -6,13 +6,13 @@ namespace spmm {
 
 template <>
 cudaError_t launch_rows<float>(const SpmmParams<float>& p, const Geometry& g, int grid,
-                               cudaStream_t st, bool overlap) {
+                               cudaStream_t st, bool overlap, const L2Window* win) {
     return dispatch_geometry<float>(g, [&]<int W, int G, int R>() -> cudaError_t {
         if (p.beta != float(0))
-            return launch_chained(rows_kernel<float, W, G, R, true>, dim3(grid), dim3(ROWS_THREADS),
-                                  0, st, overlap, p);
-        return launch_chained(rows_kernel<float, W, G, R, false>, dim3(grid), dim3(ROWS_THREADS), 0,
-                              st, overlap, p);
+            return launch_windowed(rows_kernel<float, W, G, R, true>, dim3(grid), dim3(ROWS_THREADS),
+                                  0, st, overlap, win, p);
+        return launch_windowed(rows_kernel<float, W, G, R, false>, dim3(grid), dim3(ROWS_THREADS), 0,
+                              st, overlap, win, p);
     });
 }
 

@@ -119,6 +119,22 @@ spmm_status_t spmm_csr_check(spmm_handle_t h, const int32_t *row_ptr, const int3
                              int64_t m, int64_t k, int64_t nnz, void *stream,
                              int32_t *host_status);
 
+/* Persisting L2 for B.  With `bytes` > 0 (or < 0 for the device maximum,
+ * about 81 MiB on GB300) the handle sets the process's
+ * persisting-L2 set-aside to that size (cudaLimitPersistingL2CacheSize), and
+ * every later product on the handle whose B span fits in the set-aside
+ * launches with an access-policy window over B (hit ratio 1, persisting), so
+ * that the streamed A entries and C stores cannot evict B rows between their
+ * gathers.  Products with a larger B get no window.  bytes == 0 demotes all
+ * persisting lines (cudaCtxResetPersistingL2Cache) and puts the previous
+ * set-aside back; spmm_destroy does the same.  The set-aside belongs to the
+ * whole CUDA context, so other kernels of the process see less L2 while it is
+ * on: off by default.  Not synchronising.  SPMM_ERR_UNSUPPORTED_DEVICE if the
+ * device has no persisting L2.  The pages place an access-policy window on B
+ * without further detail; this is that window, made optional because GB300
+ * measurements show a small gain only when B fits the set-aside. */
+spmm_status_t spmm_set_l2_persistence(spmm_handle_t h, int64_t bytes);
+
 /* ---- Analysis reuse: plans ------------------------------------------------
  * A plan holds the row bins of one sparsity structure (row_ptr of an m x k
  * matrix) for products with n columns, so that repeated products with the same

@@ -226,6 +226,7 @@ spmm_status_t spmm_csr_impl(spmm_handle_t h, T alpha, const int32_t* row_ptr,
         return SPMM_ERR_INVALID_ARGUMENT;
     if (ldb < std::max<int64_t>(1, n) || ldc < std::max<int64_t>(1, n))
         return SPMM_ERR_DIMENSION_MISMATCH;
+    if (ldb > (int64_t)INT_MAX) return SPMM_ERR_INVALID_ARGUMENT;   // 32-bit gather offsets
     if (m == 0 || n == 0) return SPMM_OK;             // nothing to compute (as on the page)
     if (!C) return SPMM_ERR_NULL_POINTER;
     const bool uses_a = alpha != T(0) && k > 0;
@@ -331,6 +332,7 @@ spmm_status_t spmm_plan_impl(spmm_plan_t pl, T alpha, const int32_t* row_ptr,
     const int64_t m = pl->m, k = pl->k, n = pl->n;
     if (ldb < std::max<int64_t>(1, n) || ldc < std::max<int64_t>(1, n))
         return SPMM_ERR_DIMENSION_MISMATCH;
+    if (ldb > (int64_t)INT_MAX) return SPMM_ERR_INVALID_ARGUMENT;   // 32-bit gather offsets
     if (m == 0 || n == 0) return SPMM_OK;
     if (!C) return SPMM_ERR_NULL_POINTER;
     const bool uses_a = alpha != T(0) && k > 0;

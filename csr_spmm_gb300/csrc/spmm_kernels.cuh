@@ -79,40 +79,81 @@ __device__ __forceinline__ void load_entries(int (&col)[Q], T (&val)[Q],
     }
 }
 
+// This lane's B vectors in one column pass: where each of its R vectors
+// starts (panel base + element offset) and how many of its W elements lie in
+// the panel.  A lane whose vector starts past the panel's last column re-reads
+// the panel's last vector instead: those addresses fall in the lines the other
+// lanes of the row fetch anyway, so they add no traffic, and that lane's sums
+// are never stored.  Every gather of a valid entry is then unpredicated.
+template <typename T, int W, int R>
+struct LaneVecs {
+    const T* base[R];
+    int cnt[R];
+};
+
+template <typename T, int W, int G, int R>
+__device__ __forceinline__ LaneVecs<T, W, R> lane_vecs(const T* __restrict__ Bp, int vbase,
+                                                       int pw) {
+    const int g = (threadIdx.x & 31) & (G - 1);
+    const int last = ((pw - 1) / W) * W;
+    LaneVecs<T, W, R> lv;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int c = (vbase + g + G * r) * W;
+        const int ce = c < pw ? c : last;
+        lv.base[r] = Bp + ce;
+        lv.cnt[r] = min(W, pw - ce);
+    }
+    return lv;
+}
+
+template <typename T, int W>
+__device__ __forceinline__ void gather_b(const T* p, int cnt, T (&v)[W]) {
+    if (W == 1 || cnt == W) BLoad<T, W>::run(p, v);
+    else load_b_partial<T, W>(p, cnt, v);
+}
+
 // One step: the group consumes its `cnt` (<= CH) entries held in (col, val),
-// in batches of U; `cmax` is a warp-uniform upper bound on every group's cnt.
+// in batches of U.  cmax / cmin are warp-uniform bounds on every group's cnt:
+// batches below cmin are whole for every group and gather without checks.
+// Entries past a row's end were loaded with value 0 (load_entries).
 template <typename T, int W, int G, int R, bool ROWS = false>
 __device__ __forceinline__ void consume_step(T (&acc)[R][W],
                                              const int (&col)[Cfg<T, W, G, R, ROWS>::Q],
                                              const T (&val)[Cfg<T, W, G, R, ROWS>::Q], int cnt,
-                                             int cmax, const T* __restrict__ Bp, int64_t ldb,
-                                             int vbase, int pw) {
+                                             int cmax, int cmin, int ldb,
+                                             const LaneVecs<T, W, R>& lv) {
     using C = Cfg<T, W, G, R, ROWS>;
-    const int g = (threadIdx.x & 31) & (G - 1);
 #pragma unroll
     for (int j0 = 0; j0 < C::CH; j0 += C::U) {
         if (j0 >= cmax) break;                          // warp-uniform
         T bv[C::U][R][W];
         T av[C::U];
+        if (j0 + C::U <= cmin) {                        // warp-uniform: whole batch
 #pragma unroll
-        for (int u = 0; u < C::U; ++u) {
-            const int j = j0 + u;                       // compile-time after unrolling
-            const int q = j / G;
-            const int src = j % G;
-            const int cj = __shfl_sync(FULL, col[q], src, G);
-            const T aj = __shfl_sync(FULL, val[q], src, G);
-            const bool ok = j < cnt;
-            av[u] = ok ? aj : T(0);
-            const T* brow = Bp + (int64_t)cj * ldb;
+            for (int u = 0; u < C::U; ++u) {
+                const int j = j0 + u;                   // compile-time after unrolling
+                const int cj = __shfl_sync(FULL, col[j / G], j % G, G);
+                av[u] = __shfl_sync(FULL, val[j / G], j % G, G);
+                const int64_t roff = (int64_t)cj * ldb;
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const int c = (vbase + g + G * r) * W;
-                if (ok && c < pw) {
-                    if (c + W <= pw) BLoad<T, W>::run(brow + c, bv[u][r]);
-                    else load_b_partial<T, W>(brow + c, pw - c, bv[u][r]);
-                } else {
+                for (int r = 0; r < R; ++r) gather_b<T, W>(lv.base[r] + roff, lv.cnt[r], bv[u][r]);
+            }
+        } else {
 #pragma unroll
-                    for (int e = 0; e < W; ++e) bv[u][r][e] = T(0);
+            for (int u = 0; u < C::U; ++u) {
+                const int j = j0 + u;
+                const int cj = __shfl_sync(FULL, col[j / G], j % G, G);
+                av[u] = __shfl_sync(FULL, val[j / G], j % G, G);
+                const int64_t roff = (int64_t)cj * ldb;
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    if (j < cnt) {
+                        gather_b<T, W>(lv.base[r] + roff, lv.cnt[r], bv[u][r]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < W; ++e) bv[u][r][e] = T(0);
+                    }
                 }
             }
         }
@@ -196,6 +237,7 @@ __device__ __forceinline__ void process_rows(const SpmmParams<T>& p, const int* 
     const int goff = MEDIUM ? gi * C::CH : 0;
     const int nvec = (pw + W - 1) / W;
     const T* Bp = p.B + c0col;
+    const int ldb = (int)p.ldb;                            // <= INT_MAX (host check)
 
     for (int sub = 0; sub < count; sub += 32) {
         const int nrows = min(32, count - sub);
@@ -206,6 +248,7 @@ __device__ __forceinline__ void process_rows(const SpmmParams<T>& p, const int* 
             my_len = p.row_ptr[my_row + 1] - my_e0;
         }
         for (int vbase = 0; vbase < nvec; vbase += C::SLOTS) {
+            const LaneVecs<T, W, R> lv = lane_vecs<T, W, G, R>(Bp, vbase, pw);
             int t = MEDIUM ? 0 : gi;
             int row = __shfl_sync(FULL, my_row, t & 31);
             int e0 = __shfl_sync(FULL, my_e0, t & 31);
@@ -242,9 +285,17 @@ __device__ __forceinline__ void process_rows(const SpmmParams<T>& p, const int* 
 
                 // consume the current step
                 const int cnt = active ? min(C::CH, len - s - goff) : 0;
-                const int cmax = MEDIUM ? min(C::CH, len - s)
-                                        : (int)__reduce_max_sync(FULL, (unsigned)max(cnt, 0));
-                consume_step<T, W, G, R, true>(acc, colc, valc, cnt, cmax, Bp, p.ldb, vbase, pw);
+                int cmax, cmin;
+                if constexpr (MEDIUM) {                    // groups staggered by CH entries
+                    cmax = min(C::CH, len - s);
+                    cmin = max(0, min(C::CH, len - s - (C::RPW - 1) * C::CH));
+                } else if constexpr (G == 32) {            // one group: cnt is warp-uniform
+                    cmax = cmin = max(cnt, 0);
+                } else {
+                    cmax = (int)__reduce_max_sync(FULL, (unsigned)max(cnt, 0));
+                    cmin = (int)__reduce_min_sync(FULL, (unsigned)max(cnt, 0));
+                }
+                consume_step<T, W, G, R, true>(acc, colc, valc, cnt, cmax, cmin, ldb, lv);
 
                 if (s + ESTEP >= len) {                     // row finished (uniform if MEDIUM)
                     if (MEDIUM) combine_groups<T, W, G, R>(acc);
@@ -360,6 +411,8 @@ __device__ __forceinline__ void accumulate_range(T (&acc)[R][W], const SpmmParam
     constexpr int ESTEP = C::RPW * C::CH;
     const int gi = (threadIdx.x & 31) / G;
     const int goff = gi * C::CH;
+    const int ldb = (int)p.ldb;                            // <= INT_MAX (host check)
+    const LaneVecs<T, W, R> lv = lane_vecs<T, W, G, R>(Bp, vbase, pw);
     int colc[Q];
     T valc[Q];
     load_entries<T, G, Q>(colc, valc, p.col_idx, p.values, a + goff, b, pol_s);
@@ -369,7 +422,8 @@ __device__ __forceinline__ void accumulate_range(T (&acc)[R][W], const SpmmParam
         load_entries<T, G, Q>(coln, valn, p.col_idx, p.values, s + ESTEP + goff, b, pol_s);
         const int cnt = min(C::CH, b - s - goff);
         const int cmax = min(C::CH, b - s);
-        consume_step<T, W, G, R>(acc, colc, valc, cnt, cmax, Bp, p.ldb, vbase, pw);
+        const int cmin = max(0, min(C::CH, b - s - (C::RPW - 1) * C::CH));
+        consume_step<T, W, G, R>(acc, colc, valc, cnt, cmax, cmin, ldb, lv);
 #pragma unroll
         for (int q = 0; q < Q; ++q) {
             colc[q] = coln[q];

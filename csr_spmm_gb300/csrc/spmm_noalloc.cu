@@ -110,6 +110,7 @@ extern "C" spmm_status_t spmm_csr_f32_noalloc(float alpha, const int32_t* row_pt
         return SPMM_ERR_INVALID_ARGUMENT;
     if (ldb < std::max<int64_t>(1, n) || ldc < std::max<int64_t>(1, n))
         return SPMM_ERR_DIMENSION_MISMATCH;
+    if (ldb > (int64_t)INT_MAX) return SPMM_ERR_INVALID_ARGUMENT;   // 32-bit gather offsets
     if (m > NOALLOC_MAX_ROWS || n > NOALLOC_MAX_COLS) return SPMM_ERR_TOO_LARGE;
     if (m == 0 || n == 0) return SPMM_OK;
     if (!C) return SPMM_ERR_NULL_POINTER;

@@ -89,8 +89,9 @@ spmm_status_t spmm_reserve(spmm_handle_t h, int64_t m, int64_t n, int elem_size)
  *   row_ptr [m+1], col_idx [nnz], values [nnz]   CSR of A (m x k)
  *   B  [k rows, stride ldb]   dense, row-major, only columns 0..n-1 are read
  *   C  [m rows, stride ldc]   dense, row-major, columns 0..n-1 are written
- * Requires m, k, n >= 0, m < 2^31 - 1, k <= 2^31 - 1, ldb >= max(1, n),
- * ldc >= max(1, n); the current device must be the handle's device.
+ * Requires m, k, n >= 0, m < 2^31 - 1, k <= 2^31 - 1, max(1, n) <= ldb <=
+ * 2^31 - 1 (SPMM_ERR_INVALID_ARGUMENT above), ldc >= max(1, n); the current
+ * device must be the handle's device.
  * Pointers may be NULL only where the conventions above say the array is not
  * read (A and B when alpha == 0 or k == 0; everything when m == 0 or n == 0).
  * The library cannot see nnz, so col_idx and values must be valid addresses

@@ -291,6 +291,8 @@ def test_error_paths(handle):
         cs.SPMM_ERR_DIMENSION_MISMATCH                                  # ldc < n
     assert f(1.0, *P, -1, 10, B.data_ptr(), 8, 8, 0.0, C.data_ptr(), 8, 0) == \
         cs.SPMM_ERR_INVALID_ARGUMENT
+    assert f(1.0, *P, 10, 10, B.data_ptr(), 2**31, 8, 0.0, C.data_ptr(), 8, 0) == \
+        cs.SPMM_ERR_INVALID_ARGUMENT                                    # ldb > INT32_MAX
     assert f(1.0, *P, 10, 10, B.data_ptr(), 8, 8, 0.0, 0, 8, 0) == cs.SPMM_ERR_NULL_POINTER
     assert f(1.0, 0, ci.data_ptr(), v.data_ptr(), 10, 10, B.data_ptr(), 8, 8, 0.0,
              C.data_ptr(), 8, 0) == cs.SPMM_ERR_NULL_POINTER

@@ -169,6 +169,7 @@ Plan make_plan_es(const spmm_handle_s* h, int64_t k, int64_t n, int es, bool vec
     const int batch_bytes = es == 8 ? SPMM_BATCH_BYTES_F64 : SPMM_BATCH_BYTES;
     const int U = std::min(SPMM_BATCH_MAX, std::max(1, batch_bytes / bytes_per_entry));
     const int CH = std::max(P.geo.G, U);
+    P.geo.whole = (n % W) == 0;
     P.long_min = LONG_MIN_ROW;
     P.short_max = (P.geo.G == 32) ? P.long_min - 1 : std::min(P.long_min - 1, 2 * CH);
     return P;

@@ -68,6 +68,9 @@ constexpr int ROWS_THREADS = 256;
 #ifndef SPMM_BATCH_BYTES_F64
 #define SPMM_BATCH_BYTES_F64 16
 #endif
+#ifndef SPMM_LONG_BATCH_BYTES
+#define SPMM_LONG_BATCH_BYTES 64
+#endif
 #ifndef SPMM_LONG_MIN_BLOCKS
 #define SPMM_LONG_MIN_BLOCKS 4
 #endif
@@ -127,6 +130,7 @@ struct Geometry {
     int W;        // elements per vector access (1, 2, 4 or 8)
     int G;        // lanes per row group (power of two <= 32)
     int R;        // vector slots per lane per column pass (1..4)
+    bool whole;   // n % W == 0: no lane holds a partial vector
 };
 
 // An L2 access-policy window for one launch: accesses to [base, base + bytes)

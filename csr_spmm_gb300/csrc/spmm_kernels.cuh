@@ -42,8 +42,9 @@ struct Cfg {
     static constexpr int SLOTS = G * R;                       // vectors per column pass
     static constexpr int BYTES_PER_ENTRY = R * W * (int)sizeof(T);
     static constexpr int BATCH_BYTES = sizeof(T) == 8 ? SPMM_BATCH_BYTES_F64
-                                       : (ROWS && narrow_f32<T, W, G>()) ? SPMM_BATCH_BYTES_NARROW
-                                                               : SPMM_BATCH_BYTES;
+                                       : !ROWS                   ? SPMM_LONG_BATCH_BYTES
+                                       : narrow_f32<T, W, G>()   ? SPMM_BATCH_BYTES_NARROW
+                                                                 : SPMM_BATCH_BYTES;
     static constexpr int U0 = BATCH_BYTES / BYTES_PER_ENTRY;        // B bytes in flight/lane
     static constexpr int U = U0 < 1 ? 1 : (U0 > SPMM_BATCH_MAX ? SPMM_BATCH_MAX : U0);
     static constexpr int CH = G > U ? G : U;                  // entries per group per step
@@ -107,9 +108,11 @@ __device__ __forceinline__ LaneVecs<T, W, R> lane_vecs(const T* __restrict__ Bp,
     return lv;
 }
 
-template <typename T, int W>
+// WHOLE: every lane vector of the geometry is whole (n a multiple of W), so
+// the partial-vector path is compiled out.
+template <typename T, int W, bool WHOLE>
 __device__ __forceinline__ void gather_b(const T* p, int cnt, T (&v)[W]) {
-    if (W == 1 || cnt == W) BLoad<T, W>::run(p, v);
+    if (WHOLE || W == 1 || cnt == W) BLoad<T, W>::run(p, v);
     else load_b_partial<T, W>(p, cnt, v);
 }
 
@@ -117,7 +120,7 @@ __device__ __forceinline__ void gather_b(const T* p, int cnt, T (&v)[W]) {
 // in batches of U.  cmax / cmin are warp-uniform bounds on every group's cnt:
 // batches below cmin are whole for every group and gather without checks.
 // Entries past a row's end were loaded with value 0 (load_entries).
-template <typename T, int W, int G, int R, bool ROWS = false>
+template <typename T, int W, int G, int R, bool ROWS = false, bool WHOLE = false>
 __device__ __forceinline__ void consume_step(T (&acc)[R][W],
                                              const int (&col)[Cfg<T, W, G, R, ROWS>::Q],
                                              const T (&val)[Cfg<T, W, G, R, ROWS>::Q], int cnt,
@@ -137,7 +140,8 @@ __device__ __forceinline__ void consume_step(T (&acc)[R][W],
                 av[u] = __shfl_sync(FULL, val[j / G], j % G, G);
                 const int64_t roff = (int64_t)cj * ldb;
 #pragma unroll
-                for (int r = 0; r < R; ++r) gather_b<T, W>(lv.base[r] + roff, lv.cnt[r], bv[u][r]);
+                for (int r = 0; r < R; ++r)
+                    gather_b<T, W, WHOLE>(lv.base[r] + roff, lv.cnt[r], bv[u][r]);
             }
         } else {
 #pragma unroll
@@ -149,7 +153,7 @@ __device__ __forceinline__ void consume_step(T (&acc)[R][W],
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     if (j < cnt) {
-                        gather_b<T, W>(lv.base[r] + roff, lv.cnt[r], bv[u][r]);
+                        gather_b<T, W, WHOLE>(lv.base[r] + roff, lv.cnt[r], bv[u][r]);
                     } else {
 #pragma unroll
                         for (int e = 0; e < W; ++e) bv[u][r][e] = T(0);
@@ -224,7 +228,7 @@ __device__ __forceinline__ void write_row_c0(T* __restrict__ Crow, const T (&acc
 //     group gi takes entries [s + gi*CH, s + gi*CH + CH) of each warp step of
 //     RPW*CH entries, and the groups are combined at the end of the row.
 // ---------------------------------------------------------------------------
-template <typename T, int W, int G, int R, bool MEDIUM, bool READ_C>
+template <typename T, int W, int G, int R, bool MEDIUM, bool READ_C, bool WHOLE>
 __device__ __forceinline__ void process_rows(const SpmmParams<T>& p, const int* __restrict__ list,
                                              int first, int count, int stride, int c0col, int pw,
                                              uint64_t pol_s) {
@@ -295,7 +299,7 @@ __device__ __forceinline__ void process_rows(const SpmmParams<T>& p, const int* 
                     cmax = (int)__reduce_max_sync(FULL, (unsigned)max(cnt, 0));
                     cmin = (int)__reduce_min_sync(FULL, (unsigned)max(cnt, 0));
                 }
-                consume_step<T, W, G, R, true>(acc, colc, valc, cnt, cmax, cmin, ldb, lv);
+                consume_step<T, W, G, R, true, WHOLE>(acc, colc, valc, cnt, cmax, cmin, ldb, lv);
 
                 if (s + ESTEP >= len) {                     // row finished (uniform if MEDIUM)
                     if (MEDIUM) combine_groups<T, W, G, R>(acc);
@@ -354,7 +358,8 @@ struct RowsOccupancy {
 };
 
 // READ_C: beta != 0 (C is read, and prefetched at each row start).
-template <typename T, int W, int G, int R, bool READ_C>
+// WHOLE: n is a multiple of W (no partial vectors; see gather_b).
+template <typename T, int W, int G, int R, bool READ_C, bool WHOLE>
 __global__ void __launch_bounds__(ROWS_THREADS, RowsOccupancy<T, W, G>::MIN_BLOCKS)
 rows_kernel(SpmmParams<T> p) {
     wait_for_predecessor();
@@ -389,11 +394,11 @@ rows_kernel(SpmmParams<T> p) {
         const int c0 = panel * p.panel_cols;
         const int pw = min(p.panel_cols, p.n - c0);
         if (s_count > 0)
-            process_rows<T, W, G, R, false, READ_C>(p, p.rowlist, s_first, s_count, s_stride, c0,
-                                                    pw, pol_s);
+            process_rows<T, W, G, R, false, READ_C, WHOLE>(p, p.rowlist, s_first, s_count,
+                                                           s_stride, c0, pw, pol_s);
         if (m1 > m0)
-            process_rows<T, W, G, R, true, READ_C>(p, p.rowlist + n_short, m0, m1 - m0, 1, c0, pw,
-                                                   pol_s);
+            process_rows<T, W, G, R, true, READ_C, WHOLE>(p, p.rowlist + n_short, m0, m1 - m0,
+                                                          1, c0, pw, pol_s);
     }
 }
 

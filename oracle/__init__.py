@@ -1,4 +1,5 @@
-"""CPU oracle for CSR SpMM (C = alpha * A * B + beta * C0), fp64 accumulation.
+"""CPU oracle for CSR SpMM (C = alpha * A * B + beta * C0) and the squared
+chain (C = alpha * A (A B) + beta * C0), fp64 accumulation.
 
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU
 baseline leg of ``bench.py`` use it; the product path never does.  The
@@ -43,6 +44,9 @@ def load_library(path: str):
     lib.oracle_spmm.restype = ctypes.c_int
     lib.oracle_spmm.argtypes = [ctypes.c_int, i64, i64, i64, ctypes.c_double, p, p, p, p,
                                 i64, ctypes.c_double, p, i64, p, i64, p, p, i64]
+    lib.oracle_spmm_squared.restype = ctypes.c_int
+    lib.oracle_spmm_squared.argtypes = [ctypes.c_int, i64, i64, ctypes.c_double, p, p, p, p, i64,
+                                        ctypes.c_double, p, i64, p, i64, p, p, i64]
     lib.oracle_csr_check.restype = ctypes.c_int
     lib.oracle_csr_check.argtypes = [i64, i64, i64, p, p]
     return lib
@@ -98,6 +102,36 @@ def spmm(m: int, k: int, n: int, alpha: float, row_ptr, col_idx, values, B, ldb:
                          _ptr(rsel), nrows, _ptr(out), _ptr(bound), n)
     if rc != OK:
         raise ValueError(f"oracle_spmm rejected its inputs (status {rc})")
+    return out, bound
+
+
+def spmm_squared(m: int, n: int, alpha: float, row_ptr, col_idx, values, B, ldb: int,
+                 beta: float, C0=None, ldc: int = 0, rows: Optional[np.ndarray] = None,
+                 _lib=None):
+    """Evaluate alpha * A (A B) + beta * C0 in fp64 for a square m x m CSR A.
+
+    Same conventions and return value as :func:`spmm`; the bound is
+    |alpha| |A| |A| |B| + |beta| |C0|.  The intermediate A B stays in fp64.
+    """
+    values = np.ascontiguousarray(values)
+    dt = values.dtype
+    if dt not in (np.float32, np.float64):
+        raise TypeError("values must be float32 or float64")
+    B = np.ascontiguousarray(B, dtype=dt)
+    C0 = None if C0 is None else np.ascontiguousarray(C0, dtype=dt)
+    # A may be absent when alpha == 0 (it is not read then)
+    row_ptr = None if row_ptr is None else np.ascontiguousarray(row_ptr, dtype=np.int32)
+    col_idx = None if col_idx is None else np.ascontiguousarray(col_idx, dtype=np.int32)
+    rsel = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    nrows = m if rsel is None else int(rsel.size)
+    out = np.zeros((nrows, n), dtype=np.float64)
+    bound = np.zeros((nrows, n), dtype=np.float64)
+    lib = _load() if _lib is None else _lib
+    rc = lib.oracle_spmm_squared(dt.itemsize, m, n, float(alpha), _ptr(row_ptr), _ptr(col_idx),
+                                 _ptr(values), _ptr(B), ldb, float(beta), _ptr(C0), ldc,
+                                 _ptr(rsel), nrows, _ptr(out), _ptr(bound), n)
+    if rc != OK:
+        raise ValueError(f"oracle_spmm_squared rejected its inputs (status {rc})")
     return out, bound
 
 

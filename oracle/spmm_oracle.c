@@ -140,3 +140,110 @@ int oracle_spmm(int esize, int64_t m, int64_t k, int64_t n, double alpha,
     free(absacc);
     return ORACLE_OK;
 }
+
+/*
+ * The squared chain, for a square m x m CSR matrix A (the SEACells kernel
+ * matrix K of the bixverse page, whose Frank-Wolfe kernels consume
+ * K^2 B, the output of `k_squared_matmul`, module doc):
+ *
+ *   out[r * ldo + c] = alpha * (A (A B))[i, c] + beta * C0[i * ldc + c],
+ *   i = rows[r] (all rows in order when rows is NULL), c < n.
+ *
+ * Plain definition, written out: for each entry (i, j) of row i, row j of the
+ * intermediate T = A B is formed in binary64 from row j's entries (T is never
+ * rounded to the input precision), and the output row accumulates
+ * a_ij * T[j, c] in CSR order.  alpha == 0: A and B are not read; beta == 0:
+ * C0 is not read (as for the single product).
+ *
+ * bound = |alpha| * sum_j |a_ij| * sum_l |a_jl| * |B[l, c]| + |beta| * |C0|,
+ * the same scale as the single product, with |A| |A| |B| in place of |A| |B|.
+ */
+int oracle_spmm_squared(int esize, int64_t m, int64_t n, double alpha,
+                        const int32_t *row_ptr, const int32_t *col_idx, const void *values,
+                        const void *B, int64_t ldb, double beta, const void *C0, int64_t ldc,
+                        const int64_t *rows, int64_t nrows, double *out, double *bound,
+                        int64_t ldo)
+{
+    if ((esize != 4 && esize != 8) || m < 0 || n < 0 || ldo < n) return ORACLE_BAD_ARGS;
+    if (!rows) nrows = m;
+    if (nrows <= 0 || n == 0) return ORACLE_OK;
+    if (beta != 0.0 && (!C0 || ldc < n)) return ORACLE_BAD_ARGS;
+    if (alpha != 0.0) {
+        if (!row_ptr || ldb < n) return ORACLE_BAD_ARGS;
+        if (oracle_csr_check(m, m, (int64_t)row_ptr[m], row_ptr, col_idx) != ORACLE_OK)
+            return ORACLE_BAD_CSR;
+    }
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t i = rows ? rows[r] : r;
+        if (i < 0 || i >= m) return ORACLE_BAD_ARGS;
+    }
+
+    double *acc = (double *)malloc(sizeof(double) * (size_t)n);
+    double *absacc = (double *)malloc(sizeof(double) * (size_t)n);
+    double *t = (double *)malloc(sizeof(double) * (size_t)n);      /* row j of A B */
+    double *abst = (double *)malloc(sizeof(double) * (size_t)n);   /* row j of |A| |B| */
+    if (!acc || !absacc || !t || !abst) {
+        free(acc);
+        free(absacc);
+        free(t);
+        free(abst);
+        return ORACLE_NO_MEMORY;
+    }
+
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t i = rows ? rows[r] : r;
+        double *o = out + r * ldo;
+        double *bd = bound ? bound + r * ldo : NULL;
+
+        if (alpha == 0.0) {                      /* A and B not referenced */
+            for (int64_t c = 0; c < n; ++c) {
+                double c0 = (beta == 0.0) ? 0.0 : load(C0, i * ldc + c, esize);
+                o[c] = (beta == 0.0) ? 0.0 : beta * c0;
+                if (bd) bd[c] = fabs(beta) * fabs(c0);
+            }
+            continue;
+        }
+
+        for (int64_t c = 0; c < n; ++c) {
+            acc[c] = 0.0;
+            absacc[c] = 0.0;
+        }
+        for (int64_t p = row_ptr[i]; p < (int64_t)row_ptr[i + 1]; ++p) {
+            int64_t j = col_idx[p];
+            double a = load(values, p, esize);
+            for (int64_t c = 0; c < n; ++c) {
+                t[c] = 0.0;
+                abst[c] = 0.0;
+            }
+            for (int64_t q = row_ptr[j]; q < (int64_t)row_ptr[j + 1]; ++q) {
+                int64_t l = col_idx[q];
+                double aj = load(values, q, esize);
+                for (int64_t c = 0; c < n; ++c) {
+                    double b = load(B, l * ldb + c, esize);
+                    t[c] += aj * b;
+                    abst[c] += fabs(aj) * fabs(b);
+                }
+            }
+            for (int64_t c = 0; c < n; ++c) {
+                acc[c] += a * t[c];
+                absacc[c] += fabs(a) * abst[c];
+            }
+        }
+        for (int64_t c = 0; c < n; ++c) {
+            double v = alpha * acc[c];
+            double e = fabs(alpha) * absacc[c];
+            if (beta != 0.0) {                   /* C0 read only when beta != 0 */
+                double c0 = load(C0, i * ldc + c, esize);
+                v += beta * c0;
+                e += fabs(beta) * fabs(c0);
+            }
+            o[c] = v;
+            if (bd) bd[c] = e;
+        }
+    }
+    free(acc);
+    free(absacc);
+    free(t);
+    free(abst);
+    return ORACLE_OK;
+}

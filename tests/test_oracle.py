@@ -286,9 +286,11 @@ def test_planted_mistakes_are_caught(name, tmp_path):
         pytest.skip("gcc not available")
     src = open(os.path.join(os.path.dirname(oracle.__file__), "spmm_oracle.c")).read()
     old, new = MUTANTS[name]
-    assert src.count(old) == 1, f"mutation anchor for {name} not unique"
+    # the anchor's first occurrence lies in oracle_spmm (the squared chain,
+    # further down the file, has its own mutants in test_oracle_squared.py)
+    assert src.count(old) >= 1 and src.index(old) < src.index("int oracle_spmm_squared("), name
     mutated = tmp_path / "mut.c"
-    mutated.write_text(src.replace(old, new))
+    mutated.write_text(src.replace(old, new, 1))
     so = tmp_path / "libmut.so"
     subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-o",
                     str(so), str(mutated), "-lm"], check=True)

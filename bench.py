@@ -154,34 +154,69 @@ def rows_kernel_bytes(p, prof):
     return 4 * (rows + 1) + (4 + es) * entries + share * es * p.k * p.n + c_bytes
 
 
+def is_chain(p):
+    """The squared chain C = alpha * A (A B) + beta * C (workloads marked so)."""
+    return p.meta.get("chain") == "squared"
+
+
+def problem_flops(p):
+    """2 nnz n per product; the chain is two products."""
+    return p.flops() * (2 if is_chain(p) else 1)
+
+
+def problem_bytes(p):
+    """Algorithmic bytes: CSR arrays + B once + C read (beta != 0) + C write per
+    product.  For the chain: A twice, B once, the m x n intermediate written
+    by the first product and read once by the second, then C."""
+    if not is_chain(p):
+        return p.algorithmic_bytes()
+    es = p.values.dtype.itemsize
+    csr = 4 * (p.m + 1) + (4 + es) * p.nnz
+    mn = es * p.m * p.n
+    return 2 * csr + mn + 2 * mn + mn * (2 if p.beta != 0.0 else 1)
+
+
+def oracle_rows(p, rows):
+    """The oracle on rows of the workload (all rows if None); returns its flops."""
+    import numpy as np
+
+    import oracle
+    lens = np.diff(p.row_ptr).astype(np.int64)
+    sel = np.arange(p.m) if rows is None else rows
+    if is_chain(p):
+        oracle.spmm_squared(p.m, p.n, p.alpha, p.row_ptr, p.col_idx, p.values, p.B, p.ldb,
+                            p.beta, p.C0, p.ldc, rows)
+        # the sample's share (by entries) of the chain's 2 x 2 nnz n; the
+        # oracle forms every row of A B a sampled row needs, so it does more
+        # arithmetic than that, and its rate in the metric's unit is lower
+        return int(round(problem_flops(p) * int(lens[sel].sum()) / max(1, p.nnz)))
+    oracle.spmm_problem(p, rows)
+    return 2 * p.n * int(lens[sel].sum())
+
+
 def oracle_baseline(p, target_s=10.0, max_passes=5):
     """Time the CPU oracle (as it stands, single-threaded) on the full workload,
     repeating whole passes until ~target_s of work or max_passes; for workloads
     whose single pass would exceed the budget, a strided row sample instead."""
     import numpy as np
-
-    import oracle
     t0 = time.perf_counter()
     probe = np.arange(0, p.m, max(1, p.m // 2000), dtype=np.int64)
-    oracle.spmm_problem(p, probe)
+    f_probe = oracle_rows(p, probe)
     t_probe = time.perf_counter() - t0
-    nnz_probe = int(np.diff(p.row_ptr)[probe].sum()) + len(probe)
-    est_full = t_probe * (p.nnz + p.m) / max(1, nnz_probe)
+    est_full = t_probe * problem_flops(p) / max(1, f_probe)
     if est_full <= target_s:
         rows, desc = None, "all rows"
-        flops_pass = p.flops()
     else:
         stride = int(np.ceil(est_full / target_s))
         rows = np.arange(0, p.m, stride, dtype=np.int64)
         desc = f"every {stride}th row ({len(rows)} rows)"
-        flops_pass = 2 * int(np.diff(p.row_ptr)[rows].sum()) * p.n
-    passes, elapsed = 0, 0.0
+    passes, elapsed, flops = 0, 0.0, 0
     while passes < max_passes and (passes == 0 or elapsed < target_s):
         t0 = time.perf_counter()
-        oracle.spmm_problem(p, rows)
+        flops += oracle_rows(p, rows)
         elapsed += time.perf_counter() - t0
         passes += 1
-    gflops = flops_pass * passes / elapsed / 1e9
+    gflops = flops / elapsed / 1e9
     return {"value": round(gflops, 4), "unit": "GFLOP/s", "cores": 1, "kind": "oracle",
             "sample": f"{p.name}: {desc} x {passes} pass(es), {elapsed:.1f} s, fp64 accumulation"}
 
@@ -196,25 +231,23 @@ def run_reference(args):
 
     import oracle
     oracle.build()
-    lens = np.diff(p.row_ptr)
     # each step: a bounded strided row sample of the workload (~0.5 s of oracle work)
     probe = np.arange(0, p.m, max(1, p.m // 1000), dtype=np.int64)
     t0 = time.perf_counter()
-    oracle.spmm_problem(p, probe)
+    f_probe = oracle_rows(p, probe)
     t_probe = time.perf_counter() - t0
-    est_full = t_probe * (p.nnz + p.m) / max(1, int(lens[probe].sum()) + len(probe))
+    est_full = t_probe * problem_flops(p) / max(1, f_probe)
     stride = max(1, int(np.ceil(est_full / 0.5)))
     rows = np.arange(0, p.m, stride, dtype=np.int64)
-    flops = 2 * int(lens[rows].sum()) * p.n
     for _ in range(args.warmup):
-        oracle.spmm_problem(p, rows)
-    times = []
+        oracle_rows(p, rows)
+    times, flops = [], 0
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle.spmm_problem(p, rows)
+        flops += oracle_rows(p, rows)
         times.append(time.perf_counter() - t0)
     total = sum(times)
-    value = flops * args.steps / total / 1e9
+    value = flops / total / 1e9
     sample = f"{p.name}: every {stride}th row ({len(rows)} rows) per step, fp64 accumulation"
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GFLOP/s",
@@ -267,13 +300,22 @@ def run_ours(args):
     h = cs.Handle(local)
     h.reserve(p.m, p.n, p.values.dtype.itemsize)
     cs.spmm_set_profiling(h.ptr, True)
-    fn = cs.spmm_csr_f32 if p.values.dtype == np.float32 else cs.spmm_csr_f64
+    chain = is_chain(p)
+    f32 = p.values.dtype == np.float32
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
+    if chain:
+        fn = cs.spmm_csr_squared_f32 if f32 else cs.spmm_csr_squared_f64
 
-    def call(Cbuf):
-        fn(h.ptr, p.alpha, rp.data_ptr(), ci.data_ptr(), va.data_ptr(), p.m, p.k, B.data_ptr(),
-           p.ldb, p.n, p.beta, Cbuf.data_ptr(), p.ldc, sptr)
+        def call(Cbuf):
+            fn(h.ptr, p.alpha, rp.data_ptr(), ci.data_ptr(), va.data_ptr(), p.m, B.data_ptr(),
+               p.ldb, p.n, p.beta, Cbuf.data_ptr(), p.ldc, sptr)
+    else:
+        fn = cs.spmm_csr_f32 if f32 else cs.spmm_csr_f64
+
+        def call(Cbuf):
+            fn(h.ptr, p.alpha, rp.data_ptr(), ci.data_ptr(), va.data_ptr(), p.m, p.k,
+               B.data_ptr(), p.ldb, p.n, p.beta, Cbuf.data_ptr(), p.ldc, sptr)
 
     for _ in range(max(3, args.warmup)):
         if C0 is not None:
@@ -327,13 +369,19 @@ def run_ours(args):
         tt = torch.tensor([total_ms], device=dev, dtype=torch.float64)
         pg.all_reduce(tt, op=pg.ReduceOp.MAX)
         total_ms = float(tt.item())
-    flops = p.flops()
+    flops = problem_flops(p)
     value = flops * args.steps * world / (total_ms / 1e3) / 1e9
 
     # ---- roofline of the dominant kernel (short/medium rows) ----
     peak, peak_kind = measured_hbm_peak()
     rows_ms = statistics.mean(pr["rows_ms"] for pr in profs)
     kbytes = rows_kernel_bytes(p, profs[-1])
+    if chain:
+        # a profiled chain reports its two products as rows_ms and long_ms
+        # (each a rows launch plus the long-row launch); their bytes are the
+        # chain's algorithmic bytes
+        rows_ms += statistics.mean(pr["long_ms"] for pr in profs)
+        kbytes = problem_bytes(p)
     achieved = kbytes / (rows_ms / 1e3) / 1e9
     traffic = recorded_traffic(p.name)
     launches = int(sum(pr["launches"] for pr in profs))
@@ -389,7 +437,7 @@ def run_ours(args):
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cpu = oracle_baseline(p)
-    alg = p.algorithmic_bytes()
+    alg = problem_bytes(p)
     mean_ms = total_ms / args.steps
     dtype = {"float32": "f32", "float64": "f64"}[str(p.values.dtype)]
     line = {
@@ -399,6 +447,7 @@ def run_ours(args):
         "data": "synthetic",
         "config": {"workload": p.name, "m": p.m, "k": p.k, "n": p.n, "nnz": p.nnz,
                    "alpha": p.alpha, "beta": p.beta, "algorithmic_bytes": alg,
+                   "operation": "C = alpha*A(AB) + beta*C" if chain else "C = alpha*AB + beta*C",
                    "l2_flush": "2x L2 buffer written before every timed step",
                    "parallelism": f"replicas x{world}",
                    "hbm_gbs_whole_call": round(alg / (mean_ms / 1e3) / 1e9, 1),
@@ -409,7 +458,9 @@ def run_ours(args):
                                                        "rows_long", "long_nnz")},
                    "stage_ms": {k: round(statistics.mean(pr[k] for pr in profs), 5)
                                 for k in ("prepass_ms", "rows_ms", "long_ms", "fixup_ms")}},
-        "roofline": {"bound": "hbm", "kernel": "rows_kernel", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm",
+                     "kernel": "rows_kernel (both products)" if chain else "rows_kernel",
+                     "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": int(kbytes)},

@@ -19,12 +19,14 @@ from ._lib import (EXPORTED, SPMM_ERR_ALLOC, SPMM_ERR_CUDA, SPMM_ERR_DIMENSION_M
                    spmm_csr_check, spmm_csr_f32, spmm_csr_f32_noalloc, spmm_csr_f64,
                    spmm_destroy, spmm_get_profile, spmm_plan_create, spmm_plan_csr_f32,
                    spmm_plan_csr_f64, spmm_plan_destroy, spmm_set_l2_persistence,
+                   spmm_csr_squared_f32, spmm_csr_squared_f64,
                    spmm_reserve, spmm_set_profiling, status_string)
 
 __all__ = ["Handle", "spmm", "csr_check", "SpmmError", "library", "spmm_create", "spmm_destroy",
            "spmm_reserve", "spmm_csr_f32", "spmm_csr_f64", "spmm_csr_check", "status_string",
            "spmm_set_profiling", "spmm_get_profile", "spmm_csr_f32_noalloc", "spmm_plan_create",
            "spmm_plan_destroy", "spmm_set_l2_persistence", "spmm_plan_csr_f32",
+           "spmm_csr_squared_f32", "spmm_csr_squared_f64", "spmm_squared",
            "spmm_plan_csr_f64", "Plan", "EXPORTED"]
 
 
@@ -89,6 +91,37 @@ def spmm(handle: Handle, alpha: float, row_ptr, col_idx, values, k: int, B, beta
         spmm_csr_f32(*args)
     elif values.dtype == torch.float64:
         spmm_csr_f64(*args)
+    else:
+        raise TypeError("values must be float32 or float64")
+
+
+def spmm_squared(handle: Handle, alpha: float, row_ptr, col_idx, values, B, beta: float, C,
+                 stream=None) -> None:
+    """C <- alpha * A (A B) + beta * C for a square CSR A (the K^2 B chain).
+
+    ``B`` and ``C`` are [m, n] CUDA tensors with unit column stride.
+    Enqueued on ``stream`` (default: torch's current stream).
+    """
+    import torch
+    m = int(row_ptr.numel()) - 1
+    n = int(C.shape[1])
+    if C.dim() != 2 or B.dim() != 2 or C.stride(1) != 1 or B.stride(1) != 1:
+        raise ValueError("B and C must be 2-D with unit column stride")
+    if tuple(B.shape) != (m, n) or C.shape[0] != m:
+        raise ValueError(f"shape mismatch: A {m}x{m}, B {tuple(B.shape)}, C {tuple(C.shape)}")
+    if row_ptr.dtype != torch.int32 or col_idx.dtype != torch.int32:
+        raise TypeError("row_ptr and col_idx must be int32")
+    if not (values.dtype == B.dtype == C.dtype):
+        raise TypeError("values, B and C must share one dtype")
+    st = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+    ldb = B.stride(0) if B.shape[0] > 1 else max(1, n)
+    ldc = C.stride(0) if C.shape[0] > 1 else max(1, n)
+    args = (handle.ptr, alpha, _ptr(row_ptr), _ptr(col_idx), _ptr(values), m, _ptr(B), ldb, n,
+            beta, _ptr(C), ldc, st)
+    if values.dtype == torch.float32:
+        spmm_csr_squared_f32(*args)
+    elif values.dtype == torch.float64:
+        spmm_csr_squared_f64(*args)
     else:
         raise TypeError("values must be float32 or float64")
 

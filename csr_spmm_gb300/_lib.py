@@ -27,7 +27,8 @@ SPMM_ERR_TOO_LARGE = 8
 # every symbol include/csr_spmm.h declares
 EXPORTED = ("spmm_create", "spmm_destroy", "spmm_reserve", "spmm_csr_f32", "spmm_csr_f64",
             "spmm_csr_check", "spmm_set_profiling", "spmm_get_profile", "spmm_csr_f32_noalloc",
-            "spmm_set_l2_persistence", "spmm_plan_create", "spmm_plan_destroy", "spmm_plan_csr_f32", "spmm_plan_csr_f64",
+            "spmm_set_l2_persistence", "spmm_csr_squared_f32", "spmm_csr_squared_f64",
+            "spmm_plan_create", "spmm_plan_destroy", "spmm_plan_csr_f32", "spmm_plan_csr_f64",
             "spmm_status_string")
 
 
@@ -89,6 +90,11 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.spmm_csr_f32_noalloc.argtypes = [ctypes.c_float, vp, vp, vp, i64, i64, vp, i64, i64,
                                          ctypes.c_float, vp, i64, vp]
     lib.spmm_csr_f32_noalloc.restype = st
+    for name, real in (("spmm_csr_squared_f32", ctypes.c_float),
+                       ("spmm_csr_squared_f64", ctypes.c_double)):
+        fn = getattr(lib, name)
+        fn.argtypes = [vp, real, vp, vp, vp, i64, vp, i64, i64, real, vp, i64, vp]
+        fn.restype = st
     lib.spmm_set_l2_persistence.argtypes = [vp, i64]
     lib.spmm_set_l2_persistence.restype = st
     lib.spmm_plan_create.argtypes = [vp, ctypes.POINTER(vp), vp, i64, i64, i64, ctypes.c_int, vp]
@@ -210,3 +216,23 @@ def spmm_plan_csr_f64(plan, alpha, row_ptr, col_idx, values, B, ldb, beta, C, ld
 def spmm_set_l2_persistence(handle, nbytes) -> None:
     """Persisting L2 set-aside for B (0: off, < 0: device maximum)."""
     _check(library().spmm_set_l2_persistence(handle, int(nbytes)), "spmm_set_l2_persistence")
+
+
+def spmm_csr_squared_f32(handle, alpha, row_ptr, col_idx, values, m, B, ldb, n, beta, C, ldc,
+                         stream=0, check=True) -> int:
+    """C = alpha * A (A B) + beta * C for a square m x m CSR A (binary32)."""
+    s = library().spmm_csr_squared_f32(handle, float(alpha), row_ptr, col_idx, values, m, B, ldb,
+                                       n, float(beta), C, ldc, stream or None)
+    if check:
+        _check(s, "spmm_csr_squared_f32")
+    return s
+
+
+def spmm_csr_squared_f64(handle, alpha, row_ptr, col_idx, values, m, B, ldb, n, beta, C, ldc,
+                         stream=0, check=True) -> int:
+    """C = alpha * A (A B) + beta * C for a square m x m CSR A (binary64)."""
+    s = library().spmm_csr_squared_f64(handle, float(alpha), row_ptr, col_idx, values, m, B, ldb,
+                                       n, float(beta), C, ldc, stream or None)
+    if check:
+        _check(s, "spmm_csr_squared_f64")
+    return s

@@ -408,6 +408,141 @@ spmm_status_t spmm_plan_impl(spmm_plan_t pl, T alpha, const int32_t* row_ptr,
     return SPMM_OK;
 }
 
+// The squared chain C = alpha * A (A B) + beta * C for a square A: the K^2 B
+// product that the SEACells Frank-Wolfe kernels of the bixverse page consume
+// (module doc: the n x k output of `k_squared_matmul`).  One pre-pass bins
+// the rows for both products.  The intermediate T = A B lives in handle
+// scratch with a 16-byte-aligned leading dimension and is stored with the
+// default L2 policy (not streamed), so that the second product's gathers of
+// T find it in L2 when it fits there.
+template <typename T>
+spmm_status_t spmm_squared_impl(spmm_handle_t h, T alpha, const int32_t* row_ptr,
+                                const int32_t* col_idx, const T* values, int64_t m, const T* B,
+                                int64_t ldb, int64_t n, T beta, T* C, int64_t ldc, void* stream) {
+    if (!h) return SPMM_ERR_INVALID_ARGUMENT;
+    if (m < 0 || n < 0) return SPMM_ERR_INVALID_ARGUMENT;
+    if (m > (int64_t)INT_MAX - BIN_TILE || n > (int64_t)INT_MAX) return SPMM_ERR_INVALID_ARGUMENT;
+    if (ldb < std::max<int64_t>(1, n) || ldc < std::max<int64_t>(1, n))
+        return SPMM_ERR_DIMENSION_MISMATCH;
+    if (ldb > (int64_t)INT_MAX) return SPMM_ERR_INVALID_ARGUMENT;
+    if (m == 0 || n == 0) return SPMM_OK;
+    if (!C) return SPMM_ERR_NULL_POINTER;
+    const bool uses_a = alpha != T(0);
+    if (uses_a && (!row_ptr || !col_idx || !values || !B)) return SPMM_ERR_NULL_POINTER;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device) {
+        cudaGetLastError();
+        return SPMM_ERR_INVALID_ARGUMENT;
+    }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (!uses_a) {
+        if (h->profiling) {
+            h->prof = spmm_profile_t{};
+            h->prof.launches = 1;
+            h->prof_hdr = nullptr;
+            for (int i = 0; i < 5; ++i) mark(h, i, st);
+            h->have_profile = true;
+        }
+        return launch_scale<T>(C, ldc, (int)m, (int)n, beta, h->num_sms * 8, st) == cudaSuccess
+                   ? SPMM_OK : SPMM_ERR_CUDA;
+    }
+
+    constexpr int64_t WV = 16 / (int64_t)sizeof(T);
+    const int64_t ldt = (n + WV - 1) / WV * WV;
+    if (ldt > (int64_t)INT_MAX) return SPMM_ERR_INVALID_ARGUMENT;
+    const int lg = long_grid_of(h);
+    const ScratchLayout L = layout_for(m, n, (int)sizeof(T), lg);
+    const size_t t_off = align_up(L.total, 256);
+    spmm_status_t s = ensure_scratch(h, t_off + (size_t)m * (size_t)ldt * sizeof(T));
+    if (s != SPMM_OK) return s;
+    char* base = static_cast<char*>(h->scratch);
+    T* Tm = reinterpret_cast<T*>(base + t_off);
+
+    BinScratch bs{};
+    bs.hdr = reinterpret_cast<int*>(base + L.hdr);
+    bs.tile_counts = reinterpret_cast<int*>(base + L.tile_counts);
+    bs.tile_offsets = reinterpret_cast<int*>(base + L.tile_offsets);
+    bs.rowlist = reinterpret_cast<int*>(base + L.rowlist);
+    bs.med_pre = reinterpret_cast<int*>(base + L.med_pre);
+    bs.long_pre = reinterpret_cast<int*>(base + L.long_pre);
+    bs.long_cnt = reinterpret_cast<int*>(base + L.long_cnt);
+    bin_geometry(m, &bs.items, &bs.tiles);
+
+    // first product T = A B; the bins it makes serve both products (they are
+    // valid for any geometry)
+    const Plan P1 = make_plan<T>(h, m, n, B, ldb, Tm, ldt);
+    const Plan P2 = make_plan<T>(h, m, n, Tm, ldt, C, ldc);
+    const bool overlap = SPMM_PDL && !h->profiling;
+    mark(h, 0, st);
+    if (launch_binning(row_ptr, (int)m, P1.short_max, P1.long_min, bs, st, overlap) != cudaSuccess)
+        return SPMM_ERR_CUDA;
+    mark(h, 1, st);
+
+    SpmmParams<T> p{};
+    p.row_ptr = row_ptr;
+    p.col_idx = col_idx;
+    p.values = values;
+    p.m = (int)m;
+    p.n = (int)n;
+    p.rowlist = bs.rowlist;
+    p.med_pre = bs.med_pre;
+    p.long_pre = bs.long_pre;
+    p.long_cnt = bs.long_cnt;
+    p.hdr = bs.hdr;
+    p.partials = reinterpret_cast<T*>(base + L.partials);
+    p.long_grid = lg;
+
+    p.B = B;
+    p.ldb = ldb;
+    p.C = Tm;
+    p.ldc = ldt;
+    p.alpha = T(1);
+    p.beta = T(0);
+    p.keep_c = 1;
+    p.panel_cols = P1.panel_cols;
+    p.npanels = P1.npanels;
+    L2Window w1;
+    const L2Window* win1 = b_window(h, B, m, ldb, n, &w1);
+    if (launch_rows<T>(p, P1.geo, rows_grid(h, (int)sizeof(T), P1.geo), st, overlap, win1) !=
+            cudaSuccess ||
+        launch_long<T>(p, P1.geo, st, overlap, win1) != cudaSuccess)
+        return SPMM_ERR_CUDA;
+    mark(h, 2, st);
+
+    // second product C = alpha * A T + beta * C
+    p.B = Tm;
+    p.ldb = ldt;
+    p.C = C;
+    p.ldc = ldc;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.keep_c = 0;
+    p.panel_cols = P2.panel_cols;
+    p.npanels = P2.npanels;
+    L2Window w2;
+    const L2Window* win2 = b_window(h, static_cast<const T*>(Tm), m, ldt, n, &w2);
+    if (launch_rows<T>(p, P2.geo, rows_grid(h, (int)sizeof(T), P2.geo), st, overlap, win2) !=
+            cudaSuccess ||
+        launch_long<T>(p, P2.geo, st, overlap, win2) != cudaSuccess)
+        return SPMM_ERR_CUDA;
+    mark(h, 3, st);
+    mark(h, 4, st);
+    if (h->profiling) {
+        h->prof = spmm_profile_t{};
+        h->prof.launches = (m <= BIN_SINGLE_ROWS ? 1 : 3) + 4;
+        h->prof.panels = P2.npanels;
+        h->prof.panel_cols = P2.panel_cols;
+        h->prof.vec_elems = P2.geo.W;
+        h->prof.group_lanes = P2.geo.G;
+        h->prof.slots = P2.geo.R;
+        h->prof.short_max = P1.short_max;
+        h->prof.long_min = P1.long_min;
+        h->prof_hdr = bs.hdr;
+        h->have_profile = true;
+    }
+    return SPMM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -694,6 +829,22 @@ spmm_status_t spmm_set_l2_persistence(spmm_handle_t h, int64_t bytes) {
     }
     h->persist_bytes = want;
     return SPMM_OK;
+}
+
+spmm_status_t spmm_csr_squared_f32(spmm_handle_t h, float alpha, const int32_t* row_ptr,
+                                   const int32_t* col_idx, const float* values, int64_t m,
+                                   const float* B, int64_t ldb, int64_t n, float beta, float* C,
+                                   int64_t ldc, void* stream) {
+    return spmm_squared_impl<float>(h, alpha, row_ptr, col_idx, values, m, B, ldb, n, beta, C,
+                                    ldc, stream);
+}
+
+spmm_status_t spmm_csr_squared_f64(spmm_handle_t h, double alpha, const int32_t* row_ptr,
+                                   const int32_t* col_idx, const double* values, int64_t m,
+                                   const double* B, int64_t ldb, int64_t n, double beta,
+                                   double* C, int64_t ldc, void* stream) {
+    return spmm_squared_impl<double>(h, alpha, row_ptr, col_idx, values, m, B, ldb, n, beta, C,
+                                     ldc, stream);
 }
 
 const char* spmm_status_string(spmm_status_t s) {

@@ -95,9 +95,17 @@ __device__ __forceinline__ T epi(T alpha, T acc, T beta, T c_old) {
     return alpha * acc + beta * c_old;
 }
 
+// Output store: streaming (.cs) by default; `keep` stores with the default
+// policy instead, for an output that the next product of a chain reads back.
+template <typename V>
+__device__ __forceinline__ void st_out(V* q, V o, bool keep) {
+    if (keep) *q = o;
+    else __stcs(q, o);
+}
+
 template <typename T, int W>
 __device__ __forceinline__ void store_c(T* c, int cnt, const T (&acc)[W], T alpha, T beta,
-                                        bool read_c) {
+                                        bool read_c, bool keep = false) {
     if (cnt == W && (W * sizeof(T)) % 16 == 0) {
         // W * sizeof(T) is 16 or 32 bytes: use 16-byte streaming accesses
         constexpr int PER = 16 / sizeof(T);
@@ -116,7 +124,7 @@ __device__ __forceinline__ void store_c(T* c, int cnt, const T (&acc)[W], T alph
                     o = make_float4(alpha * acc[h], alpha * acc[h + 1], alpha * acc[h + 2],
                                     alpha * acc[h + 3]);
                 }
-                __stcs(q, o);
+                st_out(q, o, keep);
             } else {
                 double2* q = reinterpret_cast<double2*>(c + h);
                 double2 o;
@@ -127,7 +135,7 @@ __device__ __forceinline__ void store_c(T* c, int cnt, const T (&acc)[W], T alph
                 } else {
                     o = make_double2(alpha * acc[h], alpha * acc[h + 1]);
                 }
-                __stcs(q, o);
+                st_out(q, o, keep);
             }
         }
     } else {
@@ -135,7 +143,7 @@ __device__ __forceinline__ void store_c(T* c, int cnt, const T (&acc)[W], T alph
         for (int e = 0; e < W; ++e) {
             if (e < cnt) {
                 T o = read_c ? epi<T>(alpha, acc[e], beta, __ldcs(c + e)) : alpha * acc[e];
-                __stcs(c + e, o);
+                st_out(c + e, o, keep);
             }
         }
     }

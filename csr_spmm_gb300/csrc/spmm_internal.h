@@ -112,6 +112,7 @@ struct SpmmParams {
     int n;               // total columns
     T alpha;
     T beta;
+    int keep_c;          // store C with the default L2 policy (a chain reads it next)
     int panel_cols;      // columns per L2 panel (multiple of the vector width)
     int npanels;
     // bins

@@ -183,12 +183,13 @@ __device__ __forceinline__ void combine_groups(T (&acc)[R][W]) {
 
 template <typename T, int W, int G, int R>
 __device__ __forceinline__ void write_row(T* __restrict__ Crow, const T (&acc)[R][W], int vbase,
-                                          int pw, T alpha, T beta, bool read_c) {
+                                          int pw, T alpha, T beta, bool read_c, bool keep = false) {
     const int g = (threadIdx.x & 31) & (G - 1);
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         const int col = (vbase + g + G * r) * W;
-        if (col < pw) store_c<T, W>(Crow + col, min(W, pw - col), acc[r], alpha, beta, read_c);
+        if (col < pw)
+            store_c<T, W>(Crow + col, min(W, pw - col), acc[r], alpha, beta, read_c, keep);
     }
 }
 
@@ -308,7 +309,8 @@ __device__ __forceinline__ void process_rows(const SpmmParams<T>& p, const int* 
                         if constexpr (READ_C)
                             write_row_c0<T, W, G, R>(Crow, acc, c0, vbase, pw, p.alpha, p.beta);
                         else
-                            write_row<T, W, G, R>(Crow, acc, vbase, pw, p.alpha, p.beta, false);
+                            write_row<T, W, G, R>(Crow, acc, vbase, pw, p.alpha, p.beta, false,
+                                                  p.keep_c);
                     }
                     zero_acc<T, W, R>(acc);
                     if (loads_c && t2 < nrows)
@@ -544,7 +546,7 @@ long_kernel(SpmmParams<T> p) {
                         }
                     if (whole) {
                         write_row<T, W, G, R>(p.C + (int64_t)row * p.ldc + c0, sum, vbase, pw,
-                                              p.alpha, p.beta, read_c);
+                                              p.alpha, p.beta, read_c, p.keep_c);
                     } else {
                         T* dst = p.partials + ((int64_t)blockIdx.x * 2 + slot) * p.n + c0;
 #pragma unroll

@@ -120,6 +120,36 @@ spmm_status_t spmm_csr_check(spmm_handle_t h, const int32_t *row_ptr, const int3
                              int64_t m, int64_t k, int64_t nnz, void *stream,
                              int32_t *host_status);
 
+/* ---- The squared chain ----------------------------------------------------
+ * C = alpha * A (A B) + beta * C for a square m x m CSR matrix A: the K^2 B
+ * product that the SEACells Frank-Wolfe kernels of the bixverse page consume
+ * (seacells_kernels.rs, module doc: the n x k output of `k_squared_matmul`,
+ * with K the cells x cells kernel matrix).  Computed as two products that
+ * share one row-binning pre-pass: T = A B into handle scratch (m x n, leading
+ * dimension n rounded up to 16 bytes, grown with cudaMalloc like the rest of
+ * the scratch), then C = alpha * A T + beta * C.  T is rounded to the element
+ * type, so the result carries the rounding of both products; the parity
+ * tolerance is twice that of one product, against the bound scale
+ * |alpha| |A| |A| |B| + |beta| |C0|.  T is stored with the default L2 policy
+ * (the single product streams C), so that the second product finds it in L2
+ * when it fits.  B and C must not overlap.  Arguments, conventions (alpha ==
+ * 0: C = beta * C and A, B are not read; beta == 0: C is not read; m == 0 or
+ * n == 0: no-op) and errors as for spmm_csr_f32, with k = m.  A profiled call
+ * reports the pre-pass in prepass_ms, the first product in rows_ms and the
+ * second in long_ms.  Asynchronous on `stream`. */
+spmm_status_t spmm_csr_squared_f32(spmm_handle_t h, float alpha,
+                                   const int32_t *row_ptr, const int32_t *col_idx,
+                                   const float *values, int64_t m,
+                                   const float *B, int64_t ldb, int64_t n,
+                                   float beta, float *C, int64_t ldc, void *stream);
+
+/* Same in binary64. */
+spmm_status_t spmm_csr_squared_f64(spmm_handle_t h, double alpha,
+                                   const int32_t *row_ptr, const int32_t *col_idx,
+                                   const double *values, int64_t m,
+                                   const double *B, int64_t ldb, int64_t n,
+                                   double beta, double *C, int64_t ldc, void *stream);
+
 /* Persisting L2 for B.  With `bytes` > 0 (or < 0 for the device maximum,
  * about 81 MiB on GB300) the handle sets the process's
  * persisting-L2 set-aside to that size (cudaLimitPersistingL2CacheSize), and

@@ -328,10 +328,20 @@ def wide_n_integer(seed: int = 4) -> Problem:
                         name="wide_n_integer")
 
 
+def seacells_k2b(seed: int = 1) -> Problem:
+    """The SEACells-shaped product applied twice: C = K (K B) with the kNN
+    kernel matrix K and the column-stochastic B of seacells_knn (the K^2 B
+    operand of the bixverse page's Frank-Wolfe kernels), alpha=1, beta=0."""
+    p = knn_kernel_graph(200_000, 30, 100, 50, seed, name="seacells_k2b")
+    p.meta["chain"] = "squared"
+    return p
+
+
 WORKLOADS = {
     "tiny_uniform": tiny_uniform,
     "seacells_knn": seacells_knn,
     "power_law_1m": power_law_1m,
     "laplacian_707": laplacian_707,
     "wide_n_integer": wide_n_integer,
+    "seacells_k2b": seacells_k2b,
 }

@@ -1,5 +1,6 @@
-"""CPU oracle for CSR SpMM (C = alpha * A * B + beta * C0) and the squared
-chain (C = alpha * A (A B) + beta * C0), fp64 accumulation.
+"""CPU oracle for CSR SpMM (C = alpha * A * B + beta * C0), the squared
+chain (C = alpha * A (A B) + beta * C0) and the Frank-Wolfe gradient scan
+(per-column argmin of G = K2B t1 - T2 and the gap sum), fp64 accumulation.
 
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU
 baseline leg of ``bench.py`` use it; the product path never does.  The
@@ -47,6 +48,10 @@ def load_library(path: str):
     lib.oracle_spmm_squared.restype = ctypes.c_int
     lib.oracle_spmm_squared.argtypes = [ctypes.c_int, i64, i64, ctypes.c_double, p, p, p, p, i64,
                                         ctypes.c_double, p, i64, p, i64, p, p, i64]
+    lib.oracle_fw_gradient.restype = ctypes.c_int
+    lib.oracle_fw_gradient.argtypes = [ctypes.c_int, i64, i64] + [p] * 9 + [p, i64, p, p]
+    lib.oracle_fw_argmin.restype = ctypes.c_int
+    lib.oracle_fw_argmin.argtypes = [ctypes.c_int, i64, i64] + [p] * 12 + [p] * 5
     lib.oracle_csr_check.restype = ctypes.c_int
     lib.oracle_csr_check.argtypes = [i64, i64, i64, p, p]
     return lib
@@ -139,3 +144,54 @@ def spmm_problem(p, rows: Optional[np.ndarray] = None):
     """Oracle on a :class:`synth.Problem`."""
     return spmm(p.m, p.k, p.n, p.alpha, p.row_ptr, p.col_idx, p.values, p.B, p.ldb,
                 p.beta, p.C0, p.ldc, rows)
+
+
+def _csr(mat, dt):
+    rp, ci, v = mat
+    return (np.ascontiguousarray(rp, dtype=np.int32), np.ascontiguousarray(ci, dtype=np.int32),
+            np.ascontiguousarray(v, dtype=dt))
+
+
+def fw_gradient(n: int, k: int, k2b, t1, t2, rows: Optional[np.ndarray] = None, _lib=None):
+    """Rows of G = K2B t1 - T2 (each argument a CSR triple (row_ptr, col_idx,
+    values), K2B and T2 n x k, t1 k x k) in fp64, with their bound scale.
+    Returns (G, gbound), float64 [len(rows) or n, k]."""
+    dt = np.asarray(k2b[2]).dtype
+    if dt not in (np.float32, np.float64):
+        raise TypeError("values must be float32 or float64")
+    a, b, c = _csr(k2b, dt), _csr(t1, dt), _csr(t2, dt)
+    rsel = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    nrows = n if rsel is None else int(rsel.size)
+    g = np.zeros((nrows, k))
+    gb = np.zeros((nrows, k))
+    lib = _load() if _lib is None else _lib
+    rc = lib.oracle_fw_gradient(dt.itemsize, n, k, *(_ptr(x) for x in a + b + c), _ptr(rsel),
+                                nrows, _ptr(g), _ptr(gb))
+    if rc != OK:
+        raise ValueError(f"oracle_fw_gradient rejected its inputs (status {rc})")
+    return g, gb
+
+
+def fw_argmin(n: int, k: int, k2b, t1, t2, bmat, _lib=None):
+    """The Frank-Wolfe B-update scan: per column the minimum of G = K2B t1 - T2
+    over rows (lowest row on ties), and gap = sum of B * G over B's entries.
+
+    Returns a dict: min_val [k], min_idx [k] (int64), col_scale [k], gap,
+    gap_bound.
+    """
+    dt = np.asarray(k2b[2]).dtype
+    if dt not in (np.float32, np.float64):
+        raise TypeError("values must be float32 or float64")
+    a, b, c, d = _csr(k2b, dt), _csr(t1, dt), _csr(t2, dt), _csr(bmat, dt)
+    mv = np.zeros(max(k, 1))
+    mi = np.zeros(max(k, 1), np.int64)
+    cs = np.zeros(max(k, 1))
+    gap = np.zeros(1)
+    gbd = np.zeros(1)
+    lib = _load() if _lib is None else _lib
+    rc = lib.oracle_fw_argmin(dt.itemsize, n, k, *(_ptr(x) for x in a + b + c + d), _ptr(mv),
+                              _ptr(mi), _ptr(cs), _ptr(gap), _ptr(gbd))
+    if rc != OK:
+        raise ValueError(f"oracle_fw_argmin rejected its inputs (status {rc})")
+    return {"min_val": mv[:k], "min_idx": mi[:k], "col_scale": cs[:k], "gap": float(gap[0]),
+            "gap_bound": float(gbd[0])}

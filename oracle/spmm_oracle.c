@@ -247,3 +247,135 @@ int oracle_spmm_squared(int esize, int64_t m, int64_t n, double alpha,
     free(abst);
     return ORACLE_OK;
 }
+
+/*
+ * The Frank-Wolfe gradient scan of the B update (bixverse page,
+ * seacells_kernels.rs: `fw_argmin_b` doc comment and the CPU reference of its
+ * tests, `cpu_fw_argmin_b`).  With K2B and T2 = K^2 A^T given as n x k CSR,
+ * t1 = A A^T as k x k CSR and B as n x k CSR:
+ *
+ *   G[i, c] = sum_m K2B[i, m] * t1[m, c] - T2[i, c]
+ *   min_val[c] = min_i G[i, c],  min_idx[c] = the lowest i attaining it
+ *   gap = sum over stored entries (i, c) of B of B[i, c] * G[i, c]
+ *
+ * Rows are scanned in increasing i with a strict <, starting from the
+ * largest finite value and index 0, as the page's CPU scan does (so n == 0,
+ * or a column whose G never falls below that start, reports it with index
+ * 0).  Stored entries each contribute (duplicates add).  Everything is
+ * accumulated in binary64.
+ *
+ * Bound scales (for the parity tests): gbound[i, c] = sum_m |K2B[i, m]| *
+ * |t1[m, c]| + |T2[i, c]| bounds the rounding of G[i, c]; col_scale[c] is its
+ * maximum over i; gap_bound = sum over B's entries of |B[i, c]| * gbound[i, c].
+ */
+static void fw_gradient_row(int esize, int64_t k, int64_t i,
+                            const int32_t *k2b_rp, const int32_t *k2b_ci, const void *k2b_v,
+                            const int32_t *t1_rp, const int32_t *t1_ci, const void *t1_v,
+                            const int32_t *t2_rp, const int32_t *t2_ci, const void *t2_v,
+                            double *g, double *gb)
+{
+    for (int64_t c = 0; c < k; ++c) {
+        g[c] = 0.0;
+        gb[c] = 0.0;
+    }
+    for (int64_t p = k2b_rp[i]; p < (int64_t)k2b_rp[i + 1]; ++p) {
+        int64_t m = k2b_ci[p];
+        double v = load(k2b_v, p, esize);
+        for (int64_t q = t1_rp[m]; q < (int64_t)t1_rp[m + 1]; ++q) {
+            int64_t c = t1_ci[q];
+            double t = load(t1_v, q, esize);
+            g[c] += v * t;
+            gb[c] += fabs(v) * fabs(t);
+        }
+    }
+    for (int64_t q = t2_rp[i]; q < (int64_t)t2_rp[i + 1]; ++q) {
+        int64_t c = t2_ci[q];
+        double t = load(t2_v, q, esize);
+        g[c] -= t;
+        gb[c] += fabs(t);
+    }
+}
+
+static int fw_check(int64_t n, int64_t k, const int32_t *k2b_rp, const int32_t *k2b_ci,
+                    const int32_t *t1_rp, const int32_t *t1_ci, const int32_t *t2_rp,
+                    const int32_t *t2_ci)
+{
+    if (!k2b_rp || !t1_rp || !t2_rp) return ORACLE_BAD_ARGS;
+    if (oracle_csr_check(n, k, (int64_t)k2b_rp[n], k2b_rp, k2b_ci) != ORACLE_OK ||
+        oracle_csr_check(k, k, (int64_t)t1_rp[k], t1_rp, t1_ci) != ORACLE_OK ||
+        oracle_csr_check(n, k, (int64_t)t2_rp[n], t2_rp, t2_ci) != ORACLE_OK)
+        return ORACLE_BAD_CSR;
+    return ORACLE_OK;
+}
+
+/* G rows: g[r * k + c] = G[rows[r], c] and gbound likewise (rows NULL: all). */
+int oracle_fw_gradient(int esize, int64_t n, int64_t k,
+                       const int32_t *k2b_rp, const int32_t *k2b_ci, const void *k2b_v,
+                       const int32_t *t1_rp, const int32_t *t1_ci, const void *t1_v,
+                       const int32_t *t2_rp, const int32_t *t2_ci, const void *t2_v,
+                       const int64_t *rows, int64_t nrows, double *g, double *gbound)
+{
+    if ((esize != 4 && esize != 8) || n < 0 || k < 0) return ORACLE_BAD_ARGS;
+    int rc = fw_check(n, k, k2b_rp, k2b_ci, t1_rp, t1_ci, t2_rp, t2_ci);
+    if (rc != ORACLE_OK) return rc;
+    if (!rows) nrows = n;
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t i = rows ? rows[r] : r;
+        if (i < 0 || i >= n) return ORACLE_BAD_ARGS;
+        fw_gradient_row(esize, k, i, k2b_rp, k2b_ci, k2b_v, t1_rp, t1_ci, t1_v, t2_rp, t2_ci,
+                        t2_v, g + r * k, gbound + r * k);
+    }
+    return ORACLE_OK;
+}
+
+int oracle_fw_argmin(int esize, int64_t n, int64_t k,
+                     const int32_t *k2b_rp, const int32_t *k2b_ci, const void *k2b_v,
+                     const int32_t *t1_rp, const int32_t *t1_ci, const void *t1_v,
+                     const int32_t *t2_rp, const int32_t *t2_ci, const void *t2_v,
+                     const int32_t *b_rp, const int32_t *b_ci, const void *b_v,
+                     double *min_val, int64_t *min_idx, double *col_scale, double *gap,
+                     double *gap_bound)
+{
+    if ((esize != 4 && esize != 8) || n < 0 || k < 0 || !gap || !gap_bound) return ORACLE_BAD_ARGS;
+    if (k > 0 && (!min_val || !min_idx || !col_scale)) return ORACLE_BAD_ARGS;
+    int rc = fw_check(n, k, k2b_rp, k2b_ci, t1_rp, t1_ci, t2_rp, t2_ci);
+    if (rc != ORACLE_OK) return rc;
+    if (!b_rp || oracle_csr_check(n, k, (int64_t)b_rp[n], b_rp, b_ci) != ORACLE_OK)
+        return ORACLE_BAD_CSR;
+    /* the start of the scan: the largest finite value of the element type */
+    const double start = (esize == 4) ? 3.4028234663852886e38 : 1.7976931348623157e308;
+    for (int64_t c = 0; c < k; ++c) {
+        min_val[c] = start;
+        min_idx[c] = 0;
+        col_scale[c] = 0.0;
+    }
+    *gap = 0.0;
+    *gap_bound = 0.0;
+    double *g = (double *)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1));
+    double *gb = (double *)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1));
+    if (!g || !gb) {
+        free(g);
+        free(gb);
+        return ORACLE_NO_MEMORY;
+    }
+    for (int64_t i = 0; i < n; ++i) {
+        fw_gradient_row(esize, k, i, k2b_rp, k2b_ci, k2b_v, t1_rp, t1_ci, t1_v, t2_rp, t2_ci,
+                        t2_v, g, gb);
+        for (int64_t r = b_rp[i]; r < (int64_t)b_rp[i + 1]; ++r) {
+            int64_t c = b_ci[r];
+            double b = load(b_v, r, esize);
+            *gap += b * g[c];
+            *gap_bound += fabs(b) * gb[c];
+        }
+        for (int64_t c = 0; c < k; ++c) {
+            if (g[c] < min_val[c]) {             /* strict: the lowest row wins a tie */
+                min_val[c] = g[c];
+                min_idx[c] = i;
+            }
+            if (gb[c] > col_scale[c]) col_scale[c] = gb[c];
+        }
+    }
+    free(g);
+    free(gb);
+    return ORACLE_OK;
+}

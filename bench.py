@@ -12,6 +12,10 @@ over ranks and ``value`` counts the work of all ranks.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference      # the CPU oracle on a bounded sample
+
+Other workloads: ``seacells_k2b`` times the squared chain C = A (A B), and
+``seacells_fw`` the Frank-Wolfe gradient scan that consumes it (per-column
+argmin of K2B t1 - K2At and the gap), both through the same JSON line.
 """
 from __future__ import annotations
 
@@ -475,8 +479,195 @@ def run_ours(args):
     return 0
 
 
+FW_WORKLOADS = ("seacells_fw",)
+
+
+def fw_problem(name):
+    from synth import fw
+    return {"seacells_fw": fw.seacells_fw}[name]()
+
+
+def run_fw_reference(args):
+    """The oracle's scan, whole workload per step (it takes about a second)."""
+    rank, _, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    p = fw_problem(args.workload)
+    oracle.build()
+    for _ in range(args.warmup):
+        oracle.fw_argmin(p.n, p.k, p.k2b, p.t1, p.t2, p.b)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.fw_argmin(p.n, p.k, p.k2b, p.t1, p.t2, p.b)
+        times.append(time.perf_counter() - t0)
+    value = p.flops() * args.steps / sum(times) / 1e9
+    sample = f"{p.name}: all {p.n} rows per step, fp64 accumulation"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * sum(times) / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": p.name, "n": p.n, "k": p.k, "nnz_k2b": int(p.k2b[0][-1])},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GFLOP/s", "cores": 1,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}), flush=True)
+    return 0
+
+
+def run_fw_ours(args):
+    """The Frank-Wolfe gradient scan through the C ABI (same JSON contract)."""
+    import numpy as np
+    import torch
+
+    import csr_spmm_gb300 as cs
+    from csr_spmm_gb300 import build as csb
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    if rank == 0:
+        csb.build()
+    if pg:
+        pg.barrier()
+    cs.library()
+    p = fw_problem(args.workload)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    mats = [tuple(t(x) for x in m) for m in (p.k2b, p.t1, p.t2, p.b)]
+    f64 = p.dtype == np.float64
+    dt = torch.float64 if f64 else torch.float32
+    mv = torch.empty(p.k, dtype=dt, device=dev)
+    mi = torch.empty(p.k, dtype=torch.int32, device=dev)
+    gap = torch.empty(1, dtype=dt, device=dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    h = cs.Handle(local)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+    ptrs = [tuple(x.data_ptr() for x in m) for m in mats]
+
+    def call():
+        cs.spmm_fw_argmin(h.ptr, p.n, p.k, *ptrs, mv.data_ptr(), mi.data_ptr(), gap.data_ptr(),
+                          f64=f64, stream=sptr)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.25)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    for a_ev, b_ev in ev:
+        flush.zero_()
+        a_ev.record(stream)
+        call()
+        b_ev.record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    clocks = sampler.stop()
+    total_ms = sum(a.elapsed_time(b) for a, b in ev)
+    if pg:
+        tt = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    mean_ms = total_ms / args.steps
+    value = p.flops() * args.steps * world / (total_ms / 1e3) / 1e9
+    alg = p.algorithmic_bytes()
+    peak, peak_kind = measured_hbm_peak()
+    achieved = alg / (mean_ms / 1e3) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        hp = [tuple(torch.from_numpy(np.ascontiguousarray(x)).pin_memory() for x in m)
+              for m in (p.k2b, p.t1, p.t2, p.b)]
+        h_mv = torch.empty(p.k, dtype=dt).pin_memory()
+        h_mi = torch.empty(p.k, dtype=torch.int32).pin_memory()
+        h_gap = torch.empty(1, dtype=dt).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for m in hp for x in m)
+        d2h = sum(x.numel() * x.element_size() for x in (h_mv, h_mi, h_gap))
+
+        def e2e_step():
+            for dm, hm in zip(mats, hp):
+                for d, hx in zip(dm, hm):
+                    d.copy_(hx, non_blocking=True)
+            call()
+            h_mv.copy_(mv, non_blocking=True)
+            h_mi.copy_(mi, non_blocking=True)
+            h_gap.copy_(gap, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e_steps = max(3, min(args.steps, 50))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1)
+        e2e = {"value": round(p.flops() * e_steps * world / (e_ms / 1e3) / 1e9, 3),
+               "unit": "GFLOP/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": round(e_ms / e_steps, 4), "steps": e_steps}
+    h.close()
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return 0
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        passes, elapsed = 0, 0.0
+        while passes < 10 and (passes == 0 or elapsed < 10.0):
+            t0 = time.perf_counter()
+            oracle.fw_argmin(p.n, p.k, p.k2b, p.t1, p.t2, p.b)
+            elapsed += time.perf_counter() - t0
+            passes += 1
+        cpu = {"value": round(p.flops() * passes / elapsed / 1e9, 4), "unit": "GFLOP/s",
+               "cores": 1, "kind": "oracle",
+               "sample": f"{p.name}: all rows x {passes} pass(es), {elapsed:.1f} s, fp64"}
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "GFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64" if f64 else "f32", "data": "synthetic",
+        "config": {"workload": p.name, "operation": "Frank-Wolfe gradient scan: argmin_i "
+                   "(K2B t1 - K2At)[i, c] and sum(B * G)", "n": p.n, "k": p.k,
+                   "nnz_k2b": int(p.k2b[0][-1]), "nnz_t1": int(p.t1[0][-1]),
+                   "nnz_k2at": int(p.t2[0][-1]), "nnz_b": int(p.b[0][-1]),
+                   "flops": "2 nnz(K2B) k", "algorithmic_bytes": alg,
+                   "l2_flush": "2x L2 buffer written before every timed step",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "fw_scan (whole call)", "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "algorithmic_bytes_per_launch": int(alg)},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * args.steps, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse_args()
+    if args.workload in FW_WORKLOADS:
+        return run_fw_reference(args) if args.impl == "reference" else run_fw_ours(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -19,7 +19,7 @@ from ._lib import (EXPORTED, SPMM_ERR_ALLOC, SPMM_ERR_CUDA, SPMM_ERR_DIMENSION_M
                    spmm_csr_check, spmm_csr_f32, spmm_csr_f32_noalloc, spmm_csr_f64,
                    spmm_destroy, spmm_get_profile, spmm_plan_create, spmm_plan_csr_f32,
                    spmm_plan_csr_f64, spmm_plan_destroy, spmm_set_l2_persistence,
-                   spmm_csr_squared_f32, spmm_csr_squared_f64,
+                   spmm_csr_squared_f32, spmm_csr_squared_f64, spmm_fw_argmin,
                    spmm_reserve, spmm_set_profiling, status_string)
 
 __all__ = ["Handle", "spmm", "csr_check", "SpmmError", "library", "spmm_create", "spmm_destroy",
@@ -27,6 +27,7 @@ __all__ = ["Handle", "spmm", "csr_check", "SpmmError", "library", "spmm_create",
            "spmm_set_profiling", "spmm_get_profile", "spmm_csr_f32_noalloc", "spmm_plan_create",
            "spmm_plan_destroy", "spmm_set_l2_persistence", "spmm_plan_csr_f32",
            "spmm_csr_squared_f32", "spmm_csr_squared_f64", "spmm_squared",
+           "spmm_fw_argmin", "fw_argmin",
            "spmm_plan_csr_f64", "Plan", "EXPORTED"]
 
 
@@ -124,6 +125,32 @@ def spmm_squared(handle: Handle, alpha: float, row_ptr, col_idx, values, B, beta
         spmm_csr_squared_f64(*args)
     else:
         raise TypeError("values must be float32 or float64")
+
+
+def fw_argmin(handle: Handle, k: int, k2b, t1, t2, bmat, stream=None):
+    """Frank-Wolfe gradient scan on CUDA tensors: each matrix a (row_ptr,
+    col_idx, values) triple of int32 / int32 / float tensors (K2B, T2 and B
+    n x k, t1 k x k).  Returns device tensors (min_val [k], min_idx [k] int32,
+    gap [1]); enqueued on ``stream``."""
+    import torch
+    n = int(k2b[0].numel()) - 1
+    dt = k2b[2].dtype
+    if dt not in (torch.float32, torch.float64):
+        raise TypeError("values must be float32 or float64")
+    for mat, rows in ((k2b, n), (t1, k), (t2, n), (bmat, n)):
+        if int(mat[0].numel()) != rows + 1 or mat[2].dtype != dt:
+            raise ValueError("CSR triples must be (row_ptr [rows+1], col_idx, values) of one dtype")
+        if mat[0].dtype != torch.int32 or mat[1].dtype != torch.int32:
+            raise TypeError("row_ptr and col_idx must be int32")
+    dev = k2b[0].device
+    min_val = torch.empty(max(k, 1), dtype=dt, device=dev)
+    min_idx = torch.empty(max(k, 1), dtype=torch.int32, device=dev)
+    gap = torch.empty(1, dtype=dt, device=dev)
+    st = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+    ptrs = lambda m: tuple(_ptr(x) for x in m)  # noqa: E731
+    spmm_fw_argmin(handle.ptr, n, k, ptrs(k2b), ptrs(t1), ptrs(t2), ptrs(bmat), _ptr(min_val),
+                   _ptr(min_idx), _ptr(gap), f64=dt == torch.float64, stream=st)
+    return min_val[:k], min_idx[:k], gap
 
 
 class Plan:

@@ -28,7 +28,7 @@ SPMM_ERR_TOO_LARGE = 8
 EXPORTED = ("spmm_create", "spmm_destroy", "spmm_reserve", "spmm_csr_f32", "spmm_csr_f64",
             "spmm_csr_check", "spmm_set_profiling", "spmm_get_profile", "spmm_csr_f32_noalloc",
             "spmm_set_l2_persistence", "spmm_csr_squared_f32", "spmm_csr_squared_f64",
-            "spmm_plan_create", "spmm_plan_destroy", "spmm_plan_csr_f32", "spmm_plan_csr_f64",
+            "spmm_fw_argmin_f32", "spmm_fw_argmin_f64", "spmm_plan_create", "spmm_plan_destroy", "spmm_plan_csr_f32", "spmm_plan_csr_f64",
             "spmm_status_string")
 
 
@@ -94,6 +94,10 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
                        ("spmm_csr_squared_f64", ctypes.c_double)):
         fn = getattr(lib, name)
         fn.argtypes = [vp, real, vp, vp, vp, i64, vp, i64, i64, real, vp, i64, vp]
+        fn.restype = st
+    for name in ("spmm_fw_argmin_f32", "spmm_fw_argmin_f64"):
+        fn = getattr(lib, name)
+        fn.argtypes = [vp, i64, i64] + [vp] * 12 + [vp, vp, vp, vp]
         fn.restype = st
     lib.spmm_set_l2_persistence.argtypes = [vp, i64]
     lib.spmm_set_l2_persistence.restype = st
@@ -235,4 +239,15 @@ def spmm_csr_squared_f64(handle, alpha, row_ptr, col_idx, values, m, B, ldb, n, 
                                        n, float(beta), C, ldc, stream or None)
     if check:
         _check(s, "spmm_csr_squared_f64")
+    return s
+
+
+def spmm_fw_argmin(handle, n, k, k2b, t1, t2, bmat, min_val, min_idx, gap, f64=False, stream=0,
+                   check=True) -> int:
+    """Frank-Wolfe gradient scan; each matrix a (row_ptr, col_idx, values)
+    triple of device pointers, outputs device pointers."""
+    fn = library().spmm_fw_argmin_f64 if f64 else library().spmm_fw_argmin_f32
+    s = fn(handle, n, k, *k2b, *t1, *t2, *bmat, min_val, min_idx, gap, stream or None)
+    if check:
+        _check(s, "spmm_fw_argmin_f64" if f64 else "spmm_fw_argmin_f32")
     return s

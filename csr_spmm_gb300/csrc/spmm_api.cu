@@ -543,6 +543,60 @@ spmm_status_t spmm_squared_impl(spmm_handle_t h, T alpha, const int32_t* row_ptr
     return SPMM_OK;
 }
 
+// The Frank-Wolfe gradient scan of the SEACells B update (bixverse page,
+// seacells_kernels.rs, `fw_argmin_b` / `reduce_argmin_blocks`).
+template <typename T>
+spmm_status_t spmm_fw_impl(spmm_handle_t h, int64_t n, int64_t k, const int32_t* k2b_rp,
+                           const int32_t* k2b_ci, const T* k2b_v, const int32_t* t1_rp,
+                           const int32_t* t1_ci, const T* t1_v, const int32_t* t2_rp,
+                           const int32_t* t2_ci, const T* t2_v, const int32_t* b_rp,
+                           const int32_t* b_ci, const T* b_v, T* min_val, int32_t* min_idx,
+                           T* gap, void* stream) {
+    if (!h || n < 0 || k < 0) return SPMM_ERR_INVALID_ARGUMENT;
+    constexpr int64_t TILE = fw_tile<T>();
+    if (n > (int64_t)INT_MAX - 1 || k > (int64_t)INT_MAX / 2 - TILE) return SPMM_ERR_INVALID_ARGUMENT;
+    if (!gap) return SPMM_ERR_NULL_POINTER;
+    if (k > 0 && (!t1_rp || !t1_ci || !t1_v || !min_val || !min_idx)) return SPMM_ERR_NULL_POINTER;
+    if (n > 0 && (!k2b_rp || !k2b_ci || !k2b_v || !t2_rp || !t2_ci || !t2_v || !b_rp || !b_ci ||
+                  !b_v))
+        return SPMM_ERR_NULL_POINTER;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device) {
+        cudaGetLastError();
+        return SPMM_ERR_INVALID_ARGUMENT;
+    }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t ldk = std::max<int64_t>(TILE, (k + TILE - 1) / TILE * TILE);
+    const int grid = fw_blocks_per_sm<T>() * h->num_sms;
+    const int nwarps = grid * (FW_THREADS / 32);
+    size_t off = 0;
+    const size_t o_t1 = off;   off = align_up(off + sizeof(T) * (size_t)k * ldk, 256);
+    const size_t o_pv = off;   off = align_up(off + sizeof(T) * (size_t)grid * ldk, 256);
+    const size_t o_pi = off;   off = align_up(off + sizeof(int) * (size_t)grid * ldk, 256);
+    const size_t o_pg = off;   off = align_up(off + sizeof(double) * (size_t)grid, 256);
+    spmm_status_t s = ensure_scratch(h, off);
+    if (s != SPMM_OK) return s;
+    char* base = static_cast<char*>(h->scratch);
+    FwParams<T> p{};
+    p.n = (int)n;
+    p.k = (int)k;
+    p.ldk = (int)ldk;
+    p.k2b_rp = k2b_rp; p.k2b_ci = k2b_ci; p.k2b_v = k2b_v;
+    p.t1_rp = t1_rp;   p.t1_ci = t1_ci;   p.t1_v = t1_v;
+    p.t2_rp = t2_rp;   p.t2_ci = t2_ci;   p.t2_v = t2_v;
+    p.b_rp = b_rp;     p.b_ci = b_ci;     p.b_v = b_v;
+    p.t1d = reinterpret_cast<T*>(base + o_t1);
+    p.part_val = reinterpret_cast<T*>(base + o_pv);
+    p.part_idx = reinterpret_cast<int*>(base + o_pi);
+    p.part_gap = reinterpret_cast<double*>(base + o_pg);
+    p.nwarps = nwarps;
+    p.nblocks = grid;
+    p.out_val = min_val;
+    p.out_idx = min_idx;
+    p.out_gap = gap;
+    return launch_fw<T>(p, grid, st) == cudaSuccess ? SPMM_OK : SPMM_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -845,6 +899,32 @@ spmm_status_t spmm_csr_squared_f64(spmm_handle_t h, double alpha, const int32_t*
                                    double* C, int64_t ldc, void* stream) {
     return spmm_squared_impl<double>(h, alpha, row_ptr, col_idx, values, m, B, ldb, n, beta, C,
                                      ldc, stream);
+}
+
+spmm_status_t spmm_fw_argmin_f32(spmm_handle_t h, int64_t n, int64_t k,
+                                 const int32_t* k2b_row_ptr, const int32_t* k2b_col_idx,
+                                 const float* k2b_values, const int32_t* t1_row_ptr,
+                                 const int32_t* t1_col_idx, const float* t1_values,
+                                 const int32_t* t2_row_ptr, const int32_t* t2_col_idx,
+                                 const float* t2_values, const int32_t* b_row_ptr,
+                                 const int32_t* b_col_idx, const float* b_values, float* min_val,
+                                 int32_t* min_idx, float* gap, void* stream) {
+    return spmm_fw_impl<float>(h, n, k, k2b_row_ptr, k2b_col_idx, k2b_values, t1_row_ptr,
+                               t1_col_idx, t1_values, t2_row_ptr, t2_col_idx, t2_values,
+                               b_row_ptr, b_col_idx, b_values, min_val, min_idx, gap, stream);
+}
+
+spmm_status_t spmm_fw_argmin_f64(spmm_handle_t h, int64_t n, int64_t k,
+                                 const int32_t* k2b_row_ptr, const int32_t* k2b_col_idx,
+                                 const double* k2b_values, const int32_t* t1_row_ptr,
+                                 const int32_t* t1_col_idx, const double* t1_values,
+                                 const int32_t* t2_row_ptr, const int32_t* t2_col_idx,
+                                 const double* t2_values, const int32_t* b_row_ptr,
+                                 const int32_t* b_col_idx, const double* b_values,
+                                 double* min_val, int32_t* min_idx, double* gap, void* stream) {
+    return spmm_fw_impl<double>(h, n, k, k2b_row_ptr, k2b_col_idx, k2b_values, t1_row_ptr,
+                                t1_col_idx, t1_values, t2_row_ptr, t2_col_idx, t2_values,
+                                b_row_ptr, b_col_idx, b_values, min_val, min_idx, gap, stream);
 }
 
 const char* spmm_status_string(spmm_status_t s) {

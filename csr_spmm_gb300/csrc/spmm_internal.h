@@ -162,6 +162,35 @@ cudaError_t launch_scale(T* C, int64_t ldc, int m, int n, T beta, int grid, cuda
 cudaError_t launch_csr_check(const int* row_ptr, const int* col_idx, int64_t m, int64_t k,
                              int64_t nnz, int* status, cudaStream_t st);
 
+// ---- Frank-Wolfe gradient scan (spmm_fw.cu) ----
+// G = K2B t1 - T2 (n x k), per-column minimum over rows (lowest row on ties),
+// gap = sum of B * G over B's stored entries.
+template <typename T>
+struct FwParams {
+    int n, k;
+    int ldk;                        // leading dimension of the dense t1 (multiple of FW_TILE)
+    const int* k2b_rp; const int* k2b_ci; const T* k2b_v;     // n x k CSR
+    const int* t1_rp;  const int* t1_ci;  const T* t1_v;      // k x k CSR
+    const int* t2_rp;  const int* t2_ci;  const T* t2_v;      // n x k CSR
+    const int* b_rp;   const int* b_ci;   const T* b_v;       // n x k CSR
+    T* t1d;                          // scratch: dense t1 [k, ldk], zero padded
+    T* part_val;                     // scratch: per-block minima [nblocks, ldk]
+    int* part_idx;                   // scratch: per-block argmins [nblocks, ldk]
+    double* part_gap;                // scratch: per-block gap sums [nblocks]
+    int nwarps;                      // the scan's grid, in warps
+    int nblocks;                     // the scan's grid, in blocks
+    T* out_val;                      // [k]
+    int* out_idx;                    // [k]
+    T* out_gap;                      // [1]
+};
+constexpr int FW_THREADS = 256;
+// columns per pass of a warp: 32 lanes x one 16-byte vector
+template <typename T> constexpr int fw_tile() { return 32 * (16 / (int)sizeof(T)); }
+template <typename T>
+cudaError_t launch_fw(const FwParams<T>& p, int grid, cudaStream_t st);
+template <typename T>
+int fw_blocks_per_sm();
+
 // Blocks per SM the rows kernel reaches for this geometry (occupancy query).
 template <typename T>
 int rows_blocks_per_sm(const Geometry& g);

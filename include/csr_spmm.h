@@ -150,6 +150,53 @@ spmm_status_t spmm_csr_squared_f64(spmm_handle_t h, double alpha,
                                    const double *B, int64_t ldb, int64_t n,
                                    double beta, double *C, int64_t ldc, void *stream);
 
+/* ---- Frank-Wolfe gradient scan ---------------------------------------------
+ * The step after the product in the SEACells B update (bixverse page,
+ * seacells_kernels.rs: `fw_argmin_b` and `reduce_argmin_blocks`).  With K2B
+ * (= K^2 B) and T2 (= K^2 A^T) n x k CSR, t1 (= A A^T) k x k CSR and B n x k
+ * CSR, all device arrays:
+ *   G[i, c]    = sum_m K2B[i, m] * t1[m, c] - T2[i, c]   (never stored)
+ *   min_val[c] = min over i of G[i, c]; min_idx[c] = the lowest i attaining it
+ *   gap[0]     = sum over B's stored entries (i, c) of B[i, c] * G[i, c]
+ * The scan starts from the largest finite value of the element type with
+ * row 0, as the page's CPU scan does, and moves only on a strictly smaller
+ * G, so n == 0 (or a column whose G never falls below the start) reports
+ * that value with row 0.  Every row takes part, including rows with no K2B
+ * entries (G = -T2 there).  Stored duplicates each contribute.  Results
+ * are deterministic: no float atomics, and the gap is summed in binary64 in a
+ * fixed order, then rounded to the element type.
+ * Requires n, k >= 0 and valid CSR structures with column indices in [0, k)
+ * (spmm_csr_check can verify them; the hot path does not), and t1's columns
+ * ascending within each row, the page's convention (duplicates, if any, then
+ * sit together and are added).
+ * Arrays may be NULL only when n == 0 (the n x k matrices) or k == 0 (t1,
+ * min_val, min_idx); gap must always be valid.  Uses handle scratch, grown
+ * with cudaMalloc: a dense, zero-padded copy of t1 (k rows of k rounded up to
+ * 128 binary32 or 64 binary64 columns) and per-warp partial minima.  Asynchronous on `stream`;
+ * SPMM_ERR_CUDA on a launch failure. */
+spmm_status_t spmm_fw_argmin_f32(spmm_handle_t h, int64_t n, int64_t k,
+                                 const int32_t *k2b_row_ptr, const int32_t *k2b_col_idx,
+                                 const float *k2b_values,
+                                 const int32_t *t1_row_ptr, const int32_t *t1_col_idx,
+                                 const float *t1_values,
+                                 const int32_t *t2_row_ptr, const int32_t *t2_col_idx,
+                                 const float *t2_values,
+                                 const int32_t *b_row_ptr, const int32_t *b_col_idx,
+                                 const float *b_values,
+                                 float *min_val, int32_t *min_idx, float *gap, void *stream);
+
+/* Same in binary64. */
+spmm_status_t spmm_fw_argmin_f64(spmm_handle_t h, int64_t n, int64_t k,
+                                 const int32_t *k2b_row_ptr, const int32_t *k2b_col_idx,
+                                 const double *k2b_values,
+                                 const int32_t *t1_row_ptr, const int32_t *t1_col_idx,
+                                 const double *t1_values,
+                                 const int32_t *t2_row_ptr, const int32_t *t2_col_idx,
+                                 const double *t2_values,
+                                 const int32_t *b_row_ptr, const int32_t *b_col_idx,
+                                 const double *b_values,
+                                 double *min_val, int32_t *min_idx, double *gap, void *stream);
+
 /* Persisting L2 for B.  With `bytes` > 0 (or < 0 for the device maximum,
  * about 81 MiB on GB300) the handle sets the process's
  * persisting-L2 set-aside to that size (cudaLimitPersistingL2CacheSize), and

@@ -22,7 +22,7 @@ _SRC = os.path.join(_HERE, "spmm_oracle.c")
 _LIB_DIR = os.path.join(_HERE, "_build")
 _LIB = os.path.join(_LIB_DIR, "liboracle.so")
 
-OK, BAD_ARGS, BAD_CSR, NO_MEMORY = 0, -1, -2, -3
+OK, BAD_ARGS, BAD_CSR, NO_MEMORY, SINGULAR = 0, -1, -2, -3, -4
 
 _lib = None
 
@@ -52,6 +52,10 @@ def load_library(path: str):
     lib.oracle_fw_gradient.argtypes = [ctypes.c_int, i64, i64] + [p] * 9 + [p, i64, p, p]
     lib.oracle_fw_argmin.restype = ctypes.c_int
     lib.oracle_fw_argmin.argtypes = [ctypes.c_int, i64, i64] + [p] * 12 + [p] * 5
+    lib.oracle_ilu0.restype = ctypes.c_int
+    lib.oracle_ilu0.argtypes = [ctypes.c_int, i64, p, p, p, p]
+    lib.oracle_ilu0_levels.restype = i64
+    lib.oracle_ilu0_levels.argtypes = [i64, p, p, p]
     lib.oracle_csr_check.restype = ctypes.c_int
     lib.oracle_csr_check.argtypes = [i64, i64, i64, p, p]
     return lib
@@ -195,3 +199,43 @@ def fw_argmin(n: int, k: int, k2b, t1, t2, bmat, _lib=None):
         raise ValueError(f"oracle_fw_argmin rejected its inputs (status {rc})")
     return {"min_val": mv[:k], "min_idx": mi[:k], "col_scale": cs[:k], "gap": float(gap[0]),
             "gap_bound": float(gbd[0])}
+
+
+class SingularMatrix(ValueError):
+    """ILU(0) met a zero or missing pivot."""
+
+
+def ilu0(row_ptr, col_idx, values, _lib=None):
+    """ILU(0) of a square CSR matrix (columns ascending within rows), in the
+    element type of ``values`` (float32 or float64), as the oxicuda page
+    computes it.  Returns (factored values in A's pattern, depth per row).
+    Raises SingularMatrix on a zero or missing pivot."""
+    values = np.array(values, copy=True)
+    dt = values.dtype
+    if dt not in (np.float32, np.float64):
+        raise TypeError("values must be float32 or float64")
+    row_ptr = np.ascontiguousarray(row_ptr, dtype=np.int32)
+    col_idx = np.ascontiguousarray(col_idx, dtype=np.int32)
+    n = row_ptr.size - 1
+    depth = np.zeros(max(n, 1), np.int64)
+    lib = _load() if _lib is None else _lib
+    rc = lib.oracle_ilu0(dt.itemsize, n, _ptr(row_ptr), _ptr(col_idx), _ptr(values), _ptr(depth))
+    if rc == SINGULAR:
+        raise SingularMatrix("zero or missing pivot")
+    if rc != OK:
+        raise ValueError(f"oracle_ilu0 rejected its inputs (status {rc})")
+    return values, depth[:n]
+
+
+def ilu0_split(row_ptr, col_idx, factored):
+    """(L, U) as dense arrays from factors stored in A's pattern: L the
+    strictly lower part plus a unit diagonal, U the diagonal and above."""
+    row_ptr = np.asarray(row_ptr)
+    n = row_ptr.size - 1
+    L = np.eye(n)
+    U = np.zeros((n, n))
+    for i in range(n):
+        for p in range(row_ptr[i], row_ptr[i + 1]):
+            j = int(col_idx[p])
+            (L if j < i else U)[i, j] = factored[p]
+    return L, U

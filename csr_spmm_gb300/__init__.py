@@ -20,6 +20,7 @@ from ._lib import (EXPORTED, SPMM_ERR_ALLOC, SPMM_ERR_CUDA, SPMM_ERR_DIMENSION_M
                    spmm_destroy, spmm_get_profile, spmm_plan_create, spmm_plan_csr_f32,
                    spmm_plan_csr_f64, spmm_plan_destroy, spmm_set_l2_persistence,
                    spmm_csr_squared_f32, spmm_csr_squared_f64, spmm_fw_argmin,
+                   spmm_ilu0, ILU0_SINGULAR, ILU0_WAIT_TIMEOUT,
                    spmm_reserve, spmm_set_profiling, status_string)
 
 __all__ = ["Handle", "spmm", "csr_check", "SpmmError", "library", "spmm_create", "spmm_destroy",
@@ -27,7 +28,7 @@ __all__ = ["Handle", "spmm", "csr_check", "SpmmError", "library", "spmm_create",
            "spmm_set_profiling", "spmm_get_profile", "spmm_csr_f32_noalloc", "spmm_plan_create",
            "spmm_plan_destroy", "spmm_set_l2_persistence", "spmm_plan_csr_f32",
            "spmm_csr_squared_f32", "spmm_csr_squared_f64", "spmm_squared",
-           "spmm_fw_argmin", "fw_argmin",
+           "spmm_fw_argmin", "fw_argmin", "spmm_ilu0", "ilu0", "Ilu0Error",
            "spmm_plan_csr_f64", "Plan", "EXPORTED"]
 
 
@@ -151,6 +152,33 @@ def fw_argmin(handle: Handle, k: int, k2b, t1, t2, bmat, stream=None):
     spmm_fw_argmin(handle.ptr, n, k, ptrs(k2b), ptrs(t1), ptrs(t2), ptrs(bmat), _ptr(min_val),
                    _ptr(min_idx), _ptr(gap), f64=dt == torch.float64, stream=st)
     return min_val[:k], min_idx[:k], gap
+
+
+class Ilu0Error(RuntimeError):
+    """ILU(0) stopped: a zero or missing pivot, or a dependency wait ran out."""
+
+
+def ilu0(handle: Handle, row_ptr, col_idx, values, with_depth: bool = False, stream=None):
+    """ILU(0) in place on ``values`` (CUDA tensors of a square CSR matrix,
+    columns strictly ascending within rows).  Waits for the result and raises
+    Ilu0Error on failure; returns the per-row levels when ``with_depth``."""
+    import torch
+    n = int(row_ptr.numel()) - 1
+    if row_ptr.dtype != torch.int32 or col_idx.dtype != torch.int32:
+        raise TypeError("row_ptr and col_idx must be int32")
+    if values.dtype not in (torch.float32, torch.float64):
+        raise TypeError("values must be float32 or float64")
+    dev = values.device
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    depth = torch.empty(max(n, 1), dtype=torch.int32, device=dev) if with_depth else None
+    st = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+    spmm_ilu0(handle.ptr, n, int(values.numel()), _ptr(row_ptr), _ptr(col_idx), _ptr(values),
+              _ptr(depth), _ptr(status), f64=values.dtype == torch.float64, stream=st)
+    code = int(status.item())                          # synchronises
+    if code:
+        why = "zero or missing pivot" if code & ILU0_SINGULAR else "a dependency wait ran out"
+        raise Ilu0Error(f"ILU(0) failed: {why} (status {code})")
+    return depth[:n] if with_depth else None
 
 
 class Plan:

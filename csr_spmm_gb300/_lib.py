@@ -28,7 +28,8 @@ SPMM_ERR_TOO_LARGE = 8
 EXPORTED = ("spmm_create", "spmm_destroy", "spmm_reserve", "spmm_csr_f32", "spmm_csr_f64",
             "spmm_csr_check", "spmm_set_profiling", "spmm_get_profile", "spmm_csr_f32_noalloc",
             "spmm_set_l2_persistence", "spmm_csr_squared_f32", "spmm_csr_squared_f64",
-            "spmm_fw_argmin_f32", "spmm_fw_argmin_f64", "spmm_plan_create", "spmm_plan_destroy", "spmm_plan_csr_f32", "spmm_plan_csr_f64",
+            "spmm_fw_argmin_f32", "spmm_fw_argmin_f64", "spmm_ilu0_f32", "spmm_ilu0_f64",
+            "spmm_plan_create", "spmm_plan_destroy", "spmm_plan_csr_f32", "spmm_plan_csr_f64",
             "spmm_status_string")
 
 
@@ -98,6 +99,10 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
     for name in ("spmm_fw_argmin_f32", "spmm_fw_argmin_f64"):
         fn = getattr(lib, name)
         fn.argtypes = [vp, i64, i64] + [vp] * 12 + [vp, vp, vp, vp]
+        fn.restype = st
+    for name in ("spmm_ilu0_f32", "spmm_ilu0_f64"):
+        fn = getattr(lib, name)
+        fn.argtypes = [vp, i64, i64, vp, vp, vp, vp, vp, vp]
         fn.restype = st
     lib.spmm_set_l2_persistence.argtypes = [vp, i64]
     lib.spmm_set_l2_persistence.restype = st
@@ -250,4 +255,18 @@ def spmm_fw_argmin(handle, n, k, k2b, t1, t2, bmat, min_val, min_idx, gap, f64=F
     s = fn(handle, n, k, *k2b, *t1, *t2, *bmat, min_val, min_idx, gap, stream or None)
     if check:
         _check(s, "spmm_fw_argmin_f64" if f64 else "spmm_fw_argmin_f32")
+    return s
+
+
+ILU0_SINGULAR = 1
+ILU0_WAIT_TIMEOUT = 2
+
+
+def spmm_ilu0(handle, n, nnz, row_ptr, col_idx, values, depth, status, f64=False, stream=0,
+              check=True) -> int:
+    """ILU(0) in place on the device values (pointers); status is a device int32."""
+    fn = library().spmm_ilu0_f64 if f64 else library().spmm_ilu0_f32
+    s = fn(handle, n, nnz, row_ptr, col_idx, values, depth, status, stream or None)
+    if check:
+        _check(s, "spmm_ilu0_f64" if f64 else "spmm_ilu0_f32")
     return s

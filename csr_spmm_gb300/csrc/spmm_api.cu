@@ -597,6 +597,54 @@ spmm_status_t spmm_fw_impl(spmm_handle_t h, int64_t n, int64_t k, const int32_t*
     return launch_fw<T>(p, grid, st) == cudaSuccess ? SPMM_OK : SPMM_ERR_CUDA;
 }
 
+// ILU(0) of the oxicuda preconditioner page, in place, scheduled on the
+// device (dependency counts, then one persistent factorisation launch).
+template <typename T>
+spmm_status_t spmm_ilu0_impl(spmm_handle_t h, int64_t n, int64_t nnz, const int32_t* row_ptr,
+                             const int32_t* col_idx, T* values, int32_t* depth, int32_t* status,
+                             void* stream) {
+    if (!h || n <= 0 || n > (int64_t)INT_MAX - 2 || nnz < 0 || nnz > (int64_t)INT_MAX)
+        return SPMM_ERR_INVALID_ARGUMENT;
+    if (!row_ptr || !col_idx || !values || !status) return SPMM_ERR_NULL_POINTER;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device) {
+        cudaGetLastError();
+        return SPMM_ERR_INVALID_ARGUMENT;
+    }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // int words: pending[n], cnt[n], head, tail, abort | dep_ptr[n+1] | queue[n] | dep_idx[nnz]
+    const size_t zero_words = 2 * (size_t)n + 3;
+    const size_t o_ptr = zero_words, o_q = o_ptr + (size_t)n + 1, o_dep = o_q + (size_t)n;
+    const size_t words = o_dep + (size_t)std::max<int64_t>(nnz, 1);
+    spmm_status_t s = ensure_scratch(h, words * sizeof(int));
+    if (s != SPMM_OK) return s;
+    int* w = static_cast<int*>(h->scratch);
+    if (cudaMemsetAsync(w, 0, zero_words * sizeof(int), st) != cudaSuccess ||
+        cudaMemsetAsync(w + o_q, 0xff, (size_t)n * sizeof(int), st) != cudaSuccess ||
+        cudaMemsetAsync(status, 0, sizeof(int32_t), st) != cudaSuccess) {
+        cudaGetLastError();
+        return SPMM_ERR_CUDA;
+    }
+    Ilu0Params<T> p{};
+    p.n = (int)n;
+    p.nnz = nnz;
+    p.rp = row_ptr;
+    p.ci = col_idx;
+    p.v = values;
+    p.depth = depth;
+    p.pending = w;
+    p.cnt = w + n;
+    p.head = w + 2 * n;
+    p.tail = w + 2 * n + 1;
+    p.abort = w + 2 * n + 2;
+    p.dep_ptr = w + o_ptr;
+    p.queue = w + o_q;
+    p.dep_idx = w + o_dep;
+    p.status = status;
+    const int grid = ilu0_blocks_per_sm<T>() * h->num_sms;
+    return launch_ilu0<T>(p, grid, st) == cudaSuccess ? SPMM_OK : SPMM_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -925,6 +973,18 @@ spmm_status_t spmm_fw_argmin_f64(spmm_handle_t h, int64_t n, int64_t k,
     return spmm_fw_impl<double>(h, n, k, k2b_row_ptr, k2b_col_idx, k2b_values, t1_row_ptr,
                                 t1_col_idx, t1_values, t2_row_ptr, t2_col_idx, t2_values,
                                 b_row_ptr, b_col_idx, b_values, min_val, min_idx, gap, stream);
+}
+
+spmm_status_t spmm_ilu0_f32(spmm_handle_t h, int64_t n, int64_t nnz, const int32_t* row_ptr,
+                            const int32_t* col_idx, float* values, int32_t* depth,
+                            int32_t* status, void* stream) {
+    return spmm_ilu0_impl<float>(h, n, nnz, row_ptr, col_idx, values, depth, status, stream);
+}
+
+spmm_status_t spmm_ilu0_f64(spmm_handle_t h, int64_t n, int64_t nnz, const int32_t* row_ptr,
+                            const int32_t* col_idx, double* values, int32_t* depth,
+                            int32_t* status, void* stream) {
+    return spmm_ilu0_impl<double>(h, n, nnz, row_ptr, col_idx, values, depth, status, stream);
 }
 
 const char* spmm_status_string(spmm_status_t s) {

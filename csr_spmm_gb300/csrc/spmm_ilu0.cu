@@ -1,0 +1,301 @@
+// ILU(0), the incomplete LU factorisation with zero fill-in of the oxicuda
+// preconditioner page (preconditioner/ilu0.rs: module doc and
+// `factor_row_host`), factored in place on A's CSR values.
+//
+// The page analyses dependency levels on the host and launches one kernel
+// per level, synchronising the stream and reading a status word back between
+// levels.  Here the schedule is dataflow, on the device, without host
+// round trips:
+//   1. every row counts its lower entries (the rows it waits for) and adds
+//      itself to the dependent count of each of them; rows with none are
+//      queued;
+//   2. a prefix sum turns the dependent counts into list offsets;
+//   3. the dependent lists are filled (the transpose of the strict lower
+//      pattern);
+//   4. one persistent launch: a warp takes the next queue slot, waits for it
+//      to be filled, factors that row (every row it needs is final by then),
+//      publishes it, and counts down each dependent, queueing the one whose
+//      count reaches zero.
+// Any row may run as soon as its last dependency is final, so the whole
+// width of every level (the anti-diagonals of a grid) runs at once.  Waits
+// are bounded, and a failure (zero or missing pivot, or a wait that ran out)
+// stops every warp through a shared abort word and is reported in the status
+// word.
+//
+// Arithmetic follows the page step for step: per lower entry k of row i in
+// CSR order, ratio = a_ik / a_kk (rounded divide), stored, then for each
+// j > k of row k present in row i, a_ij = a_ij - ratio * a_kj with a rounded
+// multiply and a rounded subtract (no fused multiply-add), so the factors
+// equal the host reference bit for bit, whatever order the rows run in.
+#include <algorithm>
+
+#include "spmm_internal.h"
+
+namespace spmm {
+namespace {
+
+constexpr int ILU0_SINGULAR = 1;
+constexpr int ILU0_WAIT_TIMEOUT = 2;
+constexpr int ILU0_SPIN_LIMIT = 1 << 22;       // polls of one queue slot (about a second)
+#ifndef SPMM_ILU0_SLEEP_NS
+#define SPMM_ILU0_SLEEP_NS 32
+#endif
+#ifndef SPMM_ILU0_BLOCKS_PER_SM
+#define SPMM_ILU0_BLOCKS_PER_SM 1      // 0: as many as fit (measured slower: idle warps poll)
+#endif
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release(int* p, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_relaxed(const int* p) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float div_rn(float a, float b) { return __fdiv_rn(a, b); }
+__device__ __forceinline__ double div_rn(double a, double b) { return __ddiv_rn(a, b); }
+__device__ __forceinline__ float mul_rn(float a, float b) { return __fmul_rn(a, b); }
+__device__ __forceinline__ double mul_rn(double a, double b) { return __dmul_rn(a, b); }
+__device__ __forceinline__ float sub_rn(float a, float b) { return __fsub_rn(a, b); }
+__device__ __forceinline__ double sub_rn(double a, double b) { return __dsub_rn(a, b); }
+
+// 1. lower entries per row, dependents per row, the first ready rows
+template <typename T>
+__global__ void __launch_bounds__(256) ilu0_count(Ilu0Params<T> p) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= p.n) return;
+    int lower = 0;
+    for (int q = p.rp[i]; q < p.rp[i + 1]; ++q) {
+        const int k = p.ci[q];
+        if (k >= i) break;                      // columns ascend
+        atomicAdd(p.cnt + k, 1);
+        ++lower;
+    }
+    p.pending[i] = lower;
+    if (lower == 0) p.queue[atomicAdd(p.tail, 1)] = i;
+}
+
+// 2. exclusive prefix sum of cnt into dep_ptr (one block; each thread owns a
+//    contiguous chunk), then cnt is cleared to serve as the fill cursor
+template <typename T>
+__global__ void __launch_bounds__(1024) ilu0_scan(Ilu0Params<T> p) {
+    __shared__ int s[1024];
+    const int per = (p.n + 1023) / 1024;
+    const int b = threadIdx.x * per, e = min(p.n, b + per);
+    int sum = 0;
+    for (int i = b; i < e; ++i) sum += p.cnt[i];
+    s[threadIdx.x] = sum;
+    __syncthreads();
+    for (int off = 1; off < 1024; off <<= 1) {           // inclusive Hillis-Steele
+        const int x = threadIdx.x >= off ? s[threadIdx.x - off] : 0;
+        __syncthreads();
+        s[threadIdx.x] += x;
+        __syncthreads();
+    }
+    int run = s[threadIdx.x] - sum;
+    for (int i = b; i < e; ++i) {
+        p.dep_ptr[i] = run;
+        run += p.cnt[i];
+        p.cnt[i] = 0;
+    }
+    if (threadIdx.x == 1023) p.dep_ptr[p.n] = s[1023];
+}
+
+// 3. dependent lists (the order within a list only decides queue order)
+template <typename T>
+__global__ void __launch_bounds__(256) ilu0_fill(Ilu0Params<T> p) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= p.n) return;
+    for (int q = p.rp[i]; q < p.rp[i + 1]; ++q) {
+        const int k = p.ci[q];
+        if (k >= i) break;
+        p.dep_idx[p.dep_ptr[k] + atomicAdd(p.cnt + k, 1)] = i;
+    }
+}
+
+__device__ __forceinline__ void stop(int* abort, int* status, int bit) {
+    atomicOr(status, bit);
+    atomicExch(abort, 1);
+}
+
+// Row i in global memory (any length): the page's steps, lanes sharing the
+// updates of each elimination step.
+template <typename T>
+__device__ bool factor_row_long(const Ilu0Params<T>& p, int i, int s, int e, int lane,
+                                int& dmax) {
+    for (int nz = s; nz < e; ++nz) {
+        const int k = p.ci[nz];
+        if (k >= i) break;                  // past the lower triangle (columns ascend)
+        // the pivot a_kk: the first position of column k in row k
+        const int ks = p.rp[k], ke = p.rp[k + 1];
+        int dp = -1;
+        for (int q0 = ks; q0 < ke && dp < 0; q0 += 32) {
+            const unsigned hit = __ballot_sync(FULL, q0 + lane < ke && p.ci[q0 + lane] == k);
+            if (hit) dp = q0 + __ffs(hit) - 1;
+        }
+        const T akk = dp >= 0 ? __ldcg(p.v + dp) : T(0);
+        if (dp < 0 || akk == T(0)) {
+            if (lane == 0) stop(p.abort, p.status, ILU0_SINGULAR);
+            return false;
+        }
+        const T ratio = div_rn(__ldcg(p.v + nz), akk);
+        if (lane == 0) p.v[nz] = ratio;
+        // a_ij -= ratio * a_kj for the columns j > k of row k stored in row i
+        for (int knz = dp + 1 + lane; knz < ke; knz += 32) {
+            const int j = p.ci[knz];
+            int ij = -1;
+            for (int q = s; q < e; ++q)
+                if (p.ci[q] == j) {
+                    ij = q;
+                    break;
+                }
+            if (ij >= 0) p.v[ij] = sub_rn(__ldcg(p.v + ij), mul_rn(ratio, __ldcg(p.v + knz)));
+        }
+        __syncwarp();
+        if (p.depth) dmax = max(dmax, __ldcg(p.depth + k));
+    }
+    return true;
+}
+
+// Row i of at most 32 entries, held in registers (lane q: entry q) from the
+// first load to the final store; pivot rows are read 32 entries at a time.
+// Same steps and operations as the page, so the same bits.
+template <typename T>
+__device__ bool factor_row_short(const Ilu0Params<T>& p, int i, int s, int e, int lane,
+                                 int& dmax) {
+    const int li = e - s;
+    const bool mine = lane < li;
+    const int my_c = mine ? p.ci[s + lane] : 0x7fffffff;
+    T my_v = mine ? __ldcg(p.v + s + lane) : T(0);
+    const int nlower = __popc(__ballot_sync(FULL, mine && my_c < i));   // columns ascend
+    // the pivot rows' extents, all at once
+    int kb = 0, kend = 0;
+    if (lane < nlower) {
+        kb = p.rp[my_c];
+        kend = p.rp[my_c + 1];
+    }
+    for (int t = 0; t < nlower; ++t) {
+        const int k = __shfl_sync(FULL, my_c, t);
+        const int ks = __shfl_sync(FULL, kb, t), ke = __shfl_sync(FULL, kend, t);
+        const T aik = __shfl_sync(FULL, my_v, t);
+        int dp = -1;                          // the pivot's position in row k
+        bool zero = false;
+        T ratio = T(0);
+        for (int q0 = ks; q0 < ke; q0 += 32) {
+            const bool have = q0 + lane < ke;
+            const int kc = have ? p.ci[q0 + lane] : -1;
+            const T kv = have ? __ldcg(p.v + q0 + lane) : T(0);
+            int first = 0;                    // first entry of this chunk past the pivot
+            if (dp < 0) {
+                const unsigned hit = __ballot_sync(FULL, kc == k);
+                if (!hit) continue;
+                const int dl = __ffs(hit) - 1;
+                dp = q0 + dl;
+                const T akk = __shfl_sync(FULL, kv, dl);
+                if (akk == T(0)) {
+                    zero = true;
+                    break;
+                }
+                ratio = div_rn(aik, akk);
+                if (lane == t) my_v = ratio;
+                first = dl + 1;
+            }
+            // a_ij -= ratio * a_kj for the entries j > k of row k that row i stores
+            const int cnt = min(32, ke - q0);
+            for (int q = first; q < cnt; ++q) {
+                const int j = __shfl_sync(FULL, kc, q);
+                const T akj = __shfl_sync(FULL, kv, q);
+                if (mine && my_c == j) my_v = sub_rn(my_v, mul_rn(ratio, akj));
+            }
+        }
+        if (dp < 0 || zero) {                 // no pivot stored, or a zero one
+            if (lane == 0) stop(p.abort, p.status, ILU0_SINGULAR);
+            return false;
+        }
+    }
+    if (p.depth) {
+        int d = lane < nlower ? __ldcg(p.depth + my_c) : -1;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) d = max(d, __shfl_xor_sync(FULL, d, off));
+        dmax = d;
+    }
+    if (mine) p.v[s + lane] = my_v;
+    return true;
+}
+
+// 4. the factorisation, one warp per ready row
+template <typename T>
+__global__ void __launch_bounds__(ILU0_THREADS) ilu0_factor(Ilu0Params<T> p) {
+    const int lane = threadIdx.x & 31;
+    for (;;) {
+        int h = 0;
+        if (lane == 0) h = atomicAdd(p.head, 1);
+        h = __shfl_sync(FULL, h, 0);
+        if (h >= p.n) return;
+        // wait for slot h to be filled (a dependency of some row becoming final)
+        int i = -1;
+        for (int it = 0;; ++it) {
+            i = ld_acquire(p.queue + h);
+            if (__all_sync(FULL, i >= 0)) break;
+            if (__any_sync(FULL, ld_relaxed(p.abort) != 0)) return;
+            if (it >= ILU0_SPIN_LIMIT) {
+                if (lane == 0) stop(p.abort, p.status, ILU0_WAIT_TIMEOUT);
+                return;
+            }
+            __nanosleep(SPMM_ILU0_SLEEP_NS);
+        }
+        const int s = p.rp[i], e = p.rp[i + 1];
+        int dmax = -1;
+        bool ok;
+        if (e - s <= 32) ok = factor_row_short<T>(p, i, s, e, lane, dmax);
+        else ok = factor_row_long<T>(p, i, s, e, lane, dmax);
+        if (!ok) return;
+        if (p.depth && lane == 0) p.depth[i] = dmax + 1;
+        __syncwarp();
+        __threadfence();                        // row i final before it is counted down
+        // count down the rows that wait for row i; queue those now ready
+        for (int d = p.dep_ptr[i] + lane; d < p.dep_ptr[i + 1]; d += 32) {
+            const int j = p.dep_idx[d];
+            if (atomicSub(p.pending + j, 1) == 1) {
+                __threadfence();
+                st_release(p.queue + atomicAdd(p.tail, 1), j);
+            }
+        }
+    }
+}
+
+}  // namespace
+
+template <typename T>
+cudaError_t launch_ilu0(const Ilu0Params<T>& p, int grid, cudaStream_t st) {
+    const int rb = (p.n + 255) / 256;
+    ilu0_count<T><<<rb, 256, 0, st>>>(p);
+    ilu0_scan<T><<<1, 1024, 0, st>>>(p);
+    ilu0_fill<T><<<rb, 256, 0, st>>>(p);
+    ilu0_factor<T><<<grid, ILU0_THREADS, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename T>
+int ilu0_blocks_per_sm() {
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, ilu0_factor<T>, ILU0_THREADS, 0) !=
+            cudaSuccess || b < 1) {
+        cudaGetLastError();
+        b = 1;
+    }
+    return SPMM_ILU0_BLOCKS_PER_SM > 0 ? std::min(b, SPMM_ILU0_BLOCKS_PER_SM) : b;
+}
+
+template cudaError_t launch_ilu0<float>(const Ilu0Params<float>&, int, cudaStream_t);
+template cudaError_t launch_ilu0<double>(const Ilu0Params<double>&, int, cudaStream_t);
+template int ilu0_blocks_per_sm<float>();
+template int ilu0_blocks_per_sm<double>();
+
+}  // namespace spmm

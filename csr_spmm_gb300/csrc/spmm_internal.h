@@ -191,6 +191,32 @@ cudaError_t launch_fw(const FwParams<T>& p, int grid, cudaStream_t st);
 template <typename T>
 int fw_blocks_per_sm();
 
+// ---- ILU(0), dataflow-scheduled (spmm_ilu0.cu) ----
+template <typename T>
+struct Ilu0Params {
+    int n;
+    int64_t nnz;
+    const int* rp;
+    const int* ci;
+    T* v;                  // A's values in, the L \ U factors out (in place)
+    int* depth;            // optional: each row's level
+    // scratch
+    int* pending;          // [n] lower entries of the row not yet final
+    int* cnt;              // [n] rows depending on the row (then a fill cursor)
+    int* dep_ptr;          // [n + 1] start of each row's dependents
+    int* dep_idx;          // [nnz] dependent rows, grouped by the row they depend on
+    int* queue;            // [n] rows in the order they became ready (-1: not yet)
+    int* head;             // next queue slot to take
+    int* tail;             // next queue slot to fill
+    int* abort;            // stop every warp (a failure was met)
+    int* status;           // caller's: 0, or ILU0 failure bits
+};
+constexpr int ILU0_THREADS = 256;
+template <typename T>
+cudaError_t launch_ilu0(const Ilu0Params<T>& p, int grid, cudaStream_t st);
+template <typename T>
+int ilu0_blocks_per_sm();
+
 // Blocks per SM the rows kernel reaches for this geometry (occupancy query).
 template <typename T>
 int rows_blocks_per_sm(const Geometry& g);

@@ -197,6 +197,43 @@ spmm_status_t spmm_fw_argmin_f64(spmm_handle_t h, int64_t n, int64_t k,
                                  const double *b_values,
                                  double *min_val, int32_t *min_idx, double *gap, void *stream);
 
+/* ---- ILU(0) ------------------------------------------------------------------
+ * Incomplete LU factorisation with zero fill-in of the oxicuda preconditioner
+ * page (preconditioner/ilu0.rs, module doc and `factor_row_host`): A ~ L U
+ * with L unit lower and U upper triangular, both in A's sparsity pattern.
+ * Factored in place on `values` (device, A's n x n CSR values): afterwards the
+ * strictly lower entries hold L (its unit diagonal is implicit) and the
+ * diagonal and upper entries hold U; the page's (L, U) split is that reading.
+ * Arithmetic as on the page: for each stored k < i of row i in CSR order,
+ * a_ik = a_ik / a_kk, then a_ij = a_ij - a_ik * a_kj for each stored j > k
+ * of row k that row i also stores, each a single rounded operation in the
+ * element type (no fused multiply-add), so the result matches the page's host
+ * reference bit for bit.  depth (optional, device [n]) receives each row's
+ * dependency level (the page's level analysis: 1 + the deepest k < i stored
+ * in row i, 0 if none).
+ * Scheduled on the device without host synchronisation: dependency counts and
+ * the lists of dependent rows are built by three small kernels, then one
+ * persistent launch factors each row as soon as the rows it depends on are
+ * final (the page launches one kernel per level and synchronises between
+ * them).  nnz = row_ptr[n] (the library cannot read it without a
+ * synchronisation).  status (device, one int32, required) is
+ * zeroed, then receives SPMM_ILU0_SINGULAR if a pivot row lacks its diagonal
+ * or has a zero one, and SPMM_ILU0_WAIT_TIMEOUT if a wait for a pivot row ran
+ * out (every wait is bounded; neither happens on valid input).  After a
+ * failure the values are partly factored.
+ * Requires n >= 1 (n == 0: SPMM_ERR_INVALID_ARGUMENT, as the page), a valid
+ * CSR structure with column indices strictly ascending within each row (no
+ * duplicates), and no concurrent call on the same handle (it uses handle
+ * scratch: 4n + nnz + 4 int32 words).  Asynchronous on `stream`. */
+#define SPMM_ILU0_SINGULAR 1
+#define SPMM_ILU0_WAIT_TIMEOUT 2
+spmm_status_t spmm_ilu0_f32(spmm_handle_t h, int64_t n, int64_t nnz, const int32_t *row_ptr,
+                            const int32_t *col_idx, float *values, int32_t *depth,
+                            int32_t *status, void *stream);
+spmm_status_t spmm_ilu0_f64(spmm_handle_t h, int64_t n, int64_t nnz, const int32_t *row_ptr,
+                            const int32_t *col_idx, double *values, int32_t *depth,
+                            int32_t *status, void *stream);
+
 /* Persisting L2 for B.  With `bytes` > 0 (or < 0 for the device maximum,
  * about 81 MiB on GB300) the handle sets the process's
  * persisting-L2 set-aside to that size (cudaLimitPersistingL2CacheSize), and

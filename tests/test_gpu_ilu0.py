@@ -1,0 +1,137 @@
+"""GPU ILU(0) (the oxicuda preconditioner page's factorisation) against the
+CPU oracle.  Both take the page's steps with single rounded operations in
+the element type, so the factors must agree bit for bit, and the per-row
+levels exactly."""
+import numpy as np
+import pytest
+
+import csr_spmm_gb300 as cs
+import oracle
+from synth import laplacian_2d
+from test_oracle_ilu0 import random_dd, tridiag
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def handle():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build_library()
+    h = cs.Handle(0)
+    yield h
+    h.close()
+
+
+def gpu_ilu0(handle, rp, ci, v):
+    import torch
+    t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a, dtype=dt)).cuda()  # noqa: E731
+    vals = t(v, v.dtype)
+    depth = cs.ilu0(handle, t(rp, np.int32), t(ci, np.int32), vals, with_depth=True)
+    return vals.cpu().numpy(), depth.cpu().numpy().astype(np.int64)
+
+
+def check(handle, rp, ci, v, what):
+    want, wdepth = oracle.ilu0(rp, ci, v)
+    got, depth = gpu_ilu0(handle, rp, ci, v)
+    bits = np.uint32 if v.dtype == np.float32 else np.uint64
+    bad = np.nonzero(got.view(bits) != want.view(bits))[0]
+    assert bad.size == 0, f"{what}: {bad.size} factors differ, first at {bad[:3]}"
+    assert np.array_equal(depth, wdepth), what
+
+
+PAGE = {
+    "dense_2x2": ([0, 2, 4], [0, 1, 0, 1], [4.0, 2.0, 1.0, 3.0]),
+    "dense_3x3": ([0, 3, 6, 9], [0, 1, 2, 0, 1, 2, 0, 1, 2],
+                  [4.0, 1.0, 2.0, 1.0, 5.0, 1.0, 2.0, 1.0, 6.0]),
+    "identity_4": ([0, 1, 2, 3, 4], [0, 1, 2, 3], [1.0, 1.0, 1.0, 1.0]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PAGE))
+def test_page_matrices(handle, name):
+    rp, ci, v = PAGE[name]
+    check(handle, np.array(rp), np.array(ci), np.array(v), name)
+
+
+@pytest.mark.parametrize("dtype", [np.float64, np.float32])
+def test_tridiagonal(handle, dtype):
+    rp, ci, v = tridiag(5, dtype=dtype)
+    check(handle, rp, ci, v, "tridiagonal 5")
+    rp, ci, v = tridiag(3000, dtype=dtype)          # one long dependency chain
+    check(handle, rp, ci, v, "tridiagonal 3000")
+
+
+@pytest.mark.parametrize("dtype", [np.float64, np.float32])
+def test_random_sparse(handle, dtype):
+    for n, per, seed in ((500, 5, 1), (20_000, 9, 2)):
+        rp, ci, v = random_dd(n, per, seed, dtype=dtype)
+        check(handle, rp, ci, v, f"random {n}")
+
+
+def mixed_lengths(n, seed, dtype=np.float64):
+    """Rows of about 12 entries, every 7th row about 60 (past one warp), so
+    both the register path and the long-row path run, and short rows pivot
+    on long ones."""
+    from synth import distinct_sorted_columns, rng
+    lens = np.where(np.arange(n) % 7 == 0, 60, 12).astype(np.int64)
+    rp, ci = distinct_sorted_columns(lens, n, seed, 21)
+    rows = np.repeat(np.arange(n), np.diff(rp))
+    keys = np.unique(np.concatenate([rows * n + ci, np.arange(n) * (n + 1)]))
+    r, c = keys // n, keys % n
+    vals = rng.uniform(seed, 22, keys.size, -1.0, 1.0)
+    vals[r == c] = 70.0 + rng.uniform(seed, 23, n)
+    rp2 = np.zeros(n + 1, np.int64)
+    np.cumsum(np.bincount(r, minlength=n), out=rp2[1:])
+    return rp2, c, vals.astype(dtype)
+
+
+@pytest.mark.parametrize("dtype", [np.float64, np.float32])
+def test_long_rows(handle, dtype):
+    rp, ci, v = mixed_lengths(4000, 3, dtype)
+    check(handle, rp, ci, v, "mixed row lengths")
+    rp, ci, v = random_dd(1500, 45, 4, dtype=dtype)          # every row past one warp
+    check(handle, rp, ci, v, "long rows")
+
+
+def test_laplacian_grid(handle):
+    p = laplacian_2d(60, 1, seed=3)
+    check(handle, p.row_ptr, p.col_idx, p.values.astype(np.float64), "laplacian 60")
+
+
+def test_laplacian_707_full(handle):
+    """The 707 x 707 5-point Laplacian of the preconditioner-shaped workload
+    (499,849 rows, 1413 levels), in binary64 and binary32."""
+    p = laplacian_2d(707, 1, seed=3)
+    check(handle, p.row_ptr, p.col_idx, p.values.astype(np.float64), "laplacian 707 f64")
+    check(handle, p.row_ptr, p.col_idx, p.values.astype(np.float32), "laplacian 707 f32")
+
+
+def test_singular_pivot_reported(handle):
+    # the page's singular case: zero diagonal in row 0, row 1 pivots on it
+    with pytest.raises(cs.Ilu0Error, match="pivot"):
+        gpu_ilu0(handle, np.array([0, 2, 4]), np.array([0, 1, 0, 1]),
+                 np.array([0.0, 2.0, 1.0, 3.0]))
+    # a pivot row without a stored diagonal
+    with pytest.raises(cs.Ilu0Error, match="pivot"):
+        gpu_ilu0(handle, np.array([0, 1, 3]), np.array([1, 0, 1]), np.array([2.0, 1.0, 3.0]))
+    # the handle still works afterwards
+    rp, ci, v = tridiag(50)
+    check(handle, rp, ci, v, "after a failure")
+
+
+def test_deterministic(handle):
+    rp, ci, v = random_dd(30_000, 7, 5)
+    a, _ = gpu_ilu0(handle, rp, ci, v)
+    b, _ = gpu_ilu0(handle, rp, ci, v)
+    assert np.array_equal(a.view(np.uint64), b.view(np.uint64))
+
+
+def test_rejects_empty(handle):
+    import torch
+    z = torch.zeros(1, dtype=torch.int32, device="cuda")
+    s = cs.spmm_ilu0(handle.ptr, 0, 0, z.data_ptr(), z.data_ptr(), z.data_ptr(), 0, z.data_ptr(),
+                     check=False)
+    assert s == 1                                     # SPMM_ERR_INVALID_ARGUMENT (as the page)

@@ -612,8 +612,9 @@ spmm_status_t spmm_ilu0_impl(spmm_handle_t h, int64_t n, int64_t nnz, const int3
         return SPMM_ERR_INVALID_ARGUMENT;
     }
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    // int words: pending[n], cnt[n], head, tail, abort | dep_ptr[n+1] | queue[n] | dep_idx[nnz]
-    const size_t zero_words = 2 * (size_t)n + 3;
+    // int words: pending[n], cnt[n], head, tail, abort, finished | dep_ptr[n+1] | queue[n] |
+    // dep_idx[nnz]
+    const size_t zero_words = 2 * (size_t)n + 4;
     const size_t o_ptr = zero_words, o_q = o_ptr + (size_t)n + 1, o_dep = o_q + (size_t)n;
     const size_t words = o_dep + (size_t)std::max<int64_t>(nnz, 1);
     spmm_status_t s = ensure_scratch(h, words * sizeof(int));
@@ -637,6 +638,7 @@ spmm_status_t spmm_ilu0_impl(spmm_handle_t h, int64_t n, int64_t nnz, const int3
     p.head = w + 2 * n;
     p.tail = w + 2 * n + 1;
     p.abort = w + 2 * n + 2;
+    p.finished = w + 2 * n + 3;
     p.dep_ptr = w + o_ptr;
     p.queue = w + o_q;
     p.dep_idx = w + o_dep;

@@ -40,8 +40,11 @@ constexpr int ILU0_SPIN_LIMIT = 1 << 22;       // polls of one queue slot (about
 #ifndef SPMM_ILU0_SLEEP_NS
 #define SPMM_ILU0_SLEEP_NS 32
 #endif
+#ifndef SPMM_ILU0_POLL_EVERY
+#define SPMM_ILU0_POLL_EVERY 16        // a power of two
+#endif
 #ifndef SPMM_ILU0_BLOCKS_PER_SM
-#define SPMM_ILU0_BLOCKS_PER_SM 1      // 0: as many as fit (measured slower: idle warps poll)
+#define SPMM_ILU0_BLOCKS_PER_SM 2      // 0: as many as fit (measured slower: idle warps poll)
 #endif
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
@@ -229,26 +232,55 @@ __device__ bool factor_row_short(const Ilu0Params<T>& p, int i, int s, int e, in
     return true;
 }
 
-// 4. the factorisation, one warp per ready row
+__device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;"
+                 : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+// 4. the factorisation, one warp per ready row.  A warp that makes rows ready
+// by finishing its own keeps the first of them (no queue round trip on the
+// critical path) and queues the rest.  Waiting warps give up only when no
+// row has finished anywhere for ILU0_SPIN_LIMIT polls, or on the abort word.
 template <typename T>
 __global__ void __launch_bounds__(ILU0_THREADS) ilu0_factor(Ilu0Params<T> p) {
     const int lane = threadIdx.x & 31;
+    int next = -1;                              // a row this warp made ready
     for (;;) {
-        int h = 0;
-        if (lane == 0) h = atomicAdd(p.head, 1);
-        h = __shfl_sync(FULL, h, 0);
-        if (h >= p.n) return;
-        // wait for slot h to be filled (a dependency of some row becoming final)
-        int i = -1;
-        for (int it = 0;; ++it) {
-            i = ld_acquire(p.queue + h);
-            if (__all_sync(FULL, i >= 0)) break;
-            if (__any_sync(FULL, ld_relaxed(p.abort) != 0)) return;
-            if (it >= ILU0_SPIN_LIMIT) {
-                if (lane == 0) stop(p.abort, p.status, ILU0_WAIT_TIMEOUT);
-                return;
+        int i = next;
+        next = -1;
+        if (i < 0) {
+            int h = 0;
+            if (lane == 0) h = atomicAdd(p.head, 1);
+            h = __shfl_sync(FULL, h, 0);
+            if (h >= p.n) return;
+            // wait for slot h to be filled, or for every row to be finished
+            int seen = -1;
+            for (int it = 0;; ++it) {
+                i = ld_acquire(p.queue + h);
+                if (__all_sync(FULL, i >= 0)) break;
+                // the shared words every SPMM_ILU0_POLL_EVERY polls (they are hot lines)
+                if ((it & (SPMM_ILU0_POLL_EVERY - 1)) == SPMM_ILU0_POLL_EVERY - 1) {
+                    int ab = 0, fin = 0;
+                    if (lane == 0) {
+                        ab = ld_relaxed(p.abort);
+                        fin = ld_relaxed(p.finished);
+                    }
+                    ab = __shfl_sync(FULL, ab, 0);
+                    fin = __shfl_sync(FULL, fin, 0);
+                    if (ab != 0 || fin >= p.n) return;
+                    if (fin != seen) {           // progress somewhere: keep waiting
+                        seen = fin;
+                        it = 0;
+                    }
+                }
+                if (it >= ILU0_SPIN_LIMIT) {
+                    if (lane == 0) stop(p.abort, p.status, ILU0_WAIT_TIMEOUT);
+                    return;
+                }
+                __nanosleep(SPMM_ILU0_SLEEP_NS);
             }
-            __nanosleep(SPMM_ILU0_SLEEP_NS);
         }
         const int s = p.rp[i], e = p.rp[i + 1];
         int dmax = -1;
@@ -259,14 +291,28 @@ __global__ void __launch_bounds__(ILU0_THREADS) ilu0_factor(Ilu0Params<T> p) {
         if (p.depth && lane == 0) p.depth[i] = dmax + 1;
         __syncwarp();
         __threadfence();                        // row i final before it is counted down
-        // count down the rows that wait for row i; queue those now ready
-        for (int d = p.dep_ptr[i] + lane; d < p.dep_ptr[i + 1]; d += 32) {
-            const int j = p.dep_idx[d];
-            if (atomicSub(p.pending + j, 1) == 1) {
-                __threadfence();
-                st_release(p.queue + atomicAdd(p.tail, 1), j);
+        // count down the rows that wait for row i (acquire: a row that becomes
+        // ready here sees its other dependencies' values); keep one, queue the rest
+        const int d0 = p.dep_ptr[i], d1 = p.dep_ptr[i + 1];
+        for (int d = d0; d < d1; d += 32) {
+            int j = -1;
+            bool ready = false;
+            if (d + lane < d1) {
+                j = p.dep_idx[d + lane];
+                ready = atom_add_acq_rel(p.pending + j, -1) == 1;
             }
+            unsigned rm = __ballot_sync(FULL, ready);
+            if (next < 0 && rm) {
+                const int keep = __ffs(rm) - 1;
+                next = __shfl_sync(FULL, j, keep);
+                if (lane == keep) ready = false;
+                rm &= rm - 1;
+            }
+            if (ready) st_release(p.queue + atomicAdd(p.tail, 1), j);
         }
+        __syncwarp();
+        if (lane == 0) atomicAdd(p.finished, 1);
+        if (next >= 0) ld_acquire(p.pending + next);   // every lane: acquire the row's inputs
     }
 }
 

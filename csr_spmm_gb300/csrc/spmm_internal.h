@@ -209,6 +209,7 @@ struct Ilu0Params {
     int* head;             // next queue slot to take
     int* tail;             // next queue slot to fill
     int* abort;            // stop every warp (a failure was met)
+    int* finished;         // rows factored so far (termination and progress)
     int* status;           // caller's: 0, or ILU0 failure bits
 };
 constexpr int ILU0_THREADS = 256;

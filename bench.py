@@ -15,7 +15,8 @@ over ranks and ``value`` counts the work of all ranks.
 
 Other workloads: ``seacells_k2b`` times the squared chain C = A (A B), and
 ``seacells_fw`` the Frank-Wolfe gradient scan that consumes it (per-column
-argmin of K2B t1 - K2At and the gap), both through the same JSON line.
+argmin of K2B t1 - K2At and the gap), and ``laplacian_707_ilu0`` the ILU(0)
+factorisation of the 707 x 707 Laplacian, all through the same JSON line.
 """
 from __future__ import annotations
 
@@ -664,8 +665,225 @@ def run_fw_ours(args):
     return 0
 
 
+ILU0_WORKLOADS = ("laplacian_707_ilu0",)
+
+
+def ilu0_problem(name):
+    """The 707 x 707 5-point Laplacian of the preconditioner-shaped workload
+    (binary64), as the matrix ILU(0) factors."""
+    import numpy as np
+
+    from synth import laplacian_2d
+    p = laplacian_2d(707, 1, seed=3, name=name)
+    return p.row_ptr, p.col_idx, p.values.astype(np.float64)
+
+
+def ilu0_flops(rp, ci):
+    """One divide per stored lower entry, a multiply and a subtract per update
+    a_ij -= l_ik u_kj (j > k stored in both rows i and k)."""
+    import numpy as np
+    n = rp.size - 1
+    lens = np.diff(rp).astype(np.int64)
+    rows = np.repeat(np.arange(n, dtype=np.int64), lens)
+    cols = ci.astype(np.int64)
+    keys = rows * n + cols
+    diag = np.full(n, -1, np.int64)
+    dmask = cols == rows
+    diag[rows[dmask]] = np.nonzero(dmask)[0]
+    lower = np.nonzero(cols < rows)[0]
+    k = cols[lower]
+    first = diag[k] + 1
+    cnt = np.where(diag[k] >= 0, rp[k + 1].astype(np.int64) - first, 0)
+    pairs_i = np.repeat(rows[lower], cnt)
+    offs = np.repeat(first - np.concatenate([[0], np.cumsum(cnt)[:-1]]), cnt)
+    pos = np.arange(int(cnt.sum()), dtype=np.int64) + offs
+    want = pairs_i * n + cols[pos]
+    hit = np.searchsorted(keys, want)
+    found = (hit < keys.size) & (keys[np.minimum(hit, keys.size - 1)] == want)
+    return int(lower.size + 2 * int(found.sum()))
+
+
+def run_ilu0_reference(args):
+    rank, _, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    rp, ci, v = ilu0_problem(args.workload)
+    oracle.build()
+    flops = ilu0_flops(rp, ci)
+    for _ in range(args.warmup):
+        oracle.ilu0(rp, ci, v)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.ilu0(rp, ci, v)
+        times.append(time.perf_counter() - t0)
+    value = flops * args.steps / sum(times) / 1e9
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "GFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * sum(times) / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "n": int(rp.size - 1), "nnz": int(ci.size),
+                   "flops_per_factorisation": flops},
+        "cpu_baseline": {"value": round(value, 5), "unit": "GFLOP/s", "cores": 1,
+                         "kind": "oracle", "sample": f"{args.workload}: whole factorisation"},
+        "e2e": {"value": round(value, 5), "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}), flush=True)
+    return 0
+
+
+def run_ilu0_ours(args):
+    """ILU(0) through the C ABI, in place on a fresh copy of A's values each
+    step (the copy and the L2 flush are outside the timed events)."""
+    import numpy as np
+    import torch
+
+    import csr_spmm_gb300 as cs
+    from csr_spmm_gb300 import build as csb
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    if rank == 0:
+        csb.build()
+    if pg:
+        pg.barrier()
+    cs.library()
+    rp, ci, v = ilu0_problem(args.workload)
+    n, nnz = int(rp.size - 1), int(ci.size)
+    flops = ilu0_flops(rp, ci)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    rpd, cid, v0 = t(rp.astype(np.int32)), t(ci.astype(np.int32)), t(v)
+    vals = v0.clone()
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    h = cs.Handle(local)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+
+    def call():
+        cs.spmm_ilu0(h.ptr, n, nnz, rpd.data_ptr(), cid.data_ptr(), vals.data_ptr(), 0,
+                     status.data_ptr(), f64=True, stream=sptr)
+
+    for _ in range(max(3, args.warmup)):
+        vals.copy_(v0)
+        call()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"ILU(0) failed with status {int(status.item())}")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.25)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    for a_ev, b_ev in ev:
+        vals.copy_(v0)
+        flush.zero_()
+        a_ev.record(stream)
+        call()
+        b_ev.record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    clocks = sampler.stop()
+    total_ms = sum(a.elapsed_time(b) for a, b in ev)
+    if pg:
+        tt = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    mean_ms = total_ms / args.steps
+    value = flops * args.steps * world / (total_ms / 1e3) / 1e9
+    # bytes: the structure read and the values read and written once
+    alg = 4 * (n + 1) + 4 * nnz + 2 * 8 * nnz
+    peak, peak_kind = measured_hbm_peak()
+    achieved = alg / (mean_ms / 1e3) / 1e9
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+        h_rp, h_ci, h_v = pin(rp.astype(np.int32)), pin(ci.astype(np.int32)), pin(v)
+        h_out = torch.empty_like(h_v).pin_memory()
+        h_status = torch.empty(1, dtype=torch.int32).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in (h_rp, h_ci, h_v))
+        d2h = h_out.numel() * h_out.element_size() + 4
+
+        def e2e_step():
+            rpd.copy_(h_rp, non_blocking=True)
+            cid.copy_(h_ci, non_blocking=True)
+            vals.copy_(h_v, non_blocking=True)
+            call()
+            h_out.copy_(vals, non_blocking=True)
+            h_status.copy_(status, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e_steps = max(3, min(args.steps, 50))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1)
+        e2e = {"value": round(flops * e_steps * world / (e_ms / 1e3) / 1e9, 4),
+               "unit": "GFLOP/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": round(e_ms / e_steps, 4), "steps": e_steps}
+    h.close()
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return 0
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        passes, elapsed = 0, 0.0
+        while passes < 200 and (passes == 0 or elapsed < 5.0):
+            t0 = time.perf_counter()
+            oracle.ilu0(rp, ci, v)
+            elapsed += time.perf_counter() - t0
+            passes += 1
+        cpu = {"value": round(flops * passes / elapsed / 1e9, 5), "unit": "GFLOP/s", "cores": 1,
+               "kind": "oracle",
+               "sample": f"{args.workload}: whole factorisation x {passes}, {elapsed:.1f} s"}
+    line = {
+        "metric": METRIC, "value": round(value, 5), "unit": "GFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "operation": "ILU(0) factorisation in place",
+                   "n": n, "nnz": nnz, "flops_per_factorisation": flops,
+                   "flops": "one divide per lower entry, multiply + subtract per update",
+                   "algorithmic_bytes": alg,
+                   "l2_flush": "2x L2 buffer written before every timed step",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "latency (dependency chain of the levels)",
+                     "kernel": "ilu0 (whole call)", "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(achieved / peak, 5), "traffic": None,
+                     "algorithmic_bytes_per_launch": int(alg)},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 4 * args.steps, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse_args()
+    if args.workload in ILU0_WORKLOADS:
+        return run_ilu0_reference(args) if args.impl == "reference" else run_ilu0_ours(args)
     if args.workload in FW_WORKLOADS:
         return run_fw_reference(args) if args.impl == "reference" else run_fw_ours(args)
     if args.impl == "reference":

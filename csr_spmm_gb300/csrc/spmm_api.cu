@@ -11,6 +11,7 @@
 
 #include "csr_spmm.h"
 #include "spmm_internal.h"
+#include "spmm_ops.h"
 
 using namespace spmm;
 

@@ -17,6 +17,7 @@
 
 #include "spmm_device.cuh"
 #include "spmm_internal.h"
+#include "spmm_ops.h"
 
 namespace spmm {
 namespace {

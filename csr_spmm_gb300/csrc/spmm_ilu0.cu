@@ -30,6 +30,7 @@
 #include <algorithm>
 
 #include "spmm_internal.h"
+#include "spmm_ops.h"
 
 namespace spmm {
 namespace {

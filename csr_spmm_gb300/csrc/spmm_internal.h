@@ -162,62 +162,6 @@ cudaError_t launch_scale(T* C, int64_t ldc, int m, int n, T beta, int grid, cuda
 cudaError_t launch_csr_check(const int* row_ptr, const int* col_idx, int64_t m, int64_t k,
                              int64_t nnz, int* status, cudaStream_t st);
 
-// ---- Frank-Wolfe gradient scan (spmm_fw.cu) ----
-// G = K2B t1 - T2 (n x k), per-column minimum over rows (lowest row on ties),
-// gap = sum of B * G over B's stored entries.
-template <typename T>
-struct FwParams {
-    int n, k;
-    int ldk;                        // leading dimension of the dense t1 (multiple of FW_TILE)
-    const int* k2b_rp; const int* k2b_ci; const T* k2b_v;     // n x k CSR
-    const int* t1_rp;  const int* t1_ci;  const T* t1_v;      // k x k CSR
-    const int* t2_rp;  const int* t2_ci;  const T* t2_v;      // n x k CSR
-    const int* b_rp;   const int* b_ci;   const T* b_v;       // n x k CSR
-    T* t1d;                          // scratch: dense t1 [k, ldk], zero padded
-    T* part_val;                     // scratch: per-block minima [nblocks, ldk]
-    int* part_idx;                   // scratch: per-block argmins [nblocks, ldk]
-    double* part_gap;                // scratch: per-block gap sums [nblocks]
-    int nwarps;                      // the scan's grid, in warps
-    int nblocks;                     // the scan's grid, in blocks
-    T* out_val;                      // [k]
-    int* out_idx;                    // [k]
-    T* out_gap;                      // [1]
-};
-constexpr int FW_THREADS = 256;
-// columns per pass of a warp: 32 lanes x one 16-byte vector
-template <typename T> constexpr int fw_tile() { return 32 * (16 / (int)sizeof(T)); }
-template <typename T>
-cudaError_t launch_fw(const FwParams<T>& p, int grid, cudaStream_t st);
-template <typename T>
-int fw_blocks_per_sm();
-
-// ---- ILU(0), dataflow-scheduled (spmm_ilu0.cu) ----
-template <typename T>
-struct Ilu0Params {
-    int n;
-    int64_t nnz;
-    const int* rp;
-    const int* ci;
-    T* v;                  // A's values in, the L \ U factors out (in place)
-    int* depth;            // optional: each row's level
-    // scratch
-    int* pending;          // [n] lower entries of the row not yet final
-    int* cnt;              // [n] rows depending on the row (then a fill cursor)
-    int* dep_ptr;          // [n + 1] start of each row's dependents
-    int* dep_idx;          // [nnz] dependent rows, grouped by the row they depend on
-    int* queue;            // [n] rows in the order they became ready (-1: not yet)
-    int* head;             // next queue slot to take
-    int* tail;             // next queue slot to fill
-    int* abort;            // stop every warp (a failure was met)
-    int* finished;         // rows factored so far (termination and progress)
-    int* status;           // caller's: 0, or ILU0 failure bits
-};
-constexpr int ILU0_THREADS = 256;
-template <typename T>
-cudaError_t launch_ilu0(const Ilu0Params<T>& p, int grid, cudaStream_t st);
-template <typename T>
-int ilu0_blocks_per_sm();
-
 // Blocks per SM the rows kernel reaches for this geometry (occupancy query).
 template <typename T>
 int rows_blocks_per_sm(const Geometry& g);

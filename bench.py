@@ -56,6 +56,23 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(x, pg=None, device=None):
+    """The largest of every rank's x (the slowest replica sets the job's time);
+    x itself when not distributed."""
+    if pg is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(work_per_rank, steps, world, total_ms):
+    """Whole-job throughput in units/s: every rank's work over the job's time."""
+    return work_per_rank * steps * world / (total_ms / 1e3)
+
+
 def measured_hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -370,12 +387,9 @@ def run_ours(args):
     unprofiled_ms = statistics.mean(a.elapsed_time(b) for a, b in uev)
     step_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = sum(step_ms)
-    if pg:
-        tt = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, pg, dev)
     flops = problem_flops(p)
-    value = flops * args.steps * world / (total_ms / 1e3) / 1e9
+    value = job_rate(flops, args.steps, world, total_ms) / 1e9
 
     # ---- roofline of the dominant kernel (short/medium rows) ----
     peak, peak_kind = measured_hbm_peak()
@@ -426,10 +440,7 @@ def run_ours(args):
         e1.record(stream)
         torch.cuda.synchronize()
         e_ms = e0.elapsed_time(e1)
-        if pg:
-            tt = torch.tensor([e_ms], device=dev, dtype=torch.float64)
-            pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-            e_ms = float(tt.item())
+        e_ms = max_over_ranks(e_ms, pg, dev)
         e2e = {"value": round(flops * e_steps * world / (e_ms / 1e3) / 1e9, 3), "unit": "GFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": round(e_ms / e_steps, 4), "steps": e_steps}
@@ -581,12 +592,9 @@ def run_fw_ours(args):
         pg.barrier()
     clocks = sampler.stop()
     total_ms = sum(a.elapsed_time(b) for a, b in ev)
-    if pg:
-        tt = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, pg, dev)
     mean_ms = total_ms / args.steps
-    value = p.flops() * args.steps * world / (total_ms / 1e3) / 1e9
+    value = job_rate(p.flops(), args.steps, world, total_ms) / 1e9
     alg = p.algorithmic_bytes()
     peak, peak_kind = measured_hbm_peak()
     achieved = alg / (mean_ms / 1e3) / 1e9
@@ -620,7 +628,7 @@ def run_fw_ours(args):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        e_ms = e0.elapsed_time(e1)
+        e_ms = max_over_ranks(e0.elapsed_time(e1), pg, dev)
         e2e = {"value": round(p.flops() * e_steps * world / (e_ms / 1e3) / 1e9, 3),
                "unit": "GFLOP/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": round(e_ms / e_steps, 4), "steps": e_steps}
@@ -798,12 +806,9 @@ def run_ilu0_ours(args):
         pg.barrier()
     clocks = sampler.stop()
     total_ms = sum(a.elapsed_time(b) for a, b in ev)
-    if pg:
-        tt = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, pg, dev)
     mean_ms = total_ms / args.steps
-    value = flops * args.steps * world / (total_ms / 1e3) / 1e9
+    value = job_rate(flops, args.steps, world, total_ms) / 1e9
     # bytes: the structure read and the values read and written once
     alg = 4 * (n + 1) + 4 * nnz + 2 * 8 * nnz
     peak, peak_kind = measured_hbm_peak()
@@ -835,7 +840,7 @@ def run_ilu0_ours(args):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        e_ms = e0.elapsed_time(e1)
+        e_ms = max_over_ranks(e0.elapsed_time(e1), pg, dev)
         e2e = {"value": round(flops * e_steps * world / (e_ms / 1e3) / 1e9, 4),
                "unit": "GFLOP/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": round(e_ms / e_steps, 4), "steps": e_steps}

@@ -568,7 +568,7 @@ spmm_status_t spmm_fw_impl(spmm_handle_t h, int64_t n, int64_t k, const int32_t*
     }
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const int64_t ldk = std::max<int64_t>(TILE, (k + TILE - 1) / TILE * TILE);
-    const int grid = fw_blocks_per_sm<T>() * h->num_sms;
+    const int grid = fw_blocks_per_sm<T>((int)k) * h->num_sms;
     const int nwarps = grid * (FW_THREADS / 32);
     size_t off = 0;
     const size_t o_t1 = off;   off = align_up(off + sizeof(T) * (size_t)k * ldk, 256);

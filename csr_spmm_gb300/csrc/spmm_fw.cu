@@ -23,6 +23,10 @@ namespace spmm {
 namespace {
 
 constexpr int FW_NONE = 0x7fffffff;   // "no row yet" (loses every index tie)
+#ifndef SPMM_FW_SMEM
+#define SPMM_FW_SMEM 1
+#endif
+constexpr size_t FW_SMEM_MAX = 96 * 1024;
 
 template <typename T> __device__ __forceinline__ T largest();
 template <> __device__ __forceinline__ float largest<float>() { return FLT_MAX; }
@@ -72,7 +76,21 @@ __device__ __forceinline__ void scatter_row(T* buf, const int* __restrict__ ci,
 // lane's strict < keeps the lowest row of its share.  The row descriptors of
 // a block are loaded at once (lane r: row r), and the first chunk of the next
 // row's K2B entries is loaded before the current row's gathers.
-template <typename T>
+// 16-byte vector load from shared memory
+template <typename T, int W>
+__device__ __forceinline__ void lds_vec(const T* p, T (&v)[W]) {
+    if constexpr (sizeof(T) == 4) {
+        const float4 x = *reinterpret_cast<const float4*>(p);
+        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+    } else {
+        const double2 x = *reinterpret_cast<const double2*>(p);
+        v[0] = x.x; v[1] = x.y;
+    }
+}
+
+// SMEM: the column pass's slice of the dense t1 (k rows x TILE columns) is
+// copied into shared memory once per pass, and the gathers read it there.
+template <typename T, bool SMEM>
 __global__ void __launch_bounds__(FW_THREADS) fw_scan(FwParams<T> p) {
     constexpr int W = 16 / (int)sizeof(T);
     constexpr int TILE = fw_tile<T>();
@@ -85,10 +103,23 @@ __global__ void __launch_bounds__(FW_THREADS) fw_scan(FwParams<T> p) {
     __shared__ __align__(16) T s_row[WPB][2][TILE];      // the T2 and B entries of a row
     __shared__ T s_val[WPB][TILE];
     __shared__ int s_idx[WPB][TILE];
+    extern __shared__ __align__(16) unsigned char fw_dyn[];
+    T* s_t1 = reinterpret_cast<T*>(fw_dyn);              // [k][TILE] when SMEM
     T* g2 = s_row[wb][0];
     T* gb = s_row[wb][1];
     double gap = 0.0;
     for (int tb = 0; tb < p.k; tb += TILE) {
+        if constexpr (SMEM) {
+            const int vecs = p.k * (TILE / W);
+            for (int q = threadIdx.x; q < vecs; q += FW_THREADS) {
+                const int m = q / (TILE / W), c = (q % (TILE / W)) * W;
+                T v[W];
+                BLoad<T, W>::run(p.t1d + (int64_t)m * p.ldk + tb + c, v);
+#pragma unroll
+                for (int e = 0; e < W; ++e) s_t1[m * TILE + c + e] = v[e];
+            }
+            __syncthreads();
+        }
         const int cbase = tb + lane * W;        // the lane's first column (< ldk)
         T best_v[W];
         int best_i[W];
@@ -97,7 +128,8 @@ __global__ void __launch_bounds__(FW_THREADS) fw_scan(FwParams<T> p) {
             best_v[e] = largest<T>();
             best_i[e] = FW_NONE;
         }
-        const T* trow = p.t1d + cbase;
+        const T* trow = SMEM ? s_t1 + lane * W : p.t1d + cbase;
+        const int tstride = SMEM ? TILE : p.ldk;
         for (int r0 = gw * 32; r0 < p.n; r0 += nw * 32) {
             const int nr = min(32, p.n - r0);
             int a0 = 0, a1 = 0, c0 = 0, c1 = 0, b0 = 0, b1 = 0;
@@ -140,8 +172,9 @@ __global__ void __launch_bounds__(FW_THREADS) fw_scan(FwParams<T> p) {
                             const int m = __shfl_sync(FULL, mj, (t0 + u) & 31);
                             const T x = __shfl_sync(FULL, vj, (t0 + u) & 31);
                             av[u] = (t0 + u < cnt) ? x : T(0);
-                            BLoad<T, W>::run(trow + (int64_t)((t0 + u < cnt) ? m : 0) * p.ldk,
-                                             bv[u]);
+                            const T* src = trow + (int64_t)((t0 + u < cnt) ? m : 0) * tstride;
+                            if constexpr (SMEM) lds_vec<T, W>(src, bv[u]);
+                            else BLoad<T, W>::run(src, bv[u]);
                         }
 #pragma unroll
                         for (int u = 0; u < U; ++u)
@@ -269,6 +302,15 @@ __global__ void __launch_bounds__(256) fw_reduce(FwParams<T> p) {
     if (threadIdx.x == 0) *p.out_gap = (T)s[0];
 }
 
+// Shared-memory bytes for the t1 slice of one column pass; 0 when it is too
+// large to leave room for at least two blocks per SM (the gathers then read
+// the dense copy through L1).
+template <typename T>
+size_t fw_smem_bytes(int k) {
+    const size_t b = (size_t)k * fw_tile<T>() * sizeof(T);
+    return (SPMM_FW_SMEM && b <= FW_SMEM_MAX) ? b : 0;
+}
+
 }  // namespace
 
 template <typename T>
@@ -276,16 +318,34 @@ cudaError_t launch_fw(const FwParams<T>& p, int grid, cudaStream_t st) {
     cudaError_t e = cudaMemsetAsync(p.t1d, 0, sizeof(T) * (size_t)p.k * p.ldk, st);
     if (e != cudaSuccess) return e;
     if (p.k > 0) fw_densify<T><<<(p.k + 7) / 8, 256, 0, st>>>(p);
-    fw_scan<T><<<grid, FW_THREADS, 0, st>>>(p);
+    const size_t smem = fw_smem_bytes<T>(p.k);
+    if (smem > 0) {
+        e = cudaFuncSetAttribute(fw_scan<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+        fw_scan<T, true><<<grid, FW_THREADS, smem, st>>>(p);
+    } else {
+        fw_scan<T, false><<<grid, FW_THREADS, 0, st>>>(p);
+    }
     fw_reduce<T><<<(p.k + 7) / 8 + 1, 256, 0, st>>>(p);
     return cudaGetLastError();
 }
 
 template <typename T>
-int fw_blocks_per_sm() {
+int fw_blocks_per_sm(int k) {
     int b = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fw_scan<T>, FW_THREADS, 0) !=
-            cudaSuccess || b < 1) {
+    const size_t smem = fw_smem_bytes<T>(k);
+    cudaError_t e;
+    if (smem > 0) {
+        e = cudaFuncSetAttribute(fw_scan<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fw_scan<T, true>, FW_THREADS,
+                                                              smem);
+    } else {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fw_scan<T, false>, FW_THREADS, 0);
+    }
+    if (e != cudaSuccess || b < 1) {
         cudaGetLastError();
         b = 1;
     }
@@ -294,7 +354,7 @@ int fw_blocks_per_sm() {
 
 template cudaError_t launch_fw<float>(const FwParams<float>&, int, cudaStream_t);
 template cudaError_t launch_fw<double>(const FwParams<double>&, int, cudaStream_t);
-template int fw_blocks_per_sm<float>();
-template int fw_blocks_per_sm<double>();
+template int fw_blocks_per_sm<float>(int);
+template int fw_blocks_per_sm<double>(int);
 
 }  // namespace spmm

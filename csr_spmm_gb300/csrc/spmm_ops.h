@@ -35,7 +35,7 @@ template <typename T> constexpr int fw_tile() { return 32 * (16 / (int)sizeof(T)
 template <typename T>
 cudaError_t launch_fw(const FwParams<T>& p, int grid, cudaStream_t st);
 template <typename T>
-int fw_blocks_per_sm();
+int fw_blocks_per_sm(int k);
 
 // ---- ILU(0), dataflow-scheduled (spmm_ilu0.cu) ----
 template <typename T>

@@ -245,7 +245,7 @@ __device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
 // critical path) and queues the rest.  Waiting warps give up only when no
 // row has finished anywhere for ILU0_SPIN_LIMIT polls, or on the abort word.
 template <typename T>
-__global__ void __launch_bounds__(ILU0_THREADS) ilu0_factor(Ilu0Params<T> p) {
+__global__ void __launch_bounds__(ILU0_THREADS, 2) ilu0_factor(Ilu0Params<T> p) {
     const int lane = threadIdx.x & 31;
     int next = -1;                              // a row this warp made ready
     for (;;) {

@@ -71,9 +71,15 @@ namespace {
 constexpr double PANEL_FRACTION = SPMM_PANEL_FRACTION;
 constexpr double PANEL_TRIGGER = SPMM_PANEL_TRIGGER;
 // Rows at least this long go to the CTA-split kernel.
-constexpr int LONG_MIN_ROW = 1024;
+#ifndef SPMM_LONG_MIN_ROW
+#define SPMM_LONG_MIN_ROW 1024
+#endif
+constexpr int LONG_MIN_ROW = SPMM_LONG_MIN_ROW;
 // Long-row grid: CTAs per SM.
-constexpr int LONG_CTAS_PER_SM = 4;
+#ifndef SPMM_LONG_CTAS
+#define SPMM_LONG_CTAS 4
+#endif
+constexpr int LONG_CTAS_PER_SM = SPMM_LONG_CTAS;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

@@ -42,6 +42,7 @@ struct spmm_handle_s {
 // and reused by every product issued on the plan.
 struct spmm_plan_s {
     spmm_handle_s* h = nullptr;
+    int device = 0;                   // the handle's device (destroy needs no handle)
     int64_t m = 0, k = 0, n = 0;
     int es = 0;
     int long_grid = 0;
@@ -839,6 +840,7 @@ spmm_status_t spmm_plan_create(spmm_handle_t h, spmm_plan_t* out, const int32_t*
     spmm_plan_s* pl = new (std::nothrow) spmm_plan_s();
     if (!pl) return SPMM_ERR_ALLOC;
     pl->h = h;
+    pl->device = h->device;
     pl->m = m;
     pl->k = k;
     pl->n = n;
@@ -885,10 +887,10 @@ spmm_status_t spmm_plan_destroy(spmm_plan_t pl) {
     if (!pl) return SPMM_OK;
     int cur = -1;
     cudaGetDevice(&cur);
-    if (cur != pl->h->device) cudaSetDevice(pl->h->device);
+    if (cur != pl->device) cudaSetDevice(pl->device);
     cudaDeviceSynchronize();
     cudaFree(pl->scratch);
-    if (cur >= 0 && cur != pl->h->device) cudaSetDevice(cur);
+    if (cur >= 0 && cur != pl->device) cudaSetDevice(cur);
     cudaGetLastError();
     delete pl;
     return SPMM_OK;

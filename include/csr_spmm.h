@@ -268,7 +268,9 @@ typedef struct spmm_plan_s *spmm_plan_t;
 spmm_status_t spmm_plan_create(spmm_handle_t h, spmm_plan_t *plan, const int32_t *row_ptr,
                                int64_t m, int64_t k, int64_t n, int elem_size, void *stream);
 
-/* Release a plan (synchronises its device).  NULL is accepted and ignored. */
+/* Release a plan (synchronises its device).  NULL is accepted and ignored.
+ * Does not touch the handle, so it may run after spmm_destroy of the handle;
+ * products on a plan need the handle alive. */
 spmm_status_t spmm_plan_destroy(spmm_plan_t plan);
 
 /* C = alpha * A * B + beta * C with A's structure taken from the plan.

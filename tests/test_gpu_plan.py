@@ -167,3 +167,16 @@ def test_plan_wrapper_class(handle):
     torch.cuda.synchronize()
     plan.close()
     assert_parity(p, C.cpu().numpy(), what="Plan class")
+
+
+def test_plan_outlives_its_handle():
+    """Destroying a plan after its handle is allowed (the plan keeps no
+    reference the destruction needs)."""
+    import torch
+    h = cs.Handle(0)
+    p = uniform_rows(300, 200, 8, 5, seed=15, dtype=np.float32)
+    rp = torch.from_numpy(p.row_ptr).cuda()
+    plan = cs.spmm_plan_create(h.ptr, rp.data_ptr(), p.m, p.k, p.n, 4,
+                               torch.cuda.current_stream().cuda_stream)
+    h.close()
+    cs.spmm_plan_destroy(plan)

@@ -18,7 +18,8 @@ from ._lib import (EXPORTED, SPMM_ERR_ALLOC, SPMM_ERR_CUDA, SPMM_ERR_DIMENSION_M
                    SPMM_ERR_UNSUPPORTED_DEVICE, SPMM_OK, SpmmError, library, spmm_create,
                    spmm_csr_check, spmm_csr_f32, spmm_csr_f32_noalloc, spmm_csr_f64,
                    spmm_destroy, spmm_get_profile, spmm_plan_create, spmm_plan_csr_f32,
-                   spmm_plan_csr_f64, spmm_plan_destroy, spmm_set_l2_persistence,
+                   spmm_plan_csr_f64, spmm_plan_destroy, spmm_plan_order_rows,
+                   spmm_row_order_bfs, spmm_set_l2_persistence,
                    spmm_csr_squared_f32, spmm_csr_squared_f64, spmm_fw_argmin,
                    spmm_ilu0, ILU0_SINGULAR, ILU0_WAIT_TIMEOUT,
                    spmm_reserve, spmm_set_profiling, status_string)
@@ -29,7 +30,8 @@ __all__ = ["Handle", "spmm", "csr_check", "SpmmError", "library", "spmm_create",
            "spmm_plan_destroy", "spmm_set_l2_persistence", "spmm_plan_csr_f32",
            "spmm_csr_squared_f32", "spmm_csr_squared_f64", "spmm_squared",
            "spmm_fw_argmin", "fw_argmin", "spmm_ilu0", "ilu0", "Ilu0Error",
-           "spmm_plan_csr_f64", "Plan", "EXPORTED"]
+           "spmm_plan_csr_f64", "spmm_plan_order_rows", "spmm_row_order_bfs", "Plan",
+           "EXPORTED"]
 
 
 class Handle:
@@ -193,6 +195,12 @@ class Plan:
         es = 4 if dtype == torch.float32 else 8
         st = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
         self.ptr = spmm_plan_create(handle.ptr, _ptr(row_ptr), self.m, self.k, self.n, es, st)
+
+    def order_rows(self, row_ptr, col_idx, stream=None) -> None:
+        """Process rows in breadth-first order of A's pattern (spmm_plan_order_rows)."""
+        import torch
+        st = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+        spmm_plan_order_rows(self.ptr, _ptr(row_ptr), _ptr(col_idx), st)
 
     def __call__(self, alpha, row_ptr, col_idx, values, B, beta, C, stream=None) -> None:
         """C <- alpha * A * B + beta * C with A's structure from the plan."""

@@ -30,7 +30,7 @@ EXPORTED = ("spmm_create", "spmm_destroy", "spmm_reserve", "spmm_csr_f32", "spmm
             "spmm_set_l2_persistence", "spmm_csr_squared_f32", "spmm_csr_squared_f64",
             "spmm_fw_argmin_f32", "spmm_fw_argmin_f64", "spmm_ilu0_f32", "spmm_ilu0_f64",
             "spmm_plan_create", "spmm_plan_destroy", "spmm_plan_csr_f32", "spmm_plan_csr_f64",
-            "spmm_status_string")
+            "spmm_plan_order_rows", "spmm_row_order_bfs", "spmm_status_string")
 
 
 class SpmmProfile(ctypes.Structure):
@@ -116,6 +116,10 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.spmm_plan_csr_f64.argtypes = [vp, ctypes.c_double, vp, vp, vp, vp, i64, ctypes.c_double,
                                       vp, i64, vp]
     lib.spmm_plan_csr_f64.restype = st
+    lib.spmm_plan_order_rows.argtypes = [vp, vp, vp, vp]
+    lib.spmm_plan_order_rows.restype = st
+    lib.spmm_row_order_bfs.argtypes = [vp, vp, i64, vp]
+    lib.spmm_row_order_bfs.restype = st
     lib.spmm_status_string.argtypes = [ctypes.c_int]
     lib.spmm_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -190,6 +194,26 @@ def spmm_csr_f32_noalloc(alpha, row_ptr, col_idx, values, m, k, B, ldb, n, beta,
     if check:
         _check(s, "spmm_csr_f32_noalloc")
     return s
+
+
+def spmm_plan_order_rows(plan, row_ptr, col_idx, stream=0) -> None:
+    """Process the plan's rows in breadth-first order of A's pattern (device arrays)."""
+    _check(library().spmm_plan_order_rows(plan, row_ptr, col_idx, stream or None),
+           "spmm_plan_order_rows")
+
+
+def spmm_row_order_bfs(row_ptr, col_idx):
+    """Breadth-first row order of a CSR pattern given as host (numpy) arrays;
+    returns an int32 numpy permutation of the m rows."""
+    import numpy as np
+    rp = np.ascontiguousarray(row_ptr, dtype=np.int32)
+    ci = np.ascontiguousarray(col_idx, dtype=np.int32)
+    m = rp.size - 1
+    order = np.empty(max(m, 0), dtype=np.int32)
+    _check(library().spmm_row_order_bfs(rp.ctypes.data, ci.ctypes.data if ci.size else None, m,
+                                        order.ctypes.data if m > 0 else None),
+           "spmm_row_order_bfs")
+    return order
 
 
 def spmm_plan_create(handle, row_ptr, m, k, n, elem_size, stream=0) -> int:

@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cstring>
 #include <new>
+#include <vector>
 
 #include "csr_spmm.h"
 #include "spmm_internal.h"
@@ -172,12 +173,23 @@ Plan make_plan_es(const spmm_handle_s* h, int64_t k, int64_t n, int es, bool vec
         P.geo.G = 32;
         P.geo.R = nvec <= 64 ? 2 : 4;
     }
-    // bin thresholds
+    P.geo.whole = (n % W) == 0;
+    // Bin thresholds: those of the 16-byte geometry whatever the operands'
+    // alignment, so that the bins, and with them the summation order of every
+    // row, depend only on the row lengths, n and the element size.  A plan
+    // (binned once, for 16-byte operands) then gives the direct call's
+    // results bit for bit for any alignment; any threshold is correct for
+    // every geometry.
+    if (!vec) {
+        const Plan V = make_plan_es(h, k, n, es, true);
+        P.short_max = V.short_max;
+        P.long_min = V.long_min;
+        return P;
+    }
     const int bytes_per_entry = P.geo.R * W * es;
     const int batch_bytes = es == 8 ? SPMM_BATCH_BYTES_F64 : SPMM_BATCH_BYTES;
     const int U = std::min(SPMM_BATCH_MAX, std::max(1, batch_bytes / bytes_per_entry));
     const int CH = std::max(P.geo.G, U);
-    P.geo.whole = (n % W) == 0;
     P.long_min = LONG_MIN_ROW;
     P.short_max = (P.geo.G == 32) ? P.long_min - 1 : std::min(P.long_min - 1, 2 * CH);
     return P;
@@ -893,6 +905,62 @@ spmm_status_t spmm_plan_destroy(spmm_plan_t pl) {
     if (cur >= 0 && cur != pl->device) cudaSetDevice(cur);
     cudaGetLastError();
     delete pl;
+    return SPMM_OK;
+}
+
+spmm_status_t spmm_plan_order_rows(spmm_plan_t pl, const int32_t* row_ptr,
+                                   const int32_t* col_idx, void* stream) {
+    if (!pl) return SPMM_ERR_INVALID_ARGUMENT;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != pl->device) {
+        cudaGetLastError();
+        return SPMM_ERR_INVALID_ARGUMENT;
+    }
+    const int n_short = pl->hdr_host[HDR_COUNT_SHORT];
+    const int n_med = pl->hdr_host[HDR_COUNT_MEDIUM];
+    const int64_t m = pl->m;
+    if (m == 0 || n_short + n_med == 0) return SPMM_OK;    // no rows binned: nothing to order
+    if (!row_ptr) return SPMM_ERR_NULL_POINTER;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    auto fail = [] {
+        cudaGetLastError();
+        return SPMM_ERR_CUDA;
+    };
+    std::vector<int32_t> rp((size_t)m + 1);
+    if (cudaMemcpyAsync(rp.data(), row_ptr, rp.size() * sizeof(int32_t), cudaMemcpyDeviceToHost,
+                        st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return fail();
+    if (!csr_rows_valid(rp.data(), m)) return SPMM_ERR_INVALID_CSR;
+    const int64_t nnz = rp[m];
+    if (nnz > 0 && !col_idx) return SPMM_ERR_NULL_POINTER;
+    std::vector<int32_t> ci((size_t)nnz);
+    std::vector<int32_t> list((size_t)n_short + n_med);
+    if ((nnz > 0 && cudaMemcpyAsync(ci.data(), col_idx, ci.size() * sizeof(int32_t),
+                                    cudaMemcpyDeviceToHost, st) != cudaSuccess) ||
+        cudaMemcpyAsync(list.data(), pl->rowlist, list.size() * sizeof(int32_t),
+                        cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return fail();
+    std::vector<int32_t> order((size_t)m), rank((size_t)m);
+    row_order_bfs(rp.data(), ci.data(), (int)m, order.data());
+    for (int64_t i = 0; i < m; ++i) rank[order[i]] = (int32_t)i;
+    auto by_rank = [&](int32_t a, int32_t b) { return rank[a] < rank[b]; };
+    std::sort(list.begin(), list.begin() + n_short, by_rank);
+    std::sort(list.begin() + n_short, list.end(), by_rank);
+    // prefix of medium-row lengths in the new list order (it balances medium
+    // rows across warps by entries)
+    std::vector<int32_t> med((size_t)n_med + 1, 0);
+    for (int i = 0; i < n_med; ++i) {
+        const int32_t r = list[(size_t)n_short + i];
+        med[i + 1] = med[i] + (rp[r + 1] - rp[r]);
+    }
+    if (cudaMemcpyAsync(pl->rowlist, list.data(), list.size() * sizeof(int32_t),
+                        cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        (n_med > 0 && cudaMemcpyAsync(pl->med_pre, med.data(), med.size() * sizeof(int32_t),
+                                      cudaMemcpyHostToDevice, st) != cudaSuccess) ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return fail();
     return SPMM_OK;
 }
 

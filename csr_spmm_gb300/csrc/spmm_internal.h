@@ -44,19 +44,34 @@ constexpr int LONG_MIN_SEGMENT = 2048;   // smallest per-CTA share of long-row e
 #define SPMM_PDL 1
 #endif
 
-// Rows kernel block size and minimum resident blocks per SM (a register cap).
-constexpr int ROWS_THREADS = 256;
+// Rows kernel block size and minimum resident blocks per SM (a register cap),
+// per geometry.  One block (or two) holds all the SM's resident warps, so the
+// warps that interleave over a block's contiguous range of rows are all the
+// warps of the SM: rows next to each other in the list, which often gather
+// the same B rows, share one L1.  Measured on GB300 against 256-thread blocks
+// at the same occupancy: wide-N -3%, Laplacian -2.5%, a SEACells matrix in
+// breadth-first row order -5%, the rest unchanged.
+#ifndef SPMM_ROWS_THREADS
+#define SPMM_ROWS_THREADS 1024
+#endif
 #ifndef SPMM_ROWS_MIN_BLOCKS
-#define SPMM_ROWS_MIN_BLOCKS 4
+#define SPMM_ROWS_MIN_BLOCKS 1
+#endif
+#ifndef SPMM_ROWS_THREADS_F64
+#define SPMM_ROWS_THREADS_F64 768
 #endif
 #ifndef SPMM_ROWS_MIN_BLOCKS_F64
-#define SPMM_ROWS_MIN_BLOCKS_F64 6
+#define SPMM_ROWS_MIN_BLOCKS_F64 2
 #endif
 // binary32 rows kernels with 16-byte vectors and lane groups narrower than a
 // warp (n <= 64 columns per panel): twice the gathers in flight per lane, at
-// one resident block fewer (measured faster on power-law and wide-N inputs)
+// a quarter fewer resident warps (measured faster on power-law and wide-N
+// inputs)
+#ifndef SPMM_ROWS_THREADS_NARROW
+#define SPMM_ROWS_THREADS_NARROW 768
+#endif
 #ifndef SPMM_ROWS_MIN_BLOCKS_NARROW
-#define SPMM_ROWS_MIN_BLOCKS_NARROW 3
+#define SPMM_ROWS_MIN_BLOCKS_NARROW 1
 #endif
 // B bytes each lane keeps in flight per gather batch, and the batch cap.
 #ifndef SPMM_BATCH_BYTES
@@ -165,6 +180,11 @@ cudaError_t launch_csr_check(const int* row_ptr, const int* col_idx, int64_t m, 
 // Blocks per SM the rows kernel reaches for this geometry (occupancy query).
 template <typename T>
 int rows_blocks_per_sm(const Geometry& g);
+
+// Host: row_ptr[0] == 0 and non-decreasing (m + 1 entries).
+bool csr_rows_valid(const int32_t* row_ptr, int64_t m);
+// Host: breadth-first order of the rows of A's pattern (spmm_order.cu).
+void row_order_bfs(const int32_t* row_ptr, const int32_t* col_idx, int m, int32_t* order);
 
 }  // namespace spmm
 

@@ -354,29 +354,33 @@ __device__ __forceinline__ int medium_lower_bound(const int* __restrict__ med_pr
 
 template <typename T, int W, int G>
 struct RowsOccupancy {
+    static constexpr int THREADS = sizeof(T) == 8 ? SPMM_ROWS_THREADS_F64
+                                   : narrow_f32<T, W, G>() ? SPMM_ROWS_THREADS_NARROW
+                                                           : SPMM_ROWS_THREADS;
     static constexpr int MIN_BLOCKS = sizeof(T) == 8 ? SPMM_ROWS_MIN_BLOCKS_F64
                                       : narrow_f32<T, W, G>() ? SPMM_ROWS_MIN_BLOCKS_NARROW
                                                               : SPMM_ROWS_MIN_BLOCKS;
+    static_assert(THREADS % 32 == 0 && THREADS <= 1024, "rows kernel block size");
 };
 
 // READ_C: beta != 0 (C is read, and prefetched at each row start).
 // WHOLE: n is a multiple of W (no partial vectors; see gather_b).
 template <typename T, int W, int G, int R, bool READ_C, bool WHOLE>
-__global__ void __launch_bounds__(ROWS_THREADS, RowsOccupancy<T, W, G>::MIN_BLOCKS)
+__global__ void __launch_bounds__(RowsOccupancy<T, W, G>::THREADS, RowsOccupancy<T, W, G>::MIN_BLOCKS)
 rows_kernel(SpmmParams<T> p) {
+    constexpr int WPB = RowsOccupancy<T, W, G>::THREADS / 32;    // warps per block
     wait_for_predecessor();
     allow_successor();
     const uint64_t pol_s = policy_evict_first();
     const int n_short = p.hdr[HDR_COUNT_SHORT];
     const int n_med = p.hdr[HDR_COUNT_MEDIUM];
     const int64_t med_nnz = p.hdr[HDR_MED_NNZ];
-    const int64_t nwarps = (int64_t)gridDim.x * (ROWS_THREADS / 32);
-    const int64_t w = (int64_t)blockIdx.x * (ROWS_THREADS / 32) + (threadIdx.x >> 5);
+    const int64_t nwarps = (int64_t)gridDim.x * WPB;
+    const int64_t w = (int64_t)blockIdx.x * WPB + (threadIdx.x >> 5);
     // short rows: equal counts per warp; medium rows: equal entries per warp
     // short rows: each CTA takes an equal contiguous range of the short list and
-    // its warps interleave over it (warp j: rows j, j + 8, ...), so rows that
+    // its warps interleave over it (warp j: rows j, j + WPB, ...), so rows that
     // sit next to each other in the list run at the same time on the same SM
-    constexpr int WPB = ROWS_THREADS / 32;
     const int64_t nblk = gridDim.x;
     const int cs0 = (int)((int64_t)blockIdx.x * n_short / nblk);
     const int cs1 = (int)((int64_t)(blockIdx.x + 1) * n_short / nblk);

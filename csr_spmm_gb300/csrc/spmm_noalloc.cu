@@ -133,34 +133,45 @@ extern "C" spmm_status_t spmm_csr_f32_noalloc(float alpha, const int32_t* row_pt
     // plan: vector width, one column panel (n <= 512 keeps k x n panels of
     // small problems whole), lane groups, bin thresholds -- the same rules the
     // handle path applies
-    Geometry geo{};
-    geo.W = (aligned16(B) && aligned16(C) && ldb % 4 == 0 && ldc % 4 == 0) ? 4 : 1;
-    int64_t panel = n;
-    const double bbytes = (double)k * (double)n * sizeof(float);
-    if (ds->l2_bytes > 0 && bbytes > 3.0 * (double)ds->l2_bytes) {
-        const int64_t align = std::max<int64_t>(geo.W, 32);
-        int64_t cols = (int64_t)(0.5 * (double)ds->l2_bytes / ((double)k * sizeof(float)));
-        cols = cols / align * align;
-        if (cols < align) cols = align;
-        const int64_t np = (n + cols - 1) / cols;
-        panel = (n + np - 1) / np;
-        panel = (panel + geo.W - 1) / geo.W * geo.W;
-    }
-    const int panel_cols = (int)std::min<int64_t>(panel, n);
+    struct Shape { Geometry geo; int panel_cols; };
+    auto shape_for = [&](int W) {
+        Shape sh{};
+        sh.geo.W = W;
+        int64_t panel = n;
+        const double bbytes = (double)k * (double)n * sizeof(float);
+        if (ds->l2_bytes > 0 && bbytes > 3.0 * (double)ds->l2_bytes) {
+            const int64_t align = std::max<int64_t>(W, 32);
+            int64_t cols = (int64_t)(0.5 * (double)ds->l2_bytes / ((double)k * sizeof(float)));
+            cols = cols / align * align;
+            if (cols < align) cols = align;
+            const int64_t np = (n + cols - 1) / cols;
+            panel = (n + np - 1) / np;
+            panel = (panel + W - 1) / W * W;
+        }
+        sh.panel_cols = (int)std::min<int64_t>(panel, n);
+        const int nvec = (sh.panel_cols + W - 1) / W;
+        if (nvec <= 32) {
+            sh.geo.G = next_pow2(nvec);
+            sh.geo.R = 1;
+        } else {
+            sh.geo.G = 32;
+            sh.geo.R = nvec <= 64 ? 2 : 4;
+        }
+        return sh;
+    };
+    const bool vec = aligned16(B) && aligned16(C) && ldb % 4 == 0 && ldc % 4 == 0;
+    const Shape sh = shape_for(vec ? 4 : 1);
+    const Geometry geo = sh.geo;
+    const int panel_cols = sh.panel_cols;
     const int npanels = (int)((n + panel_cols - 1) / panel_cols);
-    const int nvec = (panel_cols + geo.W - 1) / geo.W;
-    if (nvec <= 32) {
-        geo.G = next_pow2(nvec);
-        geo.R = 1;
-    } else {
-        geo.G = 32;
-        geo.R = nvec <= 64 ? 2 : 4;
-    }
-    const int bytes_per_entry = geo.R * geo.W * (int)sizeof(float);
+    // bin thresholds from the 16-byte geometry whatever the alignment (the
+    // bins then depend only on row lengths and n, as on the handle path)
+    const Geometry g16 = vec ? geo : shape_for(4).geo;
+    const int bytes_per_entry = g16.R * g16.W * (int)sizeof(float);
     const int U = std::min(SPMM_BATCH_MAX, std::max(1, SPMM_BATCH_BYTES / bytes_per_entry));
-    const int CH = std::max(geo.G, U);
+    const int CH = std::max(g16.G, U);
     const int long_min = 1024;
-    const int short_max = geo.G == 32 ? long_min - 1 : std::min(long_min - 1, 2 * CH);
+    const int short_max = g16.G == 32 ? long_min - 1 : std::min(long_min - 1, 2 * CH);
     const int long_grid = std::min(4 * ds->num_sms, NOALLOC_LONG_GRID_MAX);
 
     BinScratch bs{};

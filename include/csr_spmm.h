@@ -273,6 +273,36 @@ spmm_status_t spmm_plan_create(spmm_handle_t h, spmm_plan_t *plan, const int32_t
  * products on a plan need the handle alive. */
 spmm_status_t spmm_plan_destroy(spmm_plan_t plan);
 
+/* Change the order in which the plan's products process the rows of A (not
+ * where results go): the short- and medium-row lists are re-sorted into the
+ * breadth-first order of A's pattern (spmm_row_order_bfs), so that rows which
+ * gather the same B rows run next to each other and share the SM's L1.  Worth
+ * it for matrices whose pattern has locality that the row numbering hides, as
+ * in the kNN kernel matrix that the SEACells Frank-Wolfe kernels of the
+ * bixverse page apply every iteration; of no use for uniformly random
+ * columns.  Long rows keep their order.  Results stay bitwise the same as
+ * without the call: each row's sum does not depend on when it is computed.
+ * row_ptr and col_idx are device arrays holding the structure the plan
+ * analysed (row_ptr with the same values).  Copies both to the host and runs
+ * the traversal there (O(m + nnz)), then writes the lists back; synchronises
+ * `stream`.  SPMM_ERR_INVALID_CSR if row_ptr does not start at 0 or
+ * decreases.  The pages have no row reordering; this extends the plan's
+ * analysis reuse. */
+spmm_status_t spmm_plan_order_rows(spmm_plan_t plan, const int32_t *row_ptr,
+                                   const int32_t *col_idx, void *stream);
+
+/* Host function (no GPU involved): order[i] = the i-th row of an m-row CSR
+ * pattern (HOST arrays row_ptr[m + 1], col_idx[row_ptr[m]]) in breadth-first
+ * order.  Row i is adjacent to row j for each stored entry (i, j) with
+ * 0 <= j < m; other columns are skipped.  The traversal starts at row 0,
+ * visits each row's neighbours in stored order, and restarts at the lowest
+ * unvisited row when a component is exhausted, so `order` (caller-owned, m
+ * entries) is a permutation of 0..m-1.  SPMM_ERR_INVALID_CSR if row_ptr[0] != 0
+ * or row_ptr decreases; SPMM_ERR_NULL_POINTER for a missing array (col_idx
+ * may be NULL when the pattern is empty). */
+spmm_status_t spmm_row_order_bfs(const int32_t *row_ptr, const int32_t *col_idx, int64_t m,
+                                 int32_t *order);
+
 /* C = alpha * A * B + beta * C with A's structure taken from the plan.
  * row_ptr must hold the structure the plan analysed (same values); col_idx,
  * values, B and C may change from call to call.  Same argument rules as

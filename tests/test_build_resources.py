@@ -44,11 +44,11 @@ def _find(res, *parts):
     return hits
 
 
-def test_headline_rows_kernel_fits_four_blocks_per_sm():
+def test_headline_rows_kernel_fits_full_occupancy():
     # rows_kernel<float, 4, 32, 1, false, true>: the SEACells-shaped product
     res = _resources("spmm_rows_f32.cu")
     (name, (regs, spill)), = _find(res, "rows_kernel", "IfLi4ELi32ELi1ELb0ELb1E")
-    assert regs <= 64, (name, regs)                 # 4 blocks of 256 threads per SM
+    assert regs <= 64, (name, regs)                 # one 1024-thread block per SM
     assert spill[0] <= 64 and spill[1] <= 64, (name, spill)
 
 

@@ -180,3 +180,89 @@ def test_plan_outlives_its_handle():
                                torch.cuda.current_stream().cuda_stream)
     h.close()
     cs.spmm_plan_destroy(plan)
+
+
+def _order_plan_rows(plan, p):
+    import torch
+    rp = torch.from_numpy(p.row_ptr).cuda()
+    ci = (torch.from_numpy(p.col_idx).cuda() if p.col_idx.size
+          else torch.zeros(1, dtype=torch.int32, device="cuda"))
+    cs.spmm_plan_order_rows(plan, rp.data_ptr(), ci.data_ptr(),
+                            torch.cuda.current_stream().cuda_stream)
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_plan_row_order_keeps_results(handle, name):
+    """Processing the rows in breadth-first order changes when each row is
+    computed, not how: the products stay bit for bit those of the direct call,
+    including short, medium and long rows, and across new values."""
+    p = CASES[name]()
+    plan = _make_plan(handle, p)
+    try:
+        _order_plan_rows(plan, p)
+        rows = np.unique(np.linspace(0, p.m - 1, 300).astype(np.int64))
+        for it in range(2):
+            if it:
+                p = _revalue(p, 200 + it)
+            direct, _ = run_problem(handle, p)
+            got = _plan_run(handle, plan, p)
+            assert np.array_equal(_bits(got[:, :p.n]), _bits(direct[:, :p.n])), (name, it)
+            assert_parity(p, got, rows=rows, what=f"ordered plan {name} #{it}")
+    finally:
+        cs.spmm_plan_destroy(plan)
+
+
+def test_plan_row_order_medium_rows_and_unaligned(handle):
+    """Medium rows (their entry prefix is rebuilt after the reorder) on a
+    narrow geometry, and unaligned B through an ordered plan."""
+    p = power_law(20_000, 20_000, 8, 400_000, 900, seed=21)
+    plan = _make_plan(handle, p)
+    try:
+        _order_plan_rows(plan, p)
+        for off in (0, 1):
+            direct, _ = run_problem(handle, p, b_offset=off)
+            got = _plan_run(handle, plan, p, b_offset=off)
+            assert np.array_equal(_bits(got[:, :p.n]), _bits(direct[:, :p.n])), off
+    finally:
+        cs.spmm_plan_destroy(plan)
+
+
+def test_plan_row_order_errors(handle):
+    import torch
+    p = uniform_rows(100, 100, 8, 3, seed=22, dtype=np.float32)
+    plan = _make_plan(handle, p)
+    try:
+        bad = p.row_ptr.copy()
+        bad[0] = 1
+        rp = torch.from_numpy(bad).cuda()
+        ci = torch.from_numpy(p.col_idx).cuda()
+        st = torch.cuda.current_stream().cuda_stream
+        assert cs.library().spmm_plan_order_rows(plan, rp.data_ptr(), ci.data_ptr(),
+                                                 st) == cs.SPMM_ERR_INVALID_CSR
+        assert cs.library().spmm_plan_order_rows(plan, None, ci.data_ptr(),
+                                                 st) == cs.SPMM_ERR_NULL_POINTER
+        assert cs.library().spmm_plan_order_rows(None, rp.data_ptr(), ci.data_ptr(),
+                                                 st) == cs.SPMM_ERR_INVALID_ARGUMENT
+        # the plan is untouched by the rejected calls
+        direct, _ = run_problem(handle, p)
+        got = _plan_run(handle, plan, p)
+        assert np.array_equal(_bits(got[:, :p.n]), _bits(direct[:, :p.n]))
+    finally:
+        cs.spmm_plan_destroy(plan)
+
+
+def test_plan_class_order_rows(handle):
+    import torch
+    p = knn_kernel_graph(3000, 15, 40, 20, seed=23)
+    dev = torch.device("cuda")
+    rp = torch.from_numpy(p.row_ptr).to(dev)
+    ci = torch.from_numpy(p.col_idx).to(dev)
+    va = torch.from_numpy(p.values).to(dev)
+    B = torch.from_numpy(p.B).to(dev)
+    C = torch.empty(p.m, p.n, dtype=torch.float32, device=dev)
+    plan = cs.Plan(handle, rp, p.k, p.n, torch.float32)
+    plan.order_rows(rp, ci)
+    plan(p.alpha, rp, ci, va, B, p.beta, C)
+    torch.cuda.synchronize()
+    plan.close()
+    assert_parity(p, C.cpu().numpy(), what="Plan class, ordered rows")

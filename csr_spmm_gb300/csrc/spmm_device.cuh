@@ -88,11 +88,19 @@ __device__ __forceinline__ void load_b_partial(const T* p, int cnt, T (&v)[W]) {
 }
 
 // ---------------------------------------------------------------------------
-// C epilogue: C = alpha * acc (beta == 0, C not read) or alpha * acc + beta * C
+// C epilogue: C = alpha * acc (beta == 0, C not read) or alpha * acc + beta * C,
+// evaluated as fma(alpha, acc, beta * C).  BS = +1 / -1 marks a kernel built
+// for beta == +1 / -1: beta * C is then +C / -C exactly, so the multiply is
+// left out and the result is bit for bit that of the general form.  (On GB300
+// binary64 arithmetic is scarce, and the multiply is a quarter of the FP64
+// work of a 5-point-stencil product.)
 // ---------------------------------------------------------------------------
-template <typename T>
+template <typename T, int BS = 0>
 __device__ __forceinline__ T epi(T alpha, T acc, T beta, T c_old) {
-    return alpha * acc + beta * c_old;
+    static_assert(BS == 0 || BS == 1 || BS == -1, "beta sign: 0 (any beta), +1 or -1");
+    if constexpr (BS == 1) return fma(alpha, acc, c_old);
+    else if constexpr (BS == -1) return fma(alpha, acc, -c_old);
+    else return fma(alpha, acc, beta * c_old);
 }
 
 // Output store: streaming (.cs) by default; `keep` stores with the default
@@ -171,13 +179,13 @@ __device__ __forceinline__ void load_c(const T* c, int cnt, T (&v)[W]) {
     }
 }
 
-// C = alpha * acc + beta * c0 with c0 already loaded.
-template <typename T, int W>
+// C = alpha * acc + beta * c0 with c0 already loaded (BS: see epi).
+template <typename T, int W, int BS = 0>
 __device__ __forceinline__ void store_c_pre(T* c, int cnt, const T (&acc)[W], const T (&c0)[W],
                                             T alpha, T beta) {
     T o[W];
 #pragma unroll
-    for (int e = 0; e < W; ++e) o[e] = epi<T>(alpha, acc[e], beta, c0[e]);
+    for (int e = 0; e < W; ++e) o[e] = epi<T, BS>(alpha, acc[e], beta, c0[e]);
     if (cnt == W && (W * sizeof(T)) % 16 == 0) {
         constexpr int PER = 16 / sizeof(T);
 #pragma unroll

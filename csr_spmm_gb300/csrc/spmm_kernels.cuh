@@ -116,17 +116,70 @@ __device__ __forceinline__ void gather_b(const T* p, int cnt, T (&v)[W]) {
     else load_b_partial<T, W>(p, cnt, v);
 }
 
+// Broadcast of a step's (col_idx, value) pairs to every lane of the group.
+// With warp shuffles a binary64 pair costs three shuffles (the index and the
+// value's two halves), each one L1 data-pipe wavefront per group.  In the
+// binary64 rows kernel (groups of 8 or more lanes) each step's pairs are
+// instead staged in a per-group shared-memory slot, and every lane reads a
+// pair with one 16-byte broadcast load.  Measured on GB300: Laplacian 0.216 ->
+// 0.207 ms per call.  For binary32 the same staging (two pairs per 16-byte
+// load) was slower (SEACells +5%, power-law +5%, wide-N +38%; more spills),
+// so binary32 and the long-row kernel keep the shuffles.
+template <typename T, int W, int G, int R, bool ROWS>
+struct Bcast {
+    static constexpr bool SMEM = ROWS && sizeof(T) == 8 && G >= 8;
+    static constexpr int PAIR_BYTES = 16;             // {col_idx, pad, value}
+    // per-group slot; the 16-byte pad staggers the groups' banks
+    static constexpr int GROUP_BYTES = Cfg<T, W, G, R, ROWS>::CH * PAIR_BYTES + 16;
+    static constexpr int WARP_BYTES = SMEM ? Cfg<T, W, G, R, ROWS>::RPW * GROUP_BYTES : 0;
+};
+
+// Store this lane's pairs of the step (entries g + G*q) in the group's slot.
+template <int G, int Q>
+__device__ __forceinline__ void stage_entries(unsigned char* slot, const int (&col)[Q],
+                                              const double (&val)[Q]) {
+    const int g = (threadIdx.x & 31) & (G - 1);
+#pragma unroll
+    for (int q = 0; q < Q; ++q)
+        *reinterpret_cast<double2*>(slot + (g + G * q) * 16) =
+            make_double2(__hiloint2double(0, col[q]), val[q]);
+}
+
+// Pair j of the step, for every lane of the group.
+template <typename T, int W, int G, int R, bool ROWS>
+__device__ __forceinline__ void fetch_pair(int& cj, T& av, int j,
+                                           const int (&col)[Cfg<T, W, G, R, ROWS>::Q],
+                                           const T (&val)[Cfg<T, W, G, R, ROWS>::Q],
+                                           const unsigned char* slot) {
+    if constexpr (Bcast<T, W, G, R, ROWS>::SMEM) {
+        const double2 e = *reinterpret_cast<const double2*>(slot + j * 16);
+        cj = __double2loint(e.x);
+        av = e.y;
+    } else {
+        cj = __shfl_sync(FULL, col[j / G], j % G, G);   // j is compile-time after unrolling
+        av = __shfl_sync(FULL, val[j / G], j % G, G);
+    }
+}
+
 // One step: the group consumes its `cnt` (<= CH) entries held in (col, val),
 // in batches of U.  cmax / cmin are warp-uniform bounds on every group's cnt:
 // batches below cmin are whole for every group and gather without checks.
-// Entries past a row's end were loaded with value 0 (load_entries).
+// Entries past a row's end were loaded with value 0 (load_entries).  `slot`
+// is the group's shared-memory slot when Bcast::SMEM (every lane of the warp
+// must call this together), unused otherwise.
 template <typename T, int W, int G, int R, bool ROWS = false, bool WHOLE = false>
 __device__ __forceinline__ void consume_step(T (&acc)[R][W],
                                              const int (&col)[Cfg<T, W, G, R, ROWS>::Q],
                                              const T (&val)[Cfg<T, W, G, R, ROWS>::Q], int cnt,
                                              int cmax, int cmin, int ldb,
-                                             const LaneVecs<T, W, R>& lv) {
+                                             const LaneVecs<T, W, R>& lv,
+                                             unsigned char* slot = nullptr) {
     using C = Cfg<T, W, G, R, ROWS>;
+    if constexpr (Bcast<T, W, G, R, ROWS>::SMEM) {
+        __syncwarp();                                   // the previous step's reads are done
+        stage_entries<G, C::Q>(slot, col, val);
+        __syncwarp();
+    }
 #pragma unroll
     for (int j0 = 0; j0 < C::CH; j0 += C::U) {
         if (j0 >= cmax) break;                          // warp-uniform
@@ -135,9 +188,8 @@ __device__ __forceinline__ void consume_step(T (&acc)[R][W],
         if (j0 + C::U <= cmin) {                        // warp-uniform: whole batch
 #pragma unroll
             for (int u = 0; u < C::U; ++u) {
-                const int j = j0 + u;                   // compile-time after unrolling
-                const int cj = __shfl_sync(FULL, col[j / G], j % G, G);
-                av[u] = __shfl_sync(FULL, val[j / G], j % G, G);
+                int cj;
+                fetch_pair<T, W, G, R, ROWS>(cj, av[u], j0 + u, col, val, slot);
                 const int64_t roff = (int64_t)cj * ldb;
 #pragma unroll
                 for (int r = 0; r < R; ++r)
@@ -147,8 +199,8 @@ __device__ __forceinline__ void consume_step(T (&acc)[R][W],
 #pragma unroll
             for (int u = 0; u < C::U; ++u) {
                 const int j = j0 + u;
-                const int cj = __shfl_sync(FULL, col[j / G], j % G, G);
-                av[u] = __shfl_sync(FULL, val[j / G], j % G, G);
+                int cj;
+                fetch_pair<T, W, G, R, ROWS>(cj, av[u], j, col, val, slot);
                 const int64_t roff = (int64_t)cj * ldb;
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
@@ -208,7 +260,7 @@ __device__ __forceinline__ void load_c_row(T (&c0)[R][W], const T* __restrict__ 
     }
 }
 
-template <typename T, int W, int G, int R>
+template <typename T, int W, int G, int R, int BS>
 __device__ __forceinline__ void write_row_c0(T* __restrict__ Crow, const T (&acc)[R][W],
                                              const T (&c0)[R][W], int vbase, int pw, T alpha,
                                              T beta) {
@@ -216,7 +268,8 @@ __device__ __forceinline__ void write_row_c0(T* __restrict__ Crow, const T (&acc
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         const int col = (vbase + g + G * r) * W;
-        if (col < pw) store_c_pre<T, W>(Crow + col, min(W, pw - col), acc[r], c0[r], alpha, beta);
+        if (col < pw)
+            store_c_pre<T, W, BS>(Crow + col, min(W, pw - col), acc[r], c0[r], alpha, beta);
     }
 }
 
@@ -229,10 +282,10 @@ __device__ __forceinline__ void write_row_c0(T* __restrict__ Crow, const T (&acc
 //     group gi takes entries [s + gi*CH, s + gi*CH + CH) of each warp step of
 //     RPW*CH entries, and the groups are combined at the end of the row.
 // ---------------------------------------------------------------------------
-template <typename T, int W, int G, int R, bool MEDIUM, bool READ_C, bool WHOLE>
+template <typename T, int W, int G, int R, bool MEDIUM, bool READ_C, bool WHOLE, int BS>
 __device__ __forceinline__ void process_rows(const SpmmParams<T>& p, const int* __restrict__ list,
                                              int first, int count, int stride, int c0col, int pw,
-                                             uint64_t pol_s) {
+                                             uint64_t pol_s, unsigned char* wslot) {
     using C = Cfg<T, W, G, R, true>;
     constexpr int Q = C::Q;
     const int lane = threadIdx.x & 31;
@@ -240,6 +293,7 @@ __device__ __forceinline__ void process_rows(const SpmmParams<T>& p, const int* 
     constexpr int TSTEP = MEDIUM ? 1 : C::RPW;              // row-slot advance per row
     constexpr int ESTEP = MEDIUM ? C::RPW * C::CH : C::CH;  // entry advance per step
     const int goff = MEDIUM ? gi * C::CH : 0;
+    unsigned char* slot = wslot + gi * Bcast<T, W, G, R, true>::GROUP_BYTES;
     const int nvec = (pw + W - 1) / W;
     const T* Bp = p.B + c0col;
     const int ldb = (int)p.ldb;                            // <= INT_MAX (host check)
@@ -300,14 +354,16 @@ __device__ __forceinline__ void process_rows(const SpmmParams<T>& p, const int* 
                     cmax = (int)__reduce_max_sync(FULL, (unsigned)max(cnt, 0));
                     cmin = (int)__reduce_min_sync(FULL, (unsigned)max(cnt, 0));
                 }
-                consume_step<T, W, G, R, true, WHOLE>(acc, colc, valc, cnt, cmax, cmin, ldb, lv);
+                consume_step<T, W, G, R, true, WHOLE>(acc, colc, valc, cnt, cmax, cmin, ldb, lv,
+                                                      slot);
 
                 if (s + ESTEP >= len) {                     // row finished (uniform if MEDIUM)
                     if (MEDIUM) combine_groups<T, W, G, R>(acc);
                     if (active && (!MEDIUM || gi == 0)) {
                         T* Crow = p.C + (int64_t)row * p.ldc + c0col;
                         if constexpr (READ_C)
-                            write_row_c0<T, W, G, R>(Crow, acc, c0, vbase, pw, p.alpha, p.beta);
+                            write_row_c0<T, W, G, R, BS>(Crow, acc, c0, vbase, pw, p.alpha,
+                                                         p.beta);
                         else
                             write_row<T, W, G, R>(Crow, acc, vbase, pw, p.alpha, p.beta, false,
                                                   p.keep_c);
@@ -365,10 +421,15 @@ struct RowsOccupancy {
 
 // READ_C: beta != 0 (C is read, and prefetched at each row start).
 // WHOLE: n is a multiple of W (no partial vectors; see gather_b).
-template <typename T, int W, int G, int R, bool READ_C, bool WHOLE>
+// BS: 0 for any beta; +1 / -1 for a launch with beta == +1 / -1 (see epi).
+template <typename T, int W, int G, int R, bool READ_C, bool WHOLE, int BS = 0>
 __global__ void __launch_bounds__(RowsOccupancy<T, W, G>::THREADS, RowsOccupancy<T, W, G>::MIN_BLOCKS)
 rows_kernel(SpmmParams<T> p) {
     constexpr int WPB = RowsOccupancy<T, W, G>::THREADS / 32;    // warps per block
+    // per-warp slots for the (col_idx, value) broadcast (Bcast)
+    constexpr int SLOT_BYTES = Bcast<T, W, G, R, true>::WARP_BYTES;
+    __shared__ __align__(16) unsigned char s_slots[SLOT_BYTES > 0 ? WPB * SLOT_BYTES : 16];
+    unsigned char* wslot = s_slots + (threadIdx.x >> 5) * SLOT_BYTES;
     wait_for_predecessor();
     allow_successor();
     const uint64_t pol_s = policy_evict_first();
@@ -400,11 +461,11 @@ rows_kernel(SpmmParams<T> p) {
         const int c0 = panel * p.panel_cols;
         const int pw = min(p.panel_cols, p.n - c0);
         if (s_count > 0)
-            process_rows<T, W, G, R, false, READ_C, WHOLE>(p, p.rowlist, s_first, s_count,
-                                                           s_stride, c0, pw, pol_s);
+            process_rows<T, W, G, R, false, READ_C, WHOLE, BS>(p, p.rowlist, s_first, s_count,
+                                                               s_stride, c0, pw, pol_s, wslot);
         if (m1 > m0)
-            process_rows<T, W, G, R, true, READ_C, WHOLE>(p, p.rowlist + n_short, m0, m1 - m0,
-                                                          1, c0, pw, pol_s);
+            process_rows<T, W, G, R, true, READ_C, WHOLE, BS>(p, p.rowlist + n_short, m0,
+                                                              m1 - m0, 1, c0, pw, pol_s, wslot);
     }
 }
 

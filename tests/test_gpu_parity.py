@@ -312,3 +312,40 @@ def test_csr_check(handle):
     p = tiny_uniform()
     assert cs.csr_check(handle, torch.from_numpy(p.row_ptr).cuda(),
                         torch.from_numpy(p.col_idx).cuda(), p.k) == 0
+
+
+# ---------------------------------------------------------------------------
+# binary64 with beta = +1 / -1: the epilogue leaves out the multiply by beta
+# (exact), on the 16-byte path; other widths take the general epilogue
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n", [2, 6, 32, 64, 100])
+@pytest.mark.parametrize("beta", [1.0, -1.0])
+def test_f64_unit_beta(handle, n, beta):
+    p = laplacian_2d(40, n, seed=31)
+    p.beta = beta
+    got, _ = run_problem(handle, p)
+    assert_parity(p, got, what=f"f64 beta={beta} n={n}")
+    # beta = -1 with C0 and beta = +1 with -C0 give the same bits
+    if beta == -1.0:
+        q = laplacian_2d(40, n, seed=31)
+        q.beta = 1.0
+        q.C0 = -q.C0
+        other, _ = run_problem(handle, q)
+        assert np.array_equal(got[:, :n].view(np.uint64), other[:, :n].view(np.uint64))
+
+
+@pytest.mark.parametrize("beta", [1.0, -1.0])
+def test_f64_unit_beta_integer_exact(handle, beta):
+    p = uniform_rows(3000, 2500, 32, 9, seed=32, dtype=np.float64, alpha=2.0, beta=beta,
+                     integer_range=3)
+    got, _ = run_problem(handle, p)
+    assert_parity(p, got, exact=True, what=f"f64 integer beta={beta}")
+
+
+def test_f64_unit_beta_unaligned_b(handle):
+    """B at an odd element offset takes the scalar path with the general
+    epilogue; the result stays in parity."""
+    p = laplacian_2d(30, 32, seed=33)
+    got, _ = run_problem(handle, p, b_offset=1)
+    assert_parity(p, got, what="f64 beta=-1 unaligned B")

@@ -11,7 +11,8 @@
 //   bin_scan    one CTA: exclusive scans of the tile records, bin totals
 //   bin_scatter per tile: stable ranks (warp ballots + per-warp prefix),
 //               writes rowlist, med_pre and long_pre, and zeroes the
-//               per-long-row counters of the long-row kernel
+//               per-long-row counters of the long-row kernel; a tile of
+//               short rows only just lists its row range
 // Ranks come from ballots in ascending row order, never from atomics, so the
 // lists (and everything computed from them) are identical on every call.
 #include "spmm_internal.h"
@@ -133,6 +134,21 @@ __device__ __forceinline__ void tile_scatter(const int* __restrict__ row_ptr, in
     }
 }
 
+// A tile whose rows are all short (the count pass says so) lists them in
+// order at its offset in the short bin: rowlist[off + i] = first row + i.  No
+// re-read of row_ptr, no ranks, no barriers; there are no medium or long rows
+// to place.  Same list as tile_scatter gives.
+template <int ITEMS>
+__device__ __forceinline__ void tile_all_short(int m, int tile, int short_off,
+                                               int* __restrict__ rowlist) {
+    const int base = tile * BIN_THREADS * ITEMS;
+#pragma unroll
+    for (int j = 0; j < ITEMS; ++j) {
+        const int i = j * BIN_THREADS + threadIdx.x;
+        if (base + i < m) rowlist[short_off + i] = base + i;
+    }
+}
+
 __device__ __forceinline__ void write_header(const int (&total)[R_USED], int* __restrict__ hdr,
                                              int* __restrict__ med_pre, int* __restrict__ long_pre) {
     hdr[HDR_COUNT_SHORT] = total[R_SHORT];
@@ -158,6 +174,10 @@ bin_single_kernel(const int* __restrict__ row_ptr, int m, int short_max, int lon
 #pragma unroll
     for (int c = 0; c < R_USED; ++c) total[c] = tile_total(s_part, c);
     if (threadIdx.x == 0) write_header(total, hdr, med_pre, long_pre);
+    if (total[R_SHORT] == m) {                    // uniform: every row is short
+        tile_all_short<BIN_SINGLE_ITEMS>(m, 0, 0, rowlist);
+        return;
+    }
     int run[R_USED] = {0, 0, 0, 0, 0};
     const int bin_base[3] = {0, total[R_SHORT], total[R_SHORT] + total[R_MED]};
     tile_scatter<BIN_SINGLE_ITEMS>(row_ptr, m, short_max, long_min, 0, run, bin_base, rowlist,
@@ -241,12 +261,19 @@ bin_scan_kernel(const int* __restrict__ tile_counts, int tiles, int* __restrict_
 template <int ITEMS>
 __global__ void __launch_bounds__(BIN_THREADS)
 bin_scatter_kernel(const int* __restrict__ row_ptr, int m, int short_max, int long_min,
-                   const int* __restrict__ tile_offsets, const int* __restrict__ hdr,
-                   int* __restrict__ rowlist, int* __restrict__ med_pre,
-                   int* __restrict__ long_pre, int* __restrict__ long_cnt) {
+                   const int* __restrict__ tile_counts, const int* __restrict__ tile_offsets,
+                   const int* __restrict__ hdr, int* __restrict__ rowlist,
+                   int* __restrict__ med_pre, int* __restrict__ long_pre,
+                   int* __restrict__ long_cnt) {
     __shared__ int s_wc[BIN_THREADS / 32][R_USED];
     wait_for_predecessor();
     allow_successor();
+    const int rows_in_tile = min(BIN_THREADS * ITEMS, m - (int)blockIdx.x * BIN_THREADS * ITEMS);
+    if (tile_counts[blockIdx.x * BIN_REC + R_SHORT] == rows_in_tile) {   // uniform per CTA
+        tile_all_short<ITEMS>(m, blockIdx.x, tile_offsets[blockIdx.x * BIN_REC + R_SHORT],
+                              rowlist);
+        return;
+    }
     int run[R_USED];
 #pragma unroll
     for (int c = 0; c < R_USED; ++c) run[c] = tile_offsets[blockIdx.x * BIN_REC + c];
@@ -277,8 +304,9 @@ cudaError_t launch_binning(const int* row_ptr, int m, int short_max, int long_mi
                        s.long_pre);
     if (e != cudaSuccess) return e;
     return launch_chained(scatter, dim3(s.tiles), blk, 0, st, overlap, row_ptr, m,
-                          short_max, long_min, (const int*)s.tile_offsets, (const int*)s.hdr,
-                          s.rowlist, s.med_pre, s.long_pre, s.long_cnt);
+                          short_max, long_min, (const int*)s.tile_counts,
+                          (const int*)s.tile_offsets, (const int*)s.hdr, s.rowlist, s.med_pre,
+                          s.long_pre, s.long_cnt);
 }
 
 }  // namespace spmm

@@ -349,3 +349,19 @@ def test_f64_unit_beta_unaligned_b(handle):
     p = laplacian_2d(30, 32, seed=33)
     got, _ = run_problem(handle, p, b_offset=1)
     assert_parity(p, got, what="f64 beta=-1 unaligned B")
+
+
+def test_mixed_tiles_of_short_rows_and_long_rows(handle):
+    """Full-warp lane groups (n = 100) make every row under 1024 entries short,
+    so most pre-pass tiles hold short rows only (listed by their fast path)
+    while the tiles holding a long row take the ranked scatter; and one-CTA
+    pre-pass sizes, with and without a long row."""
+    p = power_law(40_000, 40_000, 100, 900_000, 20_000, seed=34)
+    lens = np.diff(p.row_ptr)
+    assert 0 < int((lens >= 1024).sum()) < 200
+    got, _ = run_problem(handle, p)
+    assert_parity(p, got, what="mixed tiles")
+    for m, cap in ((2000, 50), (2000, 1500)):
+        q = power_law(m, m, 100, 40 * m, cap, seed=35)
+        got, _ = run_problem(handle, q)
+        assert_parity(q, got, what=f"one-CTA pre-pass m={m} cap={cap}")

@@ -330,7 +330,7 @@ spmm_status_t spmm_csr_impl(spmm_handle_t h, T alpha, const int32_t* row_ptr,
     mark(h, 4, st);               // the fixup runs inside the long-row launch
     if (h->profiling) {
         h->prof = spmm_profile_t{};
-        h->prof.launches = (m <= BIN_SINGLE_ROWS ? 1 : 3) + 2;
+        h->prof.launches = binning_launches(m) + 2;
         h->prof.panels = P.npanels;
         h->prof.panel_cols = P.panel_cols;
         h->prof.vec_elems = P.geo.W;
@@ -549,7 +549,7 @@ spmm_status_t spmm_squared_impl(spmm_handle_t h, T alpha, const int32_t* row_ptr
     mark(h, 4, st);
     if (h->profiling) {
         h->prof = spmm_profile_t{};
-        h->prof.launches = (m <= BIN_SINGLE_ROWS ? 1 : 3) + 4;
+        h->prof.launches = binning_launches(m) + 4;
         h->prof.panels = P2.npanels;
         h->prof.panel_cols = P2.panel_cols;
         h->prof.vec_elems = P2.geo.W;

@@ -4,12 +4,14 @@
 // entries; the long prefix drives the long-row CTA split).
 //
 // Reads row_ptr only.  For m <= 2048 a single CTA does everything in one
-// launch; otherwise three launches:
+// launch; otherwise two launches (three when the tiles exceed about one wave,
+// m > 2.49 M, where a one-CTA scan of the tile records runs in between):
 //   bin_count   per tile (512, 1024 or 2048 rows, the smallest that keeps the
 //               tile count within about one wave): rows per bin, entries in
 //               medium and long rows
-//   bin_scan    one CTA: exclusive scans of the tile records, bin totals
-//   bin_scatter per tile: stable ranks (warp ballots + per-warp prefix),
+//   bin_scatter per tile: the tile's offsets and the bin totals, reduced
+//               from the tile records by each CTA (CTA 0 writes the
+//               header), or read from the scan; stable ranks (warp ballots + per-warp prefix),
 //               writes rowlist, med_pre and long_pre, and zeroes the
 //               per-long-row counters of the long-row kernel; a tile of
 //               short rows only just lists its row range
@@ -258,28 +260,76 @@ bin_scan_kernel(const int* __restrict__ tile_counts, int tiles, int* __restrict_
     }
 }
 
-template <int ITEMS>
+// The tile's offsets in every bin and prefix, and the bin totals.  SELF: the
+// CTA reduces the tile records itself (used while there are at most
+// BIN_WAVE_TILES of them, read from L2: this replaces the one-CTA scan
+// launch); the records of the tiles before its own give its offsets, all of
+// them the totals, and CTA 0 writes the header.  Otherwise bin_scan_kernel
+// has written the offsets and the header.
+template <int ITEMS, bool SELF>
 __global__ void __launch_bounds__(BIN_THREADS)
 bin_scatter_kernel(const int* __restrict__ row_ptr, int m, int short_max, int long_min,
                    const int* __restrict__ tile_counts, const int* __restrict__ tile_offsets,
-                   const int* __restrict__ hdr, int* __restrict__ rowlist,
+                   int tiles, int* __restrict__ hdr, int* __restrict__ rowlist,
                    int* __restrict__ med_pre, int* __restrict__ long_pre,
                    int* __restrict__ long_cnt) {
-    __shared__ int s_wc[BIN_THREADS / 32][R_USED];
+    constexpr int NW = BIN_THREADS / 32;
+    __shared__ int s_wc[NW][R_USED];
+    __shared__ int s_red[NW][2 * R_USED];
     wait_for_predecessor();
     allow_successor();
+    int run[R_USED], total[R_USED];
+    if constexpr (SELF) {
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        int before[R_USED] = {0, 0, 0, 0, 0}, all[R_USED] = {0, 0, 0, 0, 0};
+        for (int t = threadIdx.x; t < tiles; t += BIN_THREADS) {
+#pragma unroll
+            for (int c = 0; c < R_USED; ++c) {
+                const int v = tile_counts[t * BIN_REC + c];
+                all[c] += v;
+                before[c] += t < (int)blockIdx.x ? v : 0;
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < R_USED; ++c)
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                before[c] += __shfl_xor_sync(FULL, before[c], off);
+                all[c] += __shfl_xor_sync(FULL, all[c], off);
+            }
+        if (lane == 0)
+#pragma unroll
+            for (int c = 0; c < R_USED; ++c) {
+                s_red[warp][c] = before[c];
+                s_red[warp][R_USED + c] = all[c];
+            }
+        __syncthreads();
+#pragma unroll
+        for (int c = 0; c < R_USED; ++c) {
+            int b = 0, a = 0;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                b += s_red[w][c];
+                a += s_red[w][R_USED + c];
+            }
+            run[c] = b;
+            total[c] = a;
+        }
+        if (blockIdx.x == 0 && threadIdx.x == 0) write_header(total, hdr, med_pre, long_pre);
+    } else {
+#pragma unroll
+        for (int c = 0; c < R_USED; ++c) run[c] = tile_offsets[blockIdx.x * BIN_REC + c];
+        total[R_SHORT] = hdr[HDR_COUNT_SHORT];
+        total[R_MED] = hdr[HDR_COUNT_MEDIUM];
+    }
     const int rows_in_tile = min(BIN_THREADS * ITEMS, m - (int)blockIdx.x * BIN_THREADS * ITEMS);
     if (tile_counts[blockIdx.x * BIN_REC + R_SHORT] == rows_in_tile) {   // uniform per CTA
-        tile_all_short<ITEMS>(m, blockIdx.x, tile_offsets[blockIdx.x * BIN_REC + R_SHORT],
-                              rowlist);
+        tile_all_short<ITEMS>(m, blockIdx.x, run[R_SHORT], rowlist);
         return;
     }
-    int run[R_USED];
-#pragma unroll
-    for (int c = 0; c < R_USED; ++c) run[c] = tile_offsets[blockIdx.x * BIN_REC + c];
-    const int bin_base[3] = {0, hdr[HDR_COUNT_SHORT], hdr[HDR_COUNT_SHORT] + hdr[HDR_COUNT_MEDIUM]};
+    const int bin_base[3] = {0, total[R_SHORT], total[R_SHORT] + total[R_MED]};
     tile_scatter<ITEMS>(row_ptr, m, short_max, long_min, blockIdx.x, run, bin_base, rowlist,
-                            med_pre, long_pre, long_cnt, s_wc);
+                        med_pre, long_pre, long_cnt, s_wc);
 }
 
 }  // namespace
@@ -294,19 +344,26 @@ cudaError_t launch_binning(const int* row_ptr, int m, int short_max, int long_mi
                               s.long_cnt);
     auto count = s.items == 8 ? bin_count_kernel<8> : s.items == 4 ? bin_count_kernel<4>
                                                                       : bin_count_kernel<2>;
-    auto scatter = s.items == 8 ? bin_scatter_kernel<8> : s.items == 4 ? bin_scatter_kernel<4>
-                                                                        : bin_scatter_kernel<2>;
     cudaError_t e = launch_chained(count, dim3(s.tiles), blk, 0, st, false, row_ptr, m,
                                    short_max, long_min, s.tile_counts);
     if (e != cudaSuccess) return e;
+    if (s.tiles <= BIN_WAVE_TILES) {
+        auto scatter = s.items == 8 ? bin_scatter_kernel<8, true>
+                       : s.items == 4 ? bin_scatter_kernel<4, true> : bin_scatter_kernel<2, true>;
+        return launch_chained(scatter, dim3(s.tiles), blk, 0, st, overlap, row_ptr, m,
+                              short_max, long_min, (const int*)s.tile_counts,
+                              (const int*)s.tile_offsets, s.tiles, s.hdr, s.rowlist, s.med_pre,
+                              s.long_pre, s.long_cnt);
+    }
     e = launch_chained(bin_scan_kernel, dim3(1), dim3(SCAN_THREADS), 0, st, overlap,
                        (const int*)s.tile_counts, s.tiles, s.tile_offsets, s.hdr, s.med_pre,
                        s.long_pre);
     if (e != cudaSuccess) return e;
-    return launch_chained(scatter, dim3(s.tiles), blk, 0, st, overlap, row_ptr, m,
-                          short_max, long_min, (const int*)s.tile_counts,
-                          (const int*)s.tile_offsets, (const int*)s.hdr, s.rowlist, s.med_pre,
-                          s.long_pre, s.long_cnt);
+    auto scatter = s.items == 8 ? bin_scatter_kernel<8, false>
+                   : s.items == 4 ? bin_scatter_kernel<4, false> : bin_scatter_kernel<2, false>;
+    return launch_chained(scatter, dim3(s.tiles), blk, 0, st, overlap, row_ptr, m, short_max,
+                          long_min, (const int*)s.tile_counts, (const int*)s.tile_offsets,
+                          s.tiles, s.hdr, s.rowlist, s.med_pre, s.long_pre, s.long_cnt);
 }
 
 }  // namespace spmm

@@ -102,6 +102,16 @@ inline void bin_geometry(int64_t m, int* items, int* tiles) {
     *tiles = (int)((m + BIN_THREADS * it - 1) / (BIN_THREADS * it));
 }
 
+// Kernel launches of the pre-pass for m rows (spmm_bin.cu): one CTA for
+// m <= BIN_SINGLE_ROWS; count + scatter while the tiles fit one wave; count +
+// scan + scatter beyond.
+inline int binning_launches(int64_t m) {
+    if (m <= BIN_SINGLE_ROWS) return 1;
+    int items, tiles;
+    bin_geometry(m, &items, &tiles);
+    return tiles <= BIN_WAVE_TILES ? 2 : 3;
+}
+
 struct BinScratch {
     int* rowlist;       // [m]  short rows, then medium rows, then long rows (each ascending)
     int* med_pre;       // [m + 1] exclusive prefix of medium-row lengths (stable order)

@@ -324,7 +324,7 @@ spmm_status_t spmm_plan_csr_f64(spmm_plan_t plan, double alpha,
  * GPU durations between CUDA events recorded on the call's stream around each
  * stage; the counts come from the device-side row bins. */
 typedef struct {
-    float prepass_ms;      /* row-binning pre-pass (3 launches) */
+    float prepass_ms;      /* row-binning pre-pass (1 to 3 launches) */
     float rows_ms;         /* short + medium rows kernel (1 launch) */
     float long_ms;         /* long-row CTA split (1 launch) */
     float fixup_ms;        /* 0: the long-row fixup runs inside the long-row launch */

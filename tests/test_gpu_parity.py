@@ -365,3 +365,16 @@ def test_mixed_tiles_of_short_rows_and_long_rows(handle):
         q = power_law(m, m, 100, 40 * m, cap, seed=35)
         got, _ = run_problem(handle, q)
         assert_parity(q, got, what=f"one-CTA pre-pass m={m} cap={cap}")
+
+
+def test_prepass_beyond_one_wave_of_tiles(handle):
+    """More than 2.49 M rows: the pre-pass tiles exceed one wave, and a one-CTA
+    scan of the tile records runs between count and scatter (below that each
+    scatter CTA reduces the records itself)."""
+    p = power_law(2_600_000, 2_600_000, 8, 9_000_000, 4000, seed=36)
+    lens = np.diff(p.row_ptr)
+    assert int((lens >= 1024).sum()) > 0 and int(((lens > 16) & (lens < 1024)).sum()) > 0
+    got, _ = run_problem(handle, p)
+    rows = np.unique(np.concatenate([np.linspace(0, p.m - 1, 3000).astype(np.int64),
+                                     np.flatnonzero(lens >= 1024)[:50]]))
+    assert_parity(p, got, rows=rows, what="pre-pass with a scan launch")

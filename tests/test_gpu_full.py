@@ -75,3 +75,56 @@ def test_full_wide_n_integer(handle):
     want = colsum_A @ p.B.astype(np.int64)
     assert np.all(np.isfinite(got))
     assert np.array_equal(got.astype(np.int64).sum(axis=0), want)
+
+
+def test_b_and_c_beyond_2_31_elements(handle):
+    """B (k x ldb) and C (m x ldc) each hold more than 2^31 elements (8.8 GB
+    apiece), so gather and store addresses need 64-bit arithmetic.  Only a
+    few rows of A are non-empty; they read B rows on both sides of the 2^31
+    boundary and write C rows past it.  The oracle evaluates the same sums on
+    a compacted copy of the B rows that A references (same entries, same
+    order); every other row of C must come out as alpha * 0 = 0."""
+    import torch
+    from synth import Problem
+    m = k = 2_200_000
+    n, ld = 1000, 1004
+    assert m * ld > 2 ** 31 and k * ld > 2 ** 31
+    rows = np.unique(np.concatenate([[0, 1, m // 2], np.arange(m - 100, m)]))
+    per = 5
+    hi_cols = (2 ** 31) // ld + np.arange(0, 50_000, 997)              # rows past element 2^31
+    pool = np.unique(np.concatenate([[0, 1, k // 2, k - 2, k - 1], hi_cols]))
+    pick = np.floor(rng.uniform(40, 1, rows.size * per) * pool.size).astype(np.int64)
+    cols = np.sort(pool[pick].reshape(rows.size, per), axis=1)
+    lens = np.zeros(m, np.int64)
+    lens[rows] = per
+    rp = np.zeros(m + 1, np.int64)
+    np.cumsum(lens, out=rp[1:])
+    ci = cols.ravel().astype(np.int32)
+    vals = rng.uniform(40, 2, ci.size, -1.0, 1.0).astype(np.float32)
+    used, local = np.unique(ci, return_inverse=True)
+    Bused = rng.uniform(40, 3, used.size * n, -1.0, 1.0).reshape(used.size, n).astype(np.float32)
+
+    dev = torch.device("cuda")
+    Bd = torch.empty((k, ld), dtype=torch.float32, device=dev)
+    Bd[torch.from_numpy(used.astype(np.int64)).to(dev), :n] = torch.from_numpy(Bused).to(dev)
+    Cd = torch.full((m, ld), float("nan"), dtype=torch.float32, device=dev)
+    rpd = torch.from_numpy(rp.astype(np.int32)).to(dev)
+    cid = torch.from_numpy(ci).to(dev)
+    vd = torch.from_numpy(vals).to(dev)
+    alpha = 1.5
+    cs.spmm_csr_f32(handle.ptr, alpha, rpd.data_ptr(), cid.data_ptr(), vd.data_ptr(), m, k,
+                    Bd.data_ptr(), ld, n, 0.0, Cd.data_ptr(), ld,
+                    torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    empty = np.array([2, 3, m // 2 + 1, m - 101], np.int64)
+    check = np.concatenate([rows, empty])
+    got = Cd[torch.from_numpy(check).to(dev), :n].cpu().numpy()
+    del Bd, Cd
+    torch.cuda.empty_cache()
+    # the same sums on the compacted B: rows of A restricted to `rows`
+    sub_rp = np.zeros(rows.size + 1, np.int64)
+    np.cumsum(lens[rows], out=sub_rp[1:])
+    q = Problem("beyond_2_31", rows.size, used.size, n, sub_rp.astype(np.int32),
+                local.astype(np.int32), vals, Bused, None, alpha, 0.0)
+    assert_parity(q, got[: rows.size], what="64-bit addressing")
+    assert np.all(got[rows.size:] == 0.0)

@@ -39,13 +39,13 @@ constexpr int ILU0_SINGULAR = 1;
 constexpr int ILU0_WAIT_TIMEOUT = 2;
 constexpr int ILU0_SPIN_LIMIT = 1 << 22;       // polls of one queue slot (about a second)
 #ifndef SPMM_ILU0_SLEEP_NS
-#define SPMM_ILU0_SLEEP_NS 32
+#define SPMM_ILU0_SLEEP_NS 128
 #endif
 #ifndef SPMM_ILU0_POLL_EVERY
 #define SPMM_ILU0_POLL_EVERY 16        // a power of two
 #endif
 #ifndef SPMM_ILU0_BLOCKS_PER_SM
-#define SPMM_ILU0_BLOCKS_PER_SM 2      // 0: as many as fit (measured slower: idle warps poll)
+#define SPMM_ILU0_BLOCKS_PER_SM 1      // 0: as many as fit (measured slower: idle warps poll)
 #endif
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
@@ -69,7 +69,9 @@ __device__ __forceinline__ double mul_rn(double a, double b) { return __dmul_rn(
 __device__ __forceinline__ float sub_rn(float a, float b) { return __fsub_rn(a, b); }
 __device__ __forceinline__ double sub_rn(double a, double b) { return __dsub_rn(a, b); }
 
-// 1. lower entries per row, dependents per row, the first ready rows
+// 1. lower entries per row, dependents per row, the first ready rows; and
+//    for each lower entry (i, k) where row k keeps its pivot a_kk and where
+//    it ends (structure only: the factorisation then needs no search)
 template <typename T>
 __global__ void __launch_bounds__(256) ilu0_count(Ilu0Params<T> p) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -80,6 +82,14 @@ __global__ void __launch_bounds__(256) ilu0_count(Ilu0Params<T> p) {
         if (k >= i) break;                      // columns ascend
         atomicAdd(p.cnt + k, 1);
         ++lower;
+        const int ks = p.rp[k], ke = p.rp[k + 1];
+        int dp = -1;                            // first position of column k in row k
+        for (int r = ks; r < ke; ++r)
+            if (p.ci[r] == k) {
+                dp = r;
+                break;
+            }
+        p.piv[q] = make_int2(dp, ke);
     }
     p.pending[i] = lower;
     if (lower == 0) p.queue[atomicAdd(p.tail, 1)] = i;
@@ -167,60 +177,95 @@ __device__ bool factor_row_long(const Ilu0Params<T>& p, int i, int s, int e, int
     return true;
 }
 
-// Row i of at most 32 entries, held in registers (lane q: entry q) from the
-// first load to the final store; pivot rows are read 32 entries at a time.
-// Same steps and operations as the page, so the same bits.
+// Row i of at most 32 entries, held in registers (lane q: entry q, loaded by
+// the caller with the entry's pivot record) from the first load to the final
+// store.  The pivot rows (from each pivot on) are read all at once when they
+// hold at most 32 entries together, else 32 entries at a time.  Same steps
+// and operations as the page, so the same bits.
 template <typename T>
 __device__ bool factor_row_short(const Ilu0Params<T>& p, int i, int s, int e, int lane,
-                                 int& dmax) {
+                                 int my_c, T& my_v, int2 my_piv, int& dmax) {
     const int li = e - s;
     const bool mine = lane < li;
-    const int my_c = mine ? p.ci[s + lane] : 0x7fffffff;
-    T my_v = mine ? __ldcg(p.v + s + lane) : T(0);
     const int nlower = __popc(__ballot_sync(FULL, mine && my_c < i));   // columns ascend
-    // the pivot rows' extents, all at once
-    int kb = 0, kend = 0;
-    if (lane < nlower) {
-        kb = p.rp[my_c];
-        kend = p.rp[my_c + 1];
+    // the pivot rows from their pivots on: row k_t is entries [dp_t, ke_t)
+    const bool has = lane < nlower;
+    const int len = has ? (my_piv.x >= 0 ? my_piv.y - my_piv.x : 0) : 0;
+    int incl = len;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(FULL, incl, off);
+        if (lane >= off) incl += y;
+    }
+    const int total = __shfl_sync(FULL, incl, 31);
+    const int off_me = incl - len;                  // lane t: where row k_t starts in the batch
+    // batch all pivot rows into the warp's lanes when they fit (one round of loads)
+    int kc = -1;
+    T kv = T(0);
+    const bool batched = total <= 32;               // warp-uniform
+    if (batched) {
+        // lane L < total takes entry L - off_t of row k_t, t the last non-empty
+        // row with off_t <= L (offsets ascend with t)
+        int base = 0;
+        for (int t = 0; t < nlower; ++t) {
+            const int o = __shfl_sync(FULL, off_me, t);
+            const int ln = __shfl_sync(FULL, len, t);
+            const int dp = __shfl_sync(FULL, my_piv.x, t);
+            if (ln > 0 && lane >= o) base = dp - o;
+        }
+        if (lane < total) {
+            kc = p.ci[base + lane];
+            kv = __ldcg(p.v + base + lane);
+        }
     }
     for (int t = 0; t < nlower; ++t) {
-        const int k = __shfl_sync(FULL, my_c, t);
-        const int ks = __shfl_sync(FULL, kb, t), ke = __shfl_sync(FULL, kend, t);
-        const T aik = __shfl_sync(FULL, my_v, t);
-        int dp = -1;                          // the pivot's position in row k
-        bool zero = false;
-        T ratio = T(0);
-        for (int q0 = ks; q0 < ke; q0 += 32) {
-            const bool have = q0 + lane < ke;
-            const int kc = have ? p.ci[q0 + lane] : -1;
-            const T kv = have ? __ldcg(p.v + q0 + lane) : T(0);
-            int first = 0;                    // first entry of this chunk past the pivot
-            if (dp < 0) {
-                const unsigned hit = __ballot_sync(FULL, kc == k);
-                if (!hit) continue;
-                const int dl = __ffs(hit) - 1;
-                dp = q0 + dl;
-                const T akk = __shfl_sync(FULL, kv, dl);
-                if (akk == T(0)) {
-                    zero = true;
-                    break;
-                }
-                ratio = div_rn(aik, akk);
-                if (lane == t) my_v = ratio;
-                first = dl + 1;
-            }
-            // a_ij -= ratio * a_kj for the entries j > k of row k that row i stores
-            const int cnt = min(32, ke - q0);
-            for (int q = first; q < cnt; ++q) {
-                const int j = __shfl_sync(FULL, kc, q);
-                const T akj = __shfl_sync(FULL, kv, q);
-                if (mine && my_c == j) my_v = sub_rn(my_v, mul_rn(ratio, akj));
-            }
-        }
-        if (dp < 0 || zero) {                 // no pivot stored, or a zero one
+        const int dp = __shfl_sync(FULL, my_piv.x, t);
+        const int ke = __shfl_sync(FULL, my_piv.y, t);
+        if (dp < 0) {                               // row k stores no pivot
             if (lane == 0) stop(p.abort, p.status, ILU0_SINGULAR);
             return false;
+        }
+        const T aik = __shfl_sync(FULL, my_v, t);
+        if (batched) {
+            const int o = __shfl_sync(FULL, off_me, t);
+            const int ln = ke - dp;
+            const T akk = __shfl_sync(FULL, kv, o);
+            if (akk == T(0)) {
+                if (lane == 0) stop(p.abort, p.status, ILU0_SINGULAR);
+                return false;
+            }
+            const T ratio = div_rn(aik, akk);
+            if (lane == t) my_v = ratio;
+            // a_ij -= ratio * a_kj for the entries j > k of row k that row i stores
+            for (int q = 1; q < ln; ++q) {
+                const int j = __shfl_sync(FULL, kc, o + q);
+                const T akj = __shfl_sync(FULL, kv, o + q);
+                if (mine && my_c == j) my_v = sub_rn(my_v, mul_rn(ratio, akj));
+            }
+        } else {
+            T ratio = T(0);
+            for (int q0 = dp; q0 < ke; q0 += 32) {
+                const bool have = q0 + lane < ke;
+                const int c = have ? p.ci[q0 + lane] : -1;
+                const T v = have ? __ldcg(p.v + q0 + lane) : T(0);
+                int first = 0;
+                if (q0 == dp) {
+                    const T akk = __shfl_sync(FULL, v, 0);
+                    if (akk == T(0)) {
+                        if (lane == 0) stop(p.abort, p.status, ILU0_SINGULAR);
+                        return false;
+                    }
+                    ratio = div_rn(aik, akk);
+                    if (lane == t) my_v = ratio;
+                    first = 1;
+                }
+                const int cnt = min(32, ke - q0);
+                for (int q = first; q < cnt; ++q) {
+                    const int j = __shfl_sync(FULL, c, q);
+                    const T akj = __shfl_sync(FULL, v, q);
+                    if (mine && my_c == j) my_v = sub_rn(my_v, mul_rn(ratio, akj));
+                }
+            }
         }
     }
     if (p.depth) {
@@ -244,6 +289,10 @@ __device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
 // by finishing its own keeps the first of them (no queue round trip on the
 // critical path) and queues the rest.  Waiting warps give up only when no
 // row has finished anywhere for ILU0_SPIN_LIMIT polls, or on the abort word.
+//
+// The row's structure, its own values (no other row writes them), its pivot
+// records and its dependents are read before the acquire that makes the
+// pivot rows' values visible, so that those loads overlap it.
 template <typename T>
 __global__ void __launch_bounds__(ILU0_THREADS, 2) ilu0_factor(Ilu0Params<T> p) {
     const int lane = threadIdx.x & 31;
@@ -251,7 +300,8 @@ __global__ void __launch_bounds__(ILU0_THREADS, 2) ilu0_factor(Ilu0Params<T> p) 
     for (;;) {
         int i = next;
         next = -1;
-        if (i < 0) {
+        const bool kept = i >= 0;
+        if (!kept) {
             int h = 0;
             if (lane == 0) h = atomicAdd(p.head, 1);
             h = __shfl_sync(FULL, h, 0);
@@ -283,25 +333,38 @@ __global__ void __launch_bounds__(ILU0_THREADS, 2) ilu0_factor(Ilu0Params<T> p) 
                 __nanosleep(SPMM_ILU0_SLEEP_NS);
             }
         }
+        // static data of row i: extents, entries, pivot records, dependents
         const int s = p.rp[i], e = p.rp[i + 1];
+        const int d0 = p.dep_ptr[i], d1 = p.dep_ptr[i + 1];
+        // a kept row: acquire the values its finished dependencies wrote (every
+        // lane; the loads above are already in flight)
+        if (kept) ld_acquire(p.pending + i);
+        const bool short_row = e - s <= 32;
+        int my_c = 0x7fffffff;
+        T my_v = T(0);
+        int2 my_piv = make_int2(-1, 0);
+        if (short_row && lane < e - s) {
+            my_c = p.ci[s + lane];
+            my_v = __ldcg(p.v + s + lane);      // row i's own entries: written by row i only
+            if (my_c < i) my_piv = p.piv[s + lane];
+        }
+        const int dj = d0 + lane < d1 ? p.dep_idx[d0 + lane] : -1;
         int dmax = -1;
         bool ok;
-        if (e - s <= 32) ok = factor_row_short<T>(p, i, s, e, lane, dmax);
-        else ok = factor_row_long<T>(p, i, s, e, lane, dmax);
+        if (short_row)
+            ok = factor_row_short<T>(p, i, s, e, lane, my_c, my_v, my_piv, dmax);
+        else
+            ok = factor_row_long<T>(p, i, s, e, lane, dmax);
         if (!ok) return;
         if (p.depth && lane == 0) p.depth[i] = dmax + 1;
         __syncwarp();
         __threadfence();                        // row i final before it is counted down
         // count down the rows that wait for row i (acquire: a row that becomes
         // ready here sees its other dependencies' values); keep one, queue the rest
-        const int d0 = p.dep_ptr[i], d1 = p.dep_ptr[i + 1];
         for (int d = d0; d < d1; d += 32) {
-            int j = -1;
+            const int j = d == d0 ? dj : (d + lane < d1 ? p.dep_idx[d + lane] : -1);
             bool ready = false;
-            if (d + lane < d1) {
-                j = p.dep_idx[d + lane];
-                ready = atom_add_acq_rel(p.pending + j, -1) == 1;
-            }
+            if (d + lane < d1) ready = atom_add_acq_rel(p.pending + j, -1) == 1;
             unsigned rm = __ballot_sync(FULL, ready);
             if (next < 0 && rm) {
                 const int keep = __ffs(rm) - 1;
@@ -313,7 +376,6 @@ __global__ void __launch_bounds__(ILU0_THREADS, 2) ilu0_factor(Ilu0Params<T> p) 
         }
         __syncwarp();
         if (lane == 0) atomicAdd(p.finished, 1);
-        if (next >= 0) ld_acquire(p.pending + next);   // every lane: acquire the row's inputs
     }
 }
 

@@ -51,6 +51,8 @@ struct Ilu0Params {
     int* cnt;              // [n] rows depending on the row (then a fill cursor)
     int* dep_ptr;          // [n + 1] start of each row's dependents
     int* dep_idx;          // [nnz] dependent rows, grouped by the row they depend on
+    int2* piv;             // [nnz] per lower entry (i, k): the position of a_kk in row k
+                           //       (-1: none) and the end of row k
     int* queue;            // [n] rows in the order they became ready (-1: not yet)
     int* head;             // next queue slot to take
     int* tail;             // next queue slot to fill

@@ -135,3 +135,22 @@ def test_rejects_empty(handle):
     s = cs.spmm_ilu0(handle.ptr, 0, 0, z.data_ptr(), z.data_ptr(), z.data_ptr(), 0, z.data_ptr(),
                      check=False)
     assert s == 1                                     # SPMM_ERR_INVALID_ARGUMENT (as the page)
+
+
+@pytest.mark.parametrize("dtype", [np.float64, np.float32])
+def test_band_pivot_rows_past_one_warp(handle, dtype):
+    """Rows of 25 entries (band of half-width 12): a row's pivot rows, from
+    their pivots on, hold 12 x 13 entries together, more than one warp reads
+    at once, so they are read pivot row by pivot row; the narrow band below
+    (half-width 2, 5 pivot entries per row at most) reads them in one batch."""
+    from synth import rng
+    for n, w in ((3000, 12), (3000, 2)):
+        r = np.repeat(np.arange(n), 2 * w + 1)
+        c = r + np.tile(np.arange(-w, w + 1), n)
+        keep = (c >= 0) & (c < n)
+        r, c = r[keep], c[keep]
+        vals = rng.uniform(7, 1, r.size, -1.0, 1.0)
+        vals[r == c] = 4.0 * w + 1.0
+        rp = np.zeros(n + 1, np.int64)
+        np.cumsum(np.bincount(r, minlength=n), out=rp[1:])
+        check(handle, rp, c, vals.astype(dtype), f"band {w}")

@@ -128,3 +128,35 @@ def test_b_and_c_beyond_2_31_elements(handle):
                 local.astype(np.int32), vals, Bused, None, alpha, 0.0)
     assert_parity(q, got[: rows.size], what="64-bit addressing")
     assert np.all(got[rows.size:] == 0.0)
+
+
+def test_full_seacells_plan_in_breadth_first_order(handle):
+    """The SEACells product through a plan whose rows were put in
+    breadth-first order: bit for bit the direct product, at full size, on two
+    calls with different B."""
+    import copy
+
+    import torch
+    p = wl.seacells_knn()
+    direct, _ = run_problem(handle, p)
+    dev = torch.device("cuda")
+    rp = torch.from_numpy(p.row_ptr).to(dev)
+    ci = torch.from_numpy(p.col_idx).to(dev)
+    va = torch.from_numpy(p.values).to(dev)
+    C = torch.full((p.m, p.n), float("nan"), dtype=torch.float32, device=dev)
+    plan = cs.Plan(handle, rp, p.k, p.n, torch.float32)
+    try:
+        plan.order_rows(rp, ci)
+        for it, B in enumerate((p.B, p.B[::-1].copy())):
+            plan(p.alpha, rp, ci, va, torch.from_numpy(B).to(dev), p.beta, C)
+            torch.cuda.synchronize()
+            got = C.cpu().numpy()
+            if it == 0:
+                assert np.array_equal(got.view(np.uint32), direct[:, :p.n].view(np.uint32))
+            else:
+                q = copy.copy(p)
+                q.B = B
+                want, _ = run_problem(handle, q)
+                assert np.array_equal(got.view(np.uint32), want[:, :p.n].view(np.uint32))
+    finally:
+        plan.close()

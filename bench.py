@@ -409,14 +409,18 @@ def run_ours(args):
     torch.cuda.synchronize()
     unprofiled_ms = statistics.mean(a.elapsed_time(b) for a, b in uev)
 
-    # Repeated products on one analysed structure (a plan: no pre-pass per
-    # call), with the rows in their natural order and in breadth-first order
-    # of A's pattern; both give the direct call's results bit for bit.
+    # Repeated products (or chains) on one analysed structure (a plan: no
+    # pre-pass per call), with the rows in their natural order and in
+    # breadth-first order of A's pattern; both give the direct call's results
+    # bit for bit.
     plan_ms = None
-    if not chain and p.m == p.k:
+    if p.m == p.k:
         plan_ms = {}
         es = p.values.dtype.itemsize
-        pfn = cs.spmm_plan_csr_f32 if f32 else cs.spmm_plan_csr_f64
+        if chain:
+            pfn = cs.spmm_plan_csr_squared_f32 if f32 else cs.spmm_plan_csr_squared_f64
+        else:
+            pfn = cs.spmm_plan_csr_f32 if f32 else cs.spmm_plan_csr_f64
         plan = cs.spmm_plan_create(h.ptr, rp.data_ptr(), p.m, p.k, p.n, es, sptr)
         try:
             for label in ("natural", "breadth_first"):

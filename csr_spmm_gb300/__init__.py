@@ -18,7 +18,8 @@ from ._lib import (EXPORTED, SPMM_ERR_ALLOC, SPMM_ERR_CUDA, SPMM_ERR_DIMENSION_M
                    SPMM_ERR_UNSUPPORTED_DEVICE, SPMM_OK, SpmmError, library, spmm_create,
                    spmm_csr_check, spmm_csr_f32, spmm_csr_f32_noalloc, spmm_csr_f64,
                    spmm_destroy, spmm_get_profile, spmm_plan_create, spmm_plan_csr_f32,
-                   spmm_plan_csr_f64, spmm_plan_destroy, spmm_plan_order_rows,
+                   spmm_plan_csr_f64, spmm_plan_csr_squared_f32, spmm_plan_csr_squared_f64,
+                   spmm_plan_destroy, spmm_plan_order_rows,
                    spmm_row_order_bfs, spmm_set_l2_persistence,
                    spmm_csr_squared_f32, spmm_csr_squared_f64, spmm_fw_argmin,
                    spmm_ilu0, ILU0_SINGULAR, ILU0_WAIT_TIMEOUT,
@@ -30,7 +31,8 @@ __all__ = ["Handle", "spmm", "csr_check", "SpmmError", "library", "spmm_create",
            "spmm_plan_destroy", "spmm_set_l2_persistence", "spmm_plan_csr_f32",
            "spmm_csr_squared_f32", "spmm_csr_squared_f64", "spmm_squared",
            "spmm_fw_argmin", "fw_argmin", "spmm_ilu0", "ilu0", "Ilu0Error",
-           "spmm_plan_csr_f64", "spmm_plan_order_rows", "spmm_row_order_bfs", "Plan",
+           "spmm_plan_csr_f64", "spmm_plan_order_rows", "spmm_row_order_bfs",
+           "spmm_plan_csr_squared_f32", "spmm_plan_csr_squared_f64", "Plan",
            "EXPORTED"]
 
 
@@ -209,6 +211,17 @@ class Plan:
         ldb = B.stride(0) if B.shape[0] > 1 else max(1, self.n)
         ldc = C.stride(0) if C.shape[0] > 1 else max(1, self.n)
         fn = spmm_plan_csr_f32 if values.dtype == torch.float32 else spmm_plan_csr_f64
+        fn(self.ptr, alpha, _ptr(row_ptr), _ptr(col_idx), _ptr(values), _ptr(B), ldb, beta,
+           _ptr(C), ldc, st)
+
+    def squared(self, alpha, row_ptr, col_idx, values, B, beta, C, stream=None) -> None:
+        """C <- alpha * A (A B) + beta * C with A's structure from the plan (square A)."""
+        import torch
+        st = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+        ldb = B.stride(0) if B.shape[0] > 1 else max(1, self.n)
+        ldc = C.stride(0) if C.shape[0] > 1 else max(1, self.n)
+        fn = (spmm_plan_csr_squared_f32 if values.dtype == torch.float32
+              else spmm_plan_csr_squared_f64)
         fn(self.ptr, alpha, _ptr(row_ptr), _ptr(col_idx), _ptr(values), _ptr(B), ldb, beta,
            _ptr(C), ldc, st)
 

@@ -30,7 +30,8 @@ EXPORTED = ("spmm_create", "spmm_destroy", "spmm_reserve", "spmm_csr_f32", "spmm
             "spmm_set_l2_persistence", "spmm_csr_squared_f32", "spmm_csr_squared_f64",
             "spmm_fw_argmin_f32", "spmm_fw_argmin_f64", "spmm_ilu0_f32", "spmm_ilu0_f64",
             "spmm_plan_create", "spmm_plan_destroy", "spmm_plan_csr_f32", "spmm_plan_csr_f64",
-            "spmm_plan_order_rows", "spmm_row_order_bfs", "spmm_status_string")
+            "spmm_plan_order_rows", "spmm_row_order_bfs", "spmm_plan_csr_squared_f32",
+            "spmm_plan_csr_squared_f64", "spmm_status_string")
 
 
 class SpmmProfile(ctypes.Structure):
@@ -116,6 +117,12 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.spmm_plan_csr_f64.argtypes = [vp, ctypes.c_double, vp, vp, vp, vp, i64, ctypes.c_double,
                                       vp, i64, vp]
     lib.spmm_plan_csr_f64.restype = st
+    lib.spmm_plan_csr_squared_f32.argtypes = [vp, ctypes.c_float, vp, vp, vp, vp, i64,
+                                              ctypes.c_float, vp, i64, vp]
+    lib.spmm_plan_csr_squared_f32.restype = st
+    lib.spmm_plan_csr_squared_f64.argtypes = [vp, ctypes.c_double, vp, vp, vp, vp, i64,
+                                              ctypes.c_double, vp, i64, vp]
+    lib.spmm_plan_csr_squared_f64.restype = st
     lib.spmm_plan_order_rows.argtypes = [vp, vp, vp, vp]
     lib.spmm_plan_order_rows.restype = st
     lib.spmm_row_order_bfs.argtypes = [vp, vp, i64, vp]
@@ -193,6 +200,24 @@ def spmm_csr_f32_noalloc(alpha, row_ptr, col_idx, values, m, k, B, ldb, n, beta,
                                        float(beta), C, ldc, stream or None)
     if check:
         _check(s, "spmm_csr_f32_noalloc")
+    return s
+
+
+def spmm_plan_csr_squared_f32(plan, alpha, row_ptr, col_idx, values, B, ldb, beta, C, ldc,
+                              stream=0, check=True) -> int:
+    s = library().spmm_plan_csr_squared_f32(plan, float(alpha), row_ptr, col_idx, values, B, ldb,
+                                            float(beta), C, ldc, stream or None)
+    if check:
+        _check(s, "spmm_plan_csr_squared_f32")
+    return s
+
+
+def spmm_plan_csr_squared_f64(plan, alpha, row_ptr, col_idx, values, B, ldb, beta, C, ldc,
+                              stream=0, check=True) -> int:
+    s = library().spmm_plan_csr_squared_f64(plan, float(alpha), row_ptr, col_idx, values, B, ldb,
+                                            float(beta), C, ldc, stream or None)
+    if check:
+        _check(s, "spmm_plan_csr_squared_f64")
     return s
 
 

@@ -435,6 +435,55 @@ spmm_status_t spmm_plan_impl(spmm_plan_t pl, T alpha, const int32_t* row_ptr,
 // scratch with a 16-byte-aligned leading dimension and is stored with the
 // default L2 policy (not streamed), so that the second product's gathers of
 // T find it in L2 when it fits there.
+// The two products of the squared chain on bins already made (p carries A,
+// the bins and the partial-sum scratch): T = A B into Tm (leading dimension
+// ldt, default L2 policy so the second product finds it), then C = alpha A T
+// + beta C.  run_long: launch the long-row kernel (a plan knows whether its
+// structure has long rows); first_overlap: the first launch may overlap its
+// predecessor (the library's own pre-pass).  Marks profile events 2 and 3-4.
+template <typename T>
+spmm_status_t chain_products(spmm_handle_s* h, SpmmParams<T> p, const T* B, int64_t ldb, T* Tm,
+                             int64_t ldt, T alpha, T beta, T* C, int64_t ldc, bool run_long,
+                             bool first_overlap, bool overlap, cudaStream_t st) {
+    const int64_t m = p.m, n = p.n;
+    const Plan P1 = make_plan<T>(h, m, n, B, ldb, Tm, ldt);
+    const Plan P2 = make_plan<T>(h, m, n, Tm, ldt, C, ldc);
+    p.B = B;
+    p.ldb = ldb;
+    p.C = Tm;
+    p.ldc = ldt;
+    p.alpha = T(1);
+    p.beta = T(0);
+    p.keep_c = 1;
+    p.panel_cols = P1.panel_cols;
+    p.npanels = P1.npanels;
+    L2Window w1;
+    const L2Window* win1 = b_window(h, B, m, ldb, n, &w1);
+    if (launch_rows<T>(p, P1.geo, rows_grid(h, (int)sizeof(T), P1.geo), st, first_overlap,
+                       win1) != cudaSuccess ||
+        (run_long && launch_long<T>(p, P1.geo, st, overlap, win1) != cudaSuccess))
+        return SPMM_ERR_CUDA;
+    mark(h, 2, st);
+    p.B = Tm;
+    p.ldb = ldt;
+    p.C = C;
+    p.ldc = ldc;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.keep_c = 0;
+    p.panel_cols = P2.panel_cols;
+    p.npanels = P2.npanels;
+    L2Window w2;
+    const L2Window* win2 = b_window(h, static_cast<const T*>(Tm), m, ldt, n, &w2);
+    if (launch_rows<T>(p, P2.geo, rows_grid(h, (int)sizeof(T), P2.geo), st, overlap, win2) !=
+            cudaSuccess ||
+        (run_long && launch_long<T>(p, P2.geo, st, overlap, win2) != cudaSuccess))
+        return SPMM_ERR_CUDA;
+    mark(h, 3, st);
+    mark(h, 4, st);
+    return SPMM_OK;
+}
+
 template <typename T>
 spmm_status_t spmm_squared_impl(spmm_handle_t h, T alpha, const int32_t* row_ptr,
                                 const int32_t* col_idx, const T* values, int64_t m, const T* B,
@@ -491,7 +540,6 @@ spmm_status_t spmm_squared_impl(spmm_handle_t h, T alpha, const int32_t* row_ptr
     // first product T = A B; the bins it makes serve both products (they are
     // valid for any geometry)
     const Plan P1 = make_plan<T>(h, m, n, B, ldb, Tm, ldt);
-    const Plan P2 = make_plan<T>(h, m, n, Tm, ldt, C, ldc);
     const bool overlap = SPMM_PDL && !h->profiling;
     mark(h, 0, st);
     if (launch_binning(row_ptr, (int)m, P1.short_max, P1.long_min, bs, st, overlap) != cudaSuccess)
@@ -511,43 +559,10 @@ spmm_status_t spmm_squared_impl(spmm_handle_t h, T alpha, const int32_t* row_ptr
     p.hdr = bs.hdr;
     p.partials = reinterpret_cast<T*>(base + L.partials);
     p.long_grid = lg;
-
-    p.B = B;
-    p.ldb = ldb;
-    p.C = Tm;
-    p.ldc = ldt;
-    p.alpha = T(1);
-    p.beta = T(0);
-    p.keep_c = 1;
-    p.panel_cols = P1.panel_cols;
-    p.npanels = P1.npanels;
-    L2Window w1;
-    const L2Window* win1 = b_window(h, B, m, ldb, n, &w1);
-    if (launch_rows<T>(p, P1.geo, rows_grid(h, (int)sizeof(T), P1.geo), st, overlap, win1) !=
-            cudaSuccess ||
-        launch_long<T>(p, P1.geo, st, overlap, win1) != cudaSuccess)
-        return SPMM_ERR_CUDA;
-    mark(h, 2, st);
-
-    // second product C = alpha * A T + beta * C
-    p.B = Tm;
-    p.ldb = ldt;
-    p.C = C;
-    p.ldc = ldc;
-    p.alpha = alpha;
-    p.beta = beta;
-    p.keep_c = 0;
-    p.panel_cols = P2.panel_cols;
-    p.npanels = P2.npanels;
-    L2Window w2;
-    const L2Window* win2 = b_window(h, static_cast<const T*>(Tm), m, ldt, n, &w2);
-    if (launch_rows<T>(p, P2.geo, rows_grid(h, (int)sizeof(T), P2.geo), st, overlap, win2) !=
-            cudaSuccess ||
-        launch_long<T>(p, P2.geo, st, overlap, win2) != cudaSuccess)
-        return SPMM_ERR_CUDA;
-    mark(h, 3, st);
-    mark(h, 4, st);
+    s = chain_products<T>(h, p, B, ldb, Tm, ldt, alpha, beta, C, ldc, true, overlap, overlap, st);
+    if (s != SPMM_OK) return s;
     if (h->profiling) {
+        const Plan P2 = make_plan<T>(h, m, n, Tm, ldt, C, ldc);
         h->prof = spmm_profile_t{};
         h->prof.launches = binning_launches(m) + 4;
         h->prof.panels = P2.npanels;
@@ -558,6 +573,82 @@ spmm_status_t spmm_squared_impl(spmm_handle_t h, T alpha, const int32_t* row_ptr
         h->prof.short_max = P1.short_max;
         h->prof.long_min = P1.long_min;
         h->prof_hdr = bs.hdr;
+        h->have_profile = true;
+    }
+    return SPMM_OK;
+}
+
+// The squared chain through a plan: the plan's bins (and row order) serve both
+// products; the intermediate lives in the plan's handle's scratch.
+template <typename T>
+spmm_status_t spmm_plan_squared_impl(spmm_plan_t pl, T alpha, const int32_t* row_ptr,
+                                     const int32_t* col_idx, const T* values, const T* B,
+                                     int64_t ldb, T beta, T* C, int64_t ldc, void* stream) {
+    if (!pl || pl->es != (int)sizeof(T) || pl->m != pl->k) return SPMM_ERR_INVALID_ARGUMENT;
+    spmm_handle_s* h = pl->h;
+    const int64_t m = pl->m, n = pl->n;
+    if (ldb < std::max<int64_t>(1, n) || ldc < std::max<int64_t>(1, n))
+        return SPMM_ERR_DIMENSION_MISMATCH;
+    if (ldb > (int64_t)INT_MAX) return SPMM_ERR_INVALID_ARGUMENT;
+    if (m == 0 || n == 0) return SPMM_OK;
+    if (!C) return SPMM_ERR_NULL_POINTER;
+    const bool uses_a = alpha != T(0);
+    if (uses_a && (!row_ptr || !col_idx || !values || !B)) return SPMM_ERR_NULL_POINTER;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device) {
+        cudaGetLastError();
+        return SPMM_ERR_INVALID_ARGUMENT;
+    }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (!uses_a) {
+        if (h->profiling) {
+            h->prof = spmm_profile_t{};
+            h->prof.launches = 1;
+            h->prof_hdr = nullptr;
+            for (int i = 0; i < 5; ++i) mark(h, i, st);
+            h->have_profile = true;
+        }
+        return launch_scale<T>(C, ldc, (int)m, (int)n, beta, h->num_sms * 8, st) == cudaSuccess
+                   ? SPMM_OK : SPMM_ERR_CUDA;
+    }
+    constexpr int64_t WV = 16 / (int64_t)sizeof(T);
+    const int64_t ldt = (n + WV - 1) / WV * WV;
+    if (ldt > (int64_t)INT_MAX) return SPMM_ERR_INVALID_ARGUMENT;
+    spmm_status_t s = ensure_scratch(h, (size_t)m * (size_t)ldt * sizeof(T));
+    if (s != SPMM_OK) return s;
+    T* Tm = static_cast<T*>(h->scratch);
+
+    SpmmParams<T> p{};
+    p.row_ptr = row_ptr;
+    p.col_idx = col_idx;
+    p.values = values;
+    p.m = (int)m;
+    p.n = (int)n;
+    p.rowlist = pl->rowlist;
+    p.med_pre = pl->med_pre;
+    p.long_pre = pl->long_pre;
+    p.long_cnt = pl->long_cnt;
+    p.hdr = pl->hdr;
+    p.partials = static_cast<T*>(pl->partials);
+    p.long_grid = pl->long_grid;
+    const bool overlap = SPMM_PDL && !h->profiling;
+    mark(h, 0, st);
+    mark(h, 1, st);                       // no pre-pass: the plan holds the bins
+    s = chain_products<T>(h, p, B, ldb, Tm, ldt, alpha, beta, C, ldc,
+                          pl->hdr_host[HDR_COUNT_LONG] > 0, false, overlap, st);
+    if (s != SPMM_OK) return s;
+    if (h->profiling) {
+        const Plan P2 = make_plan<T>(h, m, n, Tm, ldt, C, ldc);
+        h->prof = spmm_profile_t{};
+        h->prof.launches = pl->hdr_host[HDR_COUNT_LONG] > 0 ? 4 : 2;
+        h->prof.panels = P2.npanels;
+        h->prof.panel_cols = P2.panel_cols;
+        h->prof.vec_elems = P2.geo.W;
+        h->prof.group_lanes = P2.geo.G;
+        h->prof.slots = P2.geo.R;
+        h->prof.short_max = P2.short_max;
+        h->prof.long_min = P2.long_min;
+        h->prof_hdr = pl->hdr;
         h->have_profile = true;
     }
     return SPMM_OK;
@@ -1029,6 +1120,22 @@ spmm_status_t spmm_csr_squared_f64(spmm_handle_t h, double alpha, const int32_t*
                                    double* C, int64_t ldc, void* stream) {
     return spmm_squared_impl<double>(h, alpha, row_ptr, col_idx, values, m, B, ldb, n, beta, C,
                                      ldc, stream);
+}
+
+spmm_status_t spmm_plan_csr_squared_f32(spmm_plan_t plan, float alpha, const int32_t* row_ptr,
+                                        const int32_t* col_idx, const float* values,
+                                        const float* B, int64_t ldb, float beta, float* C,
+                                        int64_t ldc, void* stream) {
+    return spmm_plan_squared_impl<float>(plan, alpha, row_ptr, col_idx, values, B, ldb, beta, C,
+                                         ldc, stream);
+}
+
+spmm_status_t spmm_plan_csr_squared_f64(spmm_plan_t plan, double alpha, const int32_t* row_ptr,
+                                        const int32_t* col_idx, const double* values,
+                                        const double* B, int64_t ldb, double beta, double* C,
+                                        int64_t ldc, void* stream) {
+    return spmm_plan_squared_impl<double>(plan, alpha, row_ptr, col_idx, values, B, ldb, beta,
+                                          C, ldc, stream);
 }
 
 spmm_status_t spmm_fw_argmin_f32(spmm_handle_t h, int64_t n, int64_t k,

@@ -273,6 +273,27 @@ spmm_status_t spmm_plan_create(spmm_handle_t h, spmm_plan_t *plan, const int32_t
  * products on a plan need the handle alive. */
 spmm_status_t spmm_plan_destroy(spmm_plan_t plan);
 
+/* The squared chain C = alpha * A (A B) + beta * C (as spmm_csr_squared_f32,
+ * the K^2 B operand of the SEACells Frank-Wolfe kernels of the bixverse page)
+ * with A's structure taken from a plan made for a square A (k == m): both
+ * products use the plan's bins and row order, so neither runs a pre-pass.
+ * The intermediate A B lives in the scratch of the plan's handle (m x n,
+ * leading dimension rounded up to 16 bytes, grown with cudaMalloc like any
+ * handle scratch).  Same arguments and conventions as spmm_csr_squared_f32,
+ * with m and n from the plan; the results equal spmm_csr_squared_f32's bit
+ * for bit.  SPMM_ERR_INVALID_ARGUMENT if the plan is not square or was made
+ * for the other element size.  Asynchronous on `stream`. */
+spmm_status_t spmm_plan_csr_squared_f32(spmm_plan_t plan, float alpha,
+                                        const int32_t *row_ptr, const int32_t *col_idx,
+                                        const float *values, const float *B, int64_t ldb,
+                                        float beta, float *C, int64_t ldc, void *stream);
+
+/* Same in binary64. */
+spmm_status_t spmm_plan_csr_squared_f64(spmm_plan_t plan, double alpha,
+                                        const int32_t *row_ptr, const int32_t *col_idx,
+                                        const double *values, const double *B, int64_t ldb,
+                                        double beta, double *C, int64_t ldc, void *stream);
+
 /* Change the order in which the plan's products process the rows of A (not
  * where results go): the short- and medium-row lists are re-sorted into the
  * breadth-first order of A's pattern (spmm_row_order_bfs), so that rows which

@@ -147,3 +147,68 @@ def test_seacells_full_size_sampled(handle):
     ab, _ = oracle.spmm(p.m, p.k, p.n, 1.0, p.row_ptr, p.col_idx, p.values, p.B, p.ldb, 0.0)
     want = a1 @ ab
     assert np.allclose(s_got, want, rtol=1e-4)
+
+
+def run_plan_squared(handle, p, order=False, b_offset=0):
+    """The chain through a plan (pre-pass once), optionally in breadth-first row order."""
+    import torch
+    dev = torch.device("cuda")
+    rp, ci, va = (_dev(a, torch, dev) for a in (p.row_ptr, p.col_idx, p.values))
+    Bd = _dev(np.concatenate([np.zeros(b_offset, p.B.dtype), p.B.ravel()]), torch, dev)
+    C_init = p.C0 if p.C0 is not None else np.full((p.m, p.ldc), np.nan, p.values.dtype)
+    Cd = _dev(np.ascontiguousarray(C_init).copy(), torch, dev)
+    st = torch.cuda.current_stream().cuda_stream
+    plan = cs.spmm_plan_create(handle.ptr, rp.data_ptr(), p.m, p.m, p.n, p.values.itemsize, st)
+    try:
+        if order:
+            cs.spmm_plan_order_rows(plan, rp.data_ptr(), ci.data_ptr(), st)
+        fn = (cs.spmm_plan_csr_squared_f32 if p.values.dtype == np.float32
+              else cs.spmm_plan_csr_squared_f64)
+        fn(plan, p.alpha, rp.data_ptr(), ci.data_ptr(), va.data_ptr(),
+           Bd.data_ptr() + b_offset * p.B.itemsize, p.ldb, p.beta, Cd.data_ptr(), p.ldc, st)
+        torch.cuda.synchronize()
+    finally:
+        cs.spmm_plan_destroy(plan)
+    return Cd.cpu().numpy()[: p.m * p.ldc].reshape(p.m, p.ldc)
+
+
+def _bits(a):
+    return a.view(np.uint32 if a.dtype == np.float32 else np.uint64)
+
+
+@pytest.mark.parametrize("name", ["knn", "power_law", "laplacian_f64"])
+@pytest.mark.parametrize("order", [False, True])
+def test_plan_chain_equals_direct_chain(handle, name, order):
+    """Through a plan, in natural or breadth-first row order, the chain gives
+    the direct chain's bits (same bins, same per-row arithmetic), and so the
+    oracle's parity."""
+    p = {"knn": lambda: knn_kernel_graph(6000, 30, 100, 50, seed=1),
+         "power_law": lambda: power_law(30_000, 30_000, 64, 600_000, 10_000, seed=5),
+         "laplacian_f64": lambda: laplacian_2d(60, 32, seed=3)}[name]()
+    direct, _ = run_squared(handle, p)
+    got = run_plan_squared(handle, p, order=order)
+    assert np.array_equal(_bits(got[:, :p.n]), _bits(direct[:, :p.n])), (name, order)
+    rows = np.unique(np.linspace(0, p.m - 1, 200).astype(np.int64))
+    assert_chain_parity(p, got, rows=rows, what=f"plan chain {name}")
+
+
+def test_plan_chain_unaligned_b_and_errors(handle):
+    import torch
+    p = knn_kernel_graph(2000, 15, 40, 20, seed=14)
+    direct, _ = run_squared(handle, p, b_offset=1)
+    got = run_plan_squared(handle, p, b_offset=1)
+    assert np.array_equal(_bits(got[:, :p.n]), _bits(direct[:, :p.n]))
+    # a plan made for a non-square structure is rejected
+    q = uniform_rows(100, 80, 8, 3, seed=15, dtype=np.float32)
+    rp = torch.from_numpy(q.row_ptr).cuda()
+    plan = cs.spmm_plan_create(handle.ptr, rp.data_ptr(), q.m, q.k, q.n, 4)
+    try:
+        d = torch.zeros(16, dtype=torch.float32, device="cuda")
+        s = cs.spmm_plan_csr_squared_f32(plan, 1.0, d.data_ptr(), d.data_ptr(), d.data_ptr(),
+                                         d.data_ptr(), q.n, 0.0, d.data_ptr(), q.n, check=False)
+        assert s == cs.SPMM_ERR_INVALID_ARGUMENT
+        s = cs.spmm_plan_csr_squared_f64(plan, 1.0, d.data_ptr(), d.data_ptr(), d.data_ptr(),
+                                         d.data_ptr(), q.n, 0.0, d.data_ptr(), q.n, check=False)
+        assert s == cs.SPMM_ERR_INVALID_ARGUMENT
+    finally:
+        cs.spmm_plan_destroy(plan)

@@ -212,3 +212,24 @@ def test_plan_chain_unaligned_b_and_errors(handle):
         assert s == cs.SPMM_ERR_INVALID_ARGUMENT
     finally:
         cs.spmm_plan_destroy(plan)
+
+
+def test_plan_class_squared(handle):
+    """The Python Plan wrapper's chain, in breadth-first row order."""
+    import torch
+    p = knn_kernel_graph(3000, 15, 40, 20, seed=16)
+    dev = torch.device("cuda")
+    rp = torch.from_numpy(p.row_ptr).to(dev)
+    ci = torch.from_numpy(p.col_idx).to(dev)
+    va = torch.from_numpy(p.values).to(dev)
+    B = torch.from_numpy(p.B).to(dev)
+    C = torch.empty(p.m, p.n, dtype=torch.float32, device=dev)
+    plan = cs.Plan(handle, rp, p.k, p.n, torch.float32)
+    try:
+        plan.order_rows(rp, ci)
+        plan.squared(p.alpha, rp, ci, va, B, p.beta, C)
+        torch.cuda.synchronize()
+    finally:
+        plan.close()
+    direct, _ = run_squared(handle, p)
+    assert np.array_equal(C.cpu().numpy().view(np.uint32), direct[:, :p.n].view(np.uint32))

@@ -761,6 +761,63 @@ spmm_status_t spmm_ilu0_impl(spmm_handle_t h, int64_t n, int64_t nnz, const int3
     return launch_ilu0<T>(p, grid, st) == cudaSuccess ? SPMM_OK : SPMM_ERR_CUDA;
 }
 
+// Host part of spmm_plan_order_rows (may throw std::bad_alloc).
+spmm_status_t plan_order_rows(spmm_plan_t pl, const int32_t* row_ptr, const int32_t* col_idx,
+                              void* stream) {
+    if (!pl) return SPMM_ERR_INVALID_ARGUMENT;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != pl->device) {
+        cudaGetLastError();
+        return SPMM_ERR_INVALID_ARGUMENT;
+    }
+    const int n_short = pl->hdr_host[HDR_COUNT_SHORT];
+    const int n_med = pl->hdr_host[HDR_COUNT_MEDIUM];
+    const int64_t m = pl->m;
+    if (m == 0 || n_short + n_med == 0) return SPMM_OK;    // no rows binned: nothing to order
+    if (!row_ptr) return SPMM_ERR_NULL_POINTER;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    auto fail = [] {
+        cudaGetLastError();
+        return SPMM_ERR_CUDA;
+    };
+    std::vector<int32_t> rp((size_t)m + 1);
+    if (cudaMemcpyAsync(rp.data(), row_ptr, rp.size() * sizeof(int32_t), cudaMemcpyDeviceToHost,
+                        st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return fail();
+    if (!csr_rows_valid(rp.data(), m)) return SPMM_ERR_INVALID_CSR;
+    const int64_t nnz = rp[m];
+    if (nnz > 0 && !col_idx) return SPMM_ERR_NULL_POINTER;
+    std::vector<int32_t> ci((size_t)nnz);
+    std::vector<int32_t> list((size_t)n_short + n_med);
+    if ((nnz > 0 && cudaMemcpyAsync(ci.data(), col_idx, ci.size() * sizeof(int32_t),
+                                    cudaMemcpyDeviceToHost, st) != cudaSuccess) ||
+        cudaMemcpyAsync(list.data(), pl->rowlist, list.size() * sizeof(int32_t),
+                        cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return fail();
+    std::vector<int32_t> order((size_t)m), rank((size_t)m);
+    row_order_bfs(rp.data(), ci.data(), (int)m, order.data());
+    for (int64_t i = 0; i < m; ++i) rank[order[i]] = (int32_t)i;
+    auto by_rank = [&](int32_t a, int32_t b) { return rank[a] < rank[b]; };
+    std::sort(list.begin(), list.begin() + n_short, by_rank);
+    std::sort(list.begin() + n_short, list.end(), by_rank);
+    // prefix of medium-row lengths in the new list order (it balances medium
+    // rows across warps by entries)
+    std::vector<int32_t> med((size_t)n_med + 1, 0);
+    for (int i = 0; i < n_med; ++i) {
+        const int32_t r = list[(size_t)n_short + i];
+        med[i + 1] = med[i] + (rp[r + 1] - rp[r]);
+    }
+    if (cudaMemcpyAsync(pl->rowlist, list.data(), list.size() * sizeof(int32_t),
+                        cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        (n_med > 0 && cudaMemcpyAsync(pl->med_pre, med.data(), med.size() * sizeof(int32_t),
+                                      cudaMemcpyHostToDevice, st) != cudaSuccess) ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return fail();
+    return SPMM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1004,58 +1061,11 @@ spmm_status_t spmm_plan_destroy(spmm_plan_t pl) {
 
 spmm_status_t spmm_plan_order_rows(spmm_plan_t pl, const int32_t* row_ptr,
                                    const int32_t* col_idx, void* stream) {
-    if (!pl) return SPMM_ERR_INVALID_ARGUMENT;
-    int cur = -1;
-    if (cudaGetDevice(&cur) != cudaSuccess || cur != pl->device) {
-        cudaGetLastError();
-        return SPMM_ERR_INVALID_ARGUMENT;
+    try {
+        return plan_order_rows(pl, row_ptr, col_idx, stream);
+    } catch (const std::bad_alloc&) {          // no C++ exception crosses the C ABI
+        return SPMM_ERR_ALLOC;
     }
-    const int n_short = pl->hdr_host[HDR_COUNT_SHORT];
-    const int n_med = pl->hdr_host[HDR_COUNT_MEDIUM];
-    const int64_t m = pl->m;
-    if (m == 0 || n_short + n_med == 0) return SPMM_OK;    // no rows binned: nothing to order
-    if (!row_ptr) return SPMM_ERR_NULL_POINTER;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    auto fail = [] {
-        cudaGetLastError();
-        return SPMM_ERR_CUDA;
-    };
-    std::vector<int32_t> rp((size_t)m + 1);
-    if (cudaMemcpyAsync(rp.data(), row_ptr, rp.size() * sizeof(int32_t), cudaMemcpyDeviceToHost,
-                        st) != cudaSuccess ||
-        cudaStreamSynchronize(st) != cudaSuccess)
-        return fail();
-    if (!csr_rows_valid(rp.data(), m)) return SPMM_ERR_INVALID_CSR;
-    const int64_t nnz = rp[m];
-    if (nnz > 0 && !col_idx) return SPMM_ERR_NULL_POINTER;
-    std::vector<int32_t> ci((size_t)nnz);
-    std::vector<int32_t> list((size_t)n_short + n_med);
-    if ((nnz > 0 && cudaMemcpyAsync(ci.data(), col_idx, ci.size() * sizeof(int32_t),
-                                    cudaMemcpyDeviceToHost, st) != cudaSuccess) ||
-        cudaMemcpyAsync(list.data(), pl->rowlist, list.size() * sizeof(int32_t),
-                        cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-        cudaStreamSynchronize(st) != cudaSuccess)
-        return fail();
-    std::vector<int32_t> order((size_t)m), rank((size_t)m);
-    row_order_bfs(rp.data(), ci.data(), (int)m, order.data());
-    for (int64_t i = 0; i < m; ++i) rank[order[i]] = (int32_t)i;
-    auto by_rank = [&](int32_t a, int32_t b) { return rank[a] < rank[b]; };
-    std::sort(list.begin(), list.begin() + n_short, by_rank);
-    std::sort(list.begin() + n_short, list.end(), by_rank);
-    // prefix of medium-row lengths in the new list order (it balances medium
-    // rows across warps by entries)
-    std::vector<int32_t> med((size_t)n_med + 1, 0);
-    for (int i = 0; i < n_med; ++i) {
-        const int32_t r = list[(size_t)n_short + i];
-        med[i + 1] = med[i] + (rp[r + 1] - rp[r]);
-    }
-    if (cudaMemcpyAsync(pl->rowlist, list.data(), list.size() * sizeof(int32_t),
-                        cudaMemcpyHostToDevice, st) != cudaSuccess ||
-        (n_med > 0 && cudaMemcpyAsync(pl->med_pre, med.data(), med.size() * sizeof(int32_t),
-                                      cudaMemcpyHostToDevice, st) != cudaSuccess) ||
-        cudaStreamSynchronize(st) != cudaSuccess)
-        return fail();
-    return SPMM_OK;
 }
 
 spmm_status_t spmm_plan_csr_f32(spmm_plan_t plan, float alpha, const int32_t* row_ptr,

@@ -17,6 +17,7 @@
 // (measured on GB300: the degree sort makes no difference to the product).
 #include <climits>
 #include <cstdint>
+#include <new>
 #include <vector>
 
 #include "csr_spmm.h"
@@ -60,6 +61,10 @@ extern "C" spmm_status_t spmm_row_order_bfs(const int32_t* row_ptr, const int32_
     if (!row_ptr || !order) return SPMM_ERR_NULL_POINTER;
     if (!spmm::csr_rows_valid(row_ptr, m)) return SPMM_ERR_INVALID_CSR;
     if (row_ptr[m] > 0 && !col_idx) return SPMM_ERR_NULL_POINTER;
-    spmm::row_order_bfs(row_ptr, col_idx, (int)m, order);
+    try {
+        spmm::row_order_bfs(row_ptr, col_idx, (int)m, order);
+    } catch (const std::bad_alloc&) {          // no C++ exception crosses the C ABI
+        return SPMM_ERR_ALLOC;
+    }
     return SPMM_OK;
 }

@@ -143,25 +143,33 @@ class ClockSampler:
             self.proc.kill()
         self.out.flush()
         self.out.seek(0)
-        rows = [ln.strip().split(", ") for ln in self.out.read().splitlines() if ln.strip()]
+        text = self.out.read()
         os.unlink(self.out.name)
-        sm, smax, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            if len(r) < 9:
-                continue
-            try:
-                sm.append(float(r[1]))
-                smax = float(r[2])
-            except ValueError:
-                continue
-            for nm, v in zip(names, r[5:9]):
-                if v.strip().lower() == "active":
-                    reasons.add(nm)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return parse_clock_samples(text)
+
+
+def parse_clock_samples(text):
+    """Median SM clock, maximum clock and the throttle reasons seen, from
+    nvidia-smi --query-gpu=<ClockSampler.FIELDS> --format=csv,noheader,nounits
+    lines (one per sample; unparsable lines are skipped)."""
+    rows = [ln.strip().split(", ") for ln in text.splitlines() if ln.strip()]
+    sm, smax, reasons = [], None, set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for r in rows:
+        if len(r) < 9:
+            continue
+        try:
+            sm.append(float(r[1]))
+            smax = float(r[2])
+        except ValueError:
+            continue
+        for nm, v in zip(names, r[5:9]):
+            if v.strip().lower() == "active":
+                reasons.add(nm)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": 0}
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+            "samples": len(sm)}
 
 
 def rows_kernel_bytes(p, prof):

@@ -1,0 +1,62 @@
+"""Host-side arithmetic of bench.py (no GPU): the clock-sample parser and the
+algorithmic byte counts behind the roofline and GB/s figures."""
+import os
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from synth import knn_kernel_graph, power_law, uniform_rows  # noqa: E402
+
+
+def test_clock_samples_median_max_and_reasons():
+    text = "\n".join([
+        "0, 2070, 2070, 812.3, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "0, 1980, 2070, 1390.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, 2010, 2070, 1200.5, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "garbage line",
+        "0, [N/A], 2070, 0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "",
+    ])
+    c = bench.parse_clock_samples(text)
+    assert c["samples"] == 3 and c["sm_mhz"] == 2010.0 and c["sm_max_mhz"] == 2070.0
+    assert c["reasons"] == ["sw_power_cap"]
+    hot = "0, 1500, 2070, 900, 0x8, Active, Not Active, Active, Not Active"
+    assert bench.parse_clock_samples(hot)["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
+    assert bench.parse_clock_samples("")["samples"] == 0
+
+
+def _all_short_profile(p):
+    return {"rows_short": p.m, "rows_medium": 0, "long_nnz": 0}
+
+
+def test_rows_kernel_bytes_equal_the_whole_product_when_every_row_is_short():
+    for p in (knn_kernel_graph(500, 8, 12, 5, seed=1),                       # beta = 0
+              uniform_rows(300, 200, 9, 4, seed=2, beta=0.5)):               # beta != 0
+        assert bench.rows_kernel_bytes(p, _all_short_profile(p)) == p.algorithmic_bytes()
+
+
+def test_rows_kernel_bytes_leave_the_long_rows_out():
+    p = power_law(5000, 5000, 16, 100_000, 3000, seed=3)
+    lens = np.diff(p.row_ptr)
+    long_rows = lens >= 1024
+    prof = {"rows_short": int((~long_rows).sum()), "rows_medium": 0,
+            "long_nnz": int(lens[long_rows].sum())}
+    got = bench.rows_kernel_bytes(p, prof)
+    es = p.values.itemsize
+    entries = p.nnz - prof["long_nnz"]
+    want = (4 * (prof["rows_short"] + 1) + (4 + es) * entries
+            + entries / p.nnz * es * p.k * p.n + 2 * es * p.n * prof["rows_short"])
+    assert got == want and got < p.algorithmic_bytes()
+
+
+def test_chain_bytes_and_flops():
+    p = knn_kernel_graph(400, 6, 10, 4, seed=4)
+    p.meta["chain"] = "squared"
+    csr, mn = 4 * (p.m + 1) + 8 * p.nnz, 4 * p.m * p.n     # binary32, beta = 0
+    # A twice, B once, the intermediate written and read once, C written
+    assert bench.problem_bytes(p) == 2 * csr + mn + 2 * mn + mn
+    assert bench.problem_flops(p) == 2 * (2 * p.nnz * p.n)

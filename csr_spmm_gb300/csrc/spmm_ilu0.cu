@@ -8,7 +8,8 @@
 // round trips:
 //   1. every row counts its lower entries (the rows it waits for) and adds
 //      itself to the dependent count of each of them; rows with none are
-//      queued;
+//      queued; for each lower entry (i, k) it records where row k keeps its
+//      pivot and where row k ends;
 //   2. a prefix sum turns the dependent counts into list offsets;
 //   3. the dependent lists are filled (the transpose of the strict lower
 //      pattern);

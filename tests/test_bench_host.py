@@ -60,3 +60,22 @@ def test_chain_bytes_and_flops():
     # A twice, B once, the intermediate written and read once, C written
     assert bench.problem_bytes(p) == 2 * csr + mn + 2 * mn + mn
     assert bench.problem_flops(p) == 2 * (2 * p.nnz * p.n)
+
+
+def test_reference_arm_line_on_cpu():
+    """`bench.py --impl reference` runs the CPU oracle only (no GPU) and prints
+    one JSON line with the contract's keys."""
+    import json
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "2", "--warmup", "1", "--workload", "tiny_uniform"],
+                       capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "GFLOP/s" and d["value"] > 0
+    assert d["metric"] == bench.METRIC and d["higher_is_better"] is True
+    assert d["steps"] == 2 and d["warmup"] == 1 and d["config"]["workload"] == "tiny_uniform"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0

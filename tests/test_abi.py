@@ -72,3 +72,23 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(_lib, "_lib", None)
     with pytest.raises(ImportError):
         _lib.library(str(tmp_path / "nope.so"))
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/csr_spmm.h compiles as C (C99 and C11), not only as C++, and
+    every declared entry point can be referenced from C."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if not gcc:
+        pytest.skip("gcc not available")
+    names = sorted(_declared_symbols())
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "csr_spmm.h"\n'
+                   + "".join(f"void (*ref_{n})(void) = (void (*)(void))&{n};\n" for n in names))
+    for std in ("c99", "c11"):
+        r = subprocess.run([gcc, f"-std={std}", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                            "-fsyntax-only",
+                            "-I", os.path.join(ROOT, "include"), str(src)],
+                           capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr

@@ -382,56 +382,64 @@ int oracle_fw_argmin(int esize, int64_t n, int64_t k,
 
 /*
  * ILU(0): the incomplete LU factorisation with zero fill-in of the oxicuda
- * preconditioner page (preconditioner/ilu0.rs: module doc, `ilu0`,
- * `factor_row_host`, `analyze_ilu0_levels`).  A is square, CSR with column
- * indices ascending within each row.
+ * preconditioner page (preconditioner/ilu0.rs: module doc, `ilu0`, the host
+ * row factorisation and the level analysis).  A is square, CSR with column
+ * indices strictly ascending within each row.
  *
  * Levels: depth(i) = 1 + max depth(k) over the stored k < i of row i (0 when
  * there is none); rows are factored level by level, and within a level in
  * increasing index order.
  *
- * Row i, in place on A's values: for each stored k < i in CSR order, the
- * pivot a_kk is looked up in row k (absent or zero: singular, stop);
- * a_ik := a_ik / a_kk; then for each stored j > k of row k, if row i stores
- * column j, a_ij := a_ij - a_ik * a_kj.  Each operation is one rounded
- * divide, multiply or subtract in the element type (binary32 or binary64),
- * as on the page (no fused multiply-add; this file is compiled without
- * contraction), so a correct implementation reproduces it bit for bit.
- * L is the strictly lower part with a unit diagonal, U the rest.
+ * The elimination is Gaussian elimination in its row-oriented (IKJ) form,
+ * confined to A's pattern.  Row i is brought to its final value by
+ * subtracting multiples of the already factored rows k < i that it stores,
+ * k ascending: l_ik = a_ik / u_kk, then a_ij -= l_ik * u_kj for every j > k
+ * stored in both rows (a j outside row i's pattern would be fill-in, which
+ * ILU(0) drops).  A zero or absent u_kk is a singular pivot.  Each operation
+ * is one rounded divide, multiply or subtract in the element type (binary32
+ * or binary64), as on the page (no fused multiply-add; this file is compiled
+ * without contraction); every a_ij receives its updates in ascending k, so a
+ * correct implementation reproduces it bit for bit.  L is the strictly
+ * lower part with a unit diagonal, U the rest.
+ *
+ * Bookkeeping: diag[r] is where row r stores its diagonal (-1 if nowhere);
+ * slot[c] is where the row being eliminated stores column c (-1 if it does
+ * not), filled before the row and cleared after it.
  */
 #define ORACLE_SINGULAR -4
 
-static int64_t find_col(const int32_t *ci, int64_t start, int64_t end, int64_t col)
-{
-    for (int64_t p = start; p < end; ++p)
-        if (ci[p] == col) return p;
-    return -1;
-}
-
-#define ILU0_FACTOR_ROW(NAME, T)                                                         \
-    static int NAME(int64_t i, const int32_t *rp, const int32_t *ci, T *v)               \
+#define ILU0_ELIMINATE(NAME, T)                                                          \
+    static int NAME(int64_t n, const int32_t *rp, const int32_t *ci, T *v,               \
+                    const int64_t *order, const int64_t *diag, int64_t *slot)            \
     {                                                                                    \
-        const int64_t s = rp[i], e = rp[i + 1];                                          \
-        for (int64_t nz = s; nz < e; ++nz) {                                             \
-            const int64_t k = ci[nz];                                                    \
-            if (k >= i) break;                  /* past the lower triangle */            \
-            const int64_t ks = rp[k], ke = rp[k + 1];                                    \
-            const int64_t dp = find_col(ci, ks, ke, k);                                  \
-            if (dp < 0 || v[dp] == (T)0) return ORACLE_SINGULAR;                         \
-            const T ratio = v[nz] / v[dp];                                               \
-            v[nz] = ratio;                                                               \
-            for (int64_t knz = dp + 1; knz < ke; ++knz) {                                \
-                const int64_t ij = find_col(ci, s, e, ci[knz]);                          \
-                if (ij >= 0) {                                                           \
-                    const T update = ratio * v[knz];                                     \
-                    v[ij] = v[ij] - update;                                              \
+        for (int64_t r = 0; r < n; ++r) {                                                \
+            const int64_t i = order[r];                                                  \
+            const int64_t lo = rp[i], hi = rp[i + 1];                                    \
+            int rc = ORACLE_OK;                                                          \
+            for (int64_t p = lo; p < hi; ++p) slot[ci[p]] = p;                           \
+            for (int64_t p = lo; p < hi && ci[p] < i; ++p) {                             \
+                const int64_t k = ci[p];                                                 \
+                const int64_t pk = diag[k];                                              \
+                if (pk < 0 || v[pk] == (T)0) {                                           \
+                    rc = ORACLE_SINGULAR;                                                \
+                    break;                                                               \
+                }                                                                        \
+                const T l_ik = v[p] / v[pk];                                             \
+                v[p] = l_ik;                                                             \
+                for (int64_t q = pk + 1; q < (int64_t)rp[k + 1]; ++q) {                  \
+                    const int64_t t = slot[ci[q]];                                       \
+                    if (t < 0) continue;                /* fill-in: dropped */           \
+                    const T prod = l_ik * v[q];                                          \
+                    v[t] = v[t] - prod;                                                  \
                 }                                                                        \
             }                                                                            \
+            for (int64_t p = lo; p < hi; ++p) slot[ci[p]] = -1;                          \
+            if (rc != ORACLE_OK) return rc;                                              \
         }                                                                                \
         return ORACLE_OK;                                                                \
     }
-ILU0_FACTOR_ROW(ilu0_row_f32, float)
-ILU0_FACTOR_ROW(ilu0_row_f64, double)
+ILU0_ELIMINATE(ilu0_eliminate_f32, float)
+ILU0_ELIMINATE(ilu0_eliminate_f64, double)
 
 /* depth[i] for every row (the page's level analysis); returns the level count. */
 int64_t oracle_ilu0_levels(int64_t n, const int32_t *rp, const int32_t *ci, int64_t *depth)
@@ -461,29 +469,31 @@ int oracle_ilu0(int esize, int64_t n, const int32_t *rp, const int32_t *ci, void
             if (ci[p] <= ci[p - 1]) return ORACLE_BAD_CSR;   /* strictly ascending */
     int64_t *d = depth ? depth : (int64_t *)malloc(sizeof(int64_t) * (size_t)n);
     int64_t *order = (int64_t *)malloc(sizeof(int64_t) * (size_t)n);
+    int64_t *diag = (int64_t *)malloc(sizeof(int64_t) * (size_t)n);
+    int64_t *slot = (int64_t *)malloc(sizeof(int64_t) * (size_t)n);
     int64_t *start = NULL;
-    if (!d || !order) {
-        if (!depth) free(d);
-        free(order);
-        return ORACLE_NO_MEMORY;
-    }
+    int rc = ORACLE_NO_MEMORY;
+    if (!d || !order || !diag || !slot) goto done;
     const int64_t nlev = oracle_ilu0_levels(n, rp, ci, d);
     /* rows grouped by level, increasing index within a level (counting sort) */
     start = (int64_t *)calloc((size_t)nlev + 1, sizeof(int64_t));
-    if (!start) {
-        if (!depth) free(d);
-        free(order);
-        return ORACLE_NO_MEMORY;
-    }
+    if (!start) goto done;
     for (int64_t i = 0; i < n; ++i) start[d[i] + 1]++;
     for (int64_t l = 0; l < nlev; ++l) start[l + 1] += start[l];
     for (int64_t i = 0; i < n; ++i) order[start[d[i]]++] = i;
-    int rc = ORACLE_OK;
-    for (int64_t r = 0; r < n && rc == ORACLE_OK; ++r)
-        rc = (esize == 4) ? ilu0_row_f32(order[r], rp, ci, (float *)values)
-                          : ilu0_row_f64(order[r], rp, ci, (double *)values);
+    for (int64_t i = 0; i < n; ++i) {
+        diag[i] = -1;
+        slot[i] = -1;
+        for (int64_t p = rp[i]; p < (int64_t)rp[i + 1]; ++p)
+            if (ci[p] == i) diag[i] = p;
+    }
+    rc = (esize == 4) ? ilu0_eliminate_f32(n, rp, ci, (float *)values, order, diag, slot)
+                      : ilu0_eliminate_f64(n, rp, ci, (double *)values, order, diag, slot);
+done:
     if (!depth) free(d);
     free(order);
+    free(diag);
+    free(slot);
     free(start);
     return rc;
 }

@@ -152,18 +152,20 @@ def test_rejects_unsorted_rows():
 
 
 MUTANTS = {
-    "ratio_not_stored": ("            v[nz] = ratio;", "            (void)0;"),
-    "update_added": ("v[ij] = v[ij] - update;", "v[ij] = v[ij] + update;"),
-    "pivot_row_is_own_row": ("const int64_t dp = find_col(ci, ks, ke, k);",
-                             "const int64_t dp = find_col(ci, s, e, k);"),
-    "update_includes_pivot": ("for (int64_t knz = dp + 1; knz < ke; ++knz) {",
-                              "for (int64_t knz = ks; knz < ke; ++knz) {"),
-    "diagonal_eliminated": ("if (k >= i) break;                  /* past the lower triangle */",
-                            "if (k > i) break;"),
+    "ratio_not_stored": ("                v[p] = l_ik;", "                (void)0;"),
+    "update_added": ("v[t] = v[t] - prod;", "v[t] = v[t] + prod;"),
+    "pivot_row_is_own_row": ("const int64_t pk = diag[k];", "const int64_t pk = slot[k];"),
+    "update_includes_pivot": ("for (int64_t q = pk + 1; q < (int64_t)rp[k + 1]; ++q) {",
+                              "for (int64_t q = rp[k]; q < (int64_t)rp[k + 1]; ++q) {"),
+    "diagonal_eliminated": ("for (int64_t p = lo; p < hi && ci[p] < i; ++p) {",
+                            "for (int64_t p = lo; p < hi && ci[p] <= i; ++p) {"),
     "level_off_by_one": ("if (j < i && depth[j] + 1 > d) d = depth[j] + 1;",
                          "if (j < i && depth[j] + 2 > d) d = depth[j] + 2;"),
-    "zero_pivot_accepted": ("if (dp < 0 || v[dp] == (T)0) return ORACLE_SINGULAR;",
-                            "if (dp < 0) return ORACLE_SINGULAR;"),
+    "zero_pivot_accepted": ("if (pk < 0 || v[pk] == (T)0) {", "if (pk < 0) {"),
+    "positions_not_cleared": ("for (int64_t p = lo; p < hi; ++p) slot[ci[p]] = -1;",
+                              "(void)0;"),
+    "fill_in_added_to_diagonal": ("if (t < 0) continue;",
+                                  "if (t < 0) { v[diag[i]] = v[diag[i]] - l_ik * v[q]; continue; }"),
 }
 
 

@@ -6,7 +6,11 @@ One step = one C = alpha * A * B + beta * C product through the C ABI
 resident in HBM.  The L2 is flushed (a 2x-L2 buffer is written) before every
 timed step so that B, A and C start in HBM, as the byte model assumes.
 Each step is timed with CUDA events on the launching stream; ``value`` is
-GFLOP/s over the K timed steps.  Under torchrun every rank runs its own
+GFLOP/s over the K timed steps.  The default workload is the wide-N integer
+product (m = k = 262,144, n = 512: the largest of the five product
+configurations); the line's ``configs`` object times all five in the same
+process (per call, L2 flushed before each), with the roofline fraction of
+each call and of its dominant kernel.  Under torchrun every rank runs its own
 replica of the workload (the product does not shard here), timing is the max
 over ranks and ``value`` counts the work of all ranks.
 
@@ -35,7 +39,10 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "SpMM GFLOP/s (2·nnz·N) and achieved HBM GB/s vs ~8 TB/s peak, 1×GB300"
-DEFAULT_WORKLOAD = "seacells_knn"
+DEFAULT_WORKLOAD = "wide_n_integer"
+# the five product configurations, timed together in the `configs` object
+PRODUCT_CONFIGS = ("tiny_uniform", "seacells_knn", "power_law_1m", "laplacian_707",
+                   "wide_n_integer")
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -48,6 +55,8 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip timing the five product configurations in the same process")
     return ap.parse_args()
 
 
@@ -204,6 +213,111 @@ def problem_bytes(p):
     csr = 4 * (p.m + 1) + (4 + es) * p.nnz
     mn = es * p.m * p.n
     return 2 * csr + mn + 2 * mn + mn * (2 if p.beta != 0.0 else 1)
+
+
+def fp64_pipe_ops(p):
+    """Binary64 arithmetic instructions one product issues: an FMA per stored
+    entry and column, then per output element the epilogue's FMA (or the
+    multiply alpha * acc when beta == 0) and, unless beta is 0 or +-1, the
+    multiply beta * C."""
+    extra = 0 if p.beta in (0.0, 1.0, -1.0) else 1
+    return p.nnz * p.n + p.m * p.n * (1 + extra)
+
+
+def roofline_of(p, kbytes, kernel_ms, hbm_peak, fma_rate):
+    """The binding roofline of the dominant kernel: HBM bytes against the
+    measured copy bandwidth, and for binary64 also the FP64 pipe (FMA-rate
+    instructions against the measured binary64 FMA rate); the larger
+    fraction names the bound."""
+    gbs = kbytes / (kernel_ms / 1e3) / 1e9
+    out = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+           "frac": round(gbs / hbm_peak, 4), "hbm_frac": round(gbs / hbm_peak, 4)}
+    if p.values.dtype.itemsize == 8 and fma_rate:
+        ops = fp64_pipe_ops(p)
+        tflops = 2.0 * ops / (kernel_ms / 1e3) / 1e12
+        peak_t = 2.0 * fma_rate / 1e12
+        out["fp64_frac"] = round(tflops / peak_t, 4)
+        out["fp64_tflops"] = round(tflops, 4)
+        out["fp64_peak_tflops"] = round(peak_t, 4)
+        if out["fp64_frac"] > out["hbm_frac"]:
+            out.update({"bound": "alu", "achieved": round(tflops, 4), "peak": round(peak_t, 4),
+                        "unit": "TFLOP/s", "frac": out["fp64_frac"],
+                        "alu": "binary64 FMA pipe (FMA per entry and column, epilogue)"})
+    return out
+
+
+def time_product_configs(torch, dev, hbm_peak, fma_rate, calls=20):
+    """Every product configuration in this process, one at a time, through
+    the C ABI: per call (CUDA events, 2x L2 flushed before each call, the
+    median of `calls`), the per-stage kernel times of profiled calls, the
+    algorithmic bytes, and the roofline fraction of the whole call and of the
+    dominant (rows) kernel."""
+    import numpy as np
+
+    import csr_spmm_gb300 as cs
+    from synth import workloads
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+    out = {}
+    h = cs.Handle(dev.index if dev.index is not None else 0)
+    try:
+        for name in PRODUCT_CONFIGS:
+            p = workloads.WORKLOADS[name]()
+            t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+            rp, ci, va, B = t(p.row_ptr), t(p.col_idx), t(p.values), t(p.B)
+            C0 = t(p.C0) if p.C0 is not None else None
+            C = torch.empty((p.m, p.ldc), dtype=va.dtype, device=dev)
+            f32 = p.values.dtype == np.float32
+            fn = cs.spmm_csr_f32 if f32 else cs.spmm_csr_f64
+
+            def call():
+                fn(h.ptr, p.alpha, rp.data_ptr(), ci.data_ptr(), va.data_ptr(), p.m, p.k,
+                   B.data_ptr(), p.ldb, p.n, p.beta, C.data_ptr(), p.ldc, sptr)
+
+            def timed(n_calls, profiled):
+                cs.spmm_set_profiling(h.ptr, profiled)
+                ms, profs = [], []
+                for j in range(-3, n_calls):
+                    if C0 is not None:
+                        C.copy_(C0)
+                    flush.zero_()
+                    a_ev = torch.cuda.Event(enable_timing=True)
+                    b_ev = torch.cuda.Event(enable_timing=True)
+                    a_ev.record(stream)
+                    call()
+                    b_ev.record(stream)
+                    b_ev.synchronize()
+                    if j >= 0:
+                        ms.append(a_ev.elapsed_time(b_ev))
+                        if profiled:
+                            profs.append(cs.spmm_get_profile(h.ptr))
+                cs.spmm_set_profiling(h.ptr, False)
+                return ms, profs
+
+            ms, _ = timed(calls, False)
+            _, profs = timed(max(5, calls // 2), True)
+            per_call = statistics.median(ms)
+            stage = {k: round(statistics.mean(pr[k] for pr in profs), 5)
+                     for k in ("prepass_ms", "rows_ms", "long_ms")}
+            alg = p.algorithmic_bytes()
+            kbytes = rows_kernel_bytes(p, profs[-1])
+            entry = {"ms_per_call": round(per_call, 5), "ms_per_call_min": round(min(ms), 5),
+                     "gflops": round(p.flops() / (per_call / 1e3) / 1e9, 2),
+                     "algorithmic_bytes": int(alg),
+                     "hbm_gbs": round(alg / (per_call / 1e3) / 1e9, 1),
+                     "frac": round(alg / (per_call / 1e3) / 1e9 / hbm_peak, 4),
+                     "dtype": "f32" if f32 else "f64", "nnz": p.nnz, "n": p.n,
+                     "stage_ms_profiled": stage,
+                     "rows_kernel": roofline_of(p, kbytes, stage["rows_ms"], hbm_peak, fma_rate)}
+            out[name] = entry
+            del rp, ci, va, B, C0, C
+            torch.cuda.empty_cache()
+    finally:
+        h.close()
+    return out
 
 
 def oracle_rows(p, rows):
@@ -517,9 +631,13 @@ def run_ours(args):
         # chain's algorithmic bytes
         rows_ms += statistics.mean(pr["long_ms"] for pr in profs)
         kbytes = problem_bytes(p)
-    achieved = kbytes / (rows_ms / 1e3) / 1e9
     traffic = recorded_traffic(p.name)
     launches = int(sum(pr["launches"] for pr in profs))
+    # the binary64 FMA rate the FP64-bound products are set against (measured
+    # here, outside every timed region)
+    need_fma = p.values.dtype.itemsize == 8 or (world == 1 and not args.no_configs)
+    fma_rate = cs.spmm_measure_fp64_fma_rate(h.ptr) if need_fma else None
+    roof = roofline_of(p, kbytes, rows_ms, peak, fma_rate)
 
     # ---- end to end through the public API with host buffers ----
     e2e = None
@@ -573,6 +691,10 @@ def run_ours(args):
                "ms_per_step_one_stream": round(e_ms / e_steps, 4)}
     h.close()
 
+    configs = None
+    if world == 1 and not args.no_configs:
+        configs = time_product_configs(torch, dev, peak, fma_rate)
+
     if rank != 0:
         if pg:
             pg.destroy_process_group()
@@ -602,12 +724,14 @@ def run_ours(args):
                                                        "rows_long", "long_nnz")},
                    "stage_ms": {k: round(statistics.mean(pr[k] for pr in profs), 5)
                                 for k in ("prepass_ms", "rows_ms", "long_ms", "fixup_ms")}},
-        "roofline": {"bound": "hbm",
-                     "kernel": "rows_kernel (both products)" if chain else "rows_kernel",
-                     "achieved": round(achieved, 1),
-                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "algorithmic_bytes_per_launch": int(kbytes)},
+        "roofline": dict(roof, **{
+            "kernel": "rows_kernel (both products)" if chain else "rows_kernel",
+            "peak_kind": peak_kind if roof["bound"] == "hbm"
+            else "binary64 FMA rate measured in this run (spmm_measure_fp64_fma_rate)",
+            "hbm_peak": peak, "hbm_peak_kind": peak_kind, "traffic": traffic,
+            "algorithmic_bytes_per_launch": int(kbytes)}),
+        "configs": configs,
+        "fp64_fma_per_s": fma_rate,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,

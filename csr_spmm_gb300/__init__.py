@@ -20,7 +20,7 @@ from ._lib import (EXPORTED, SPMM_ERR_ALLOC, SPMM_ERR_CUDA, SPMM_ERR_DIMENSION_M
                    spmm_destroy, spmm_get_profile, spmm_plan_create, spmm_plan_csr_f32,
                    spmm_plan_csr_f64, spmm_plan_csr_squared_f32, spmm_plan_csr_squared_f64,
                    spmm_plan_destroy, spmm_plan_order_rows,
-                   spmm_row_order_bfs, spmm_set_l2_persistence,
+                   spmm_row_order_bfs, spmm_set_l2_persistence, spmm_measure_fp64_fma_rate,
                    spmm_csr_squared_f32, spmm_csr_squared_f64, spmm_fw_argmin,
                    spmm_ilu0, ILU0_SINGULAR, ILU0_WAIT_TIMEOUT,
                    spmm_reserve, spmm_set_profiling, status_string)
@@ -33,7 +33,7 @@ __all__ = ["Handle", "spmm", "csr_check", "SpmmError", "library", "spmm_create",
            "spmm_fw_argmin", "fw_argmin", "spmm_ilu0", "ilu0", "Ilu0Error",
            "spmm_plan_csr_f64", "spmm_plan_order_rows", "spmm_row_order_bfs",
            "spmm_plan_csr_squared_f32", "spmm_plan_csr_squared_f64", "Plan",
-           "EXPORTED"]
+           "spmm_measure_fp64_fma_rate", "EXPORTED"]
 
 
 class Handle:

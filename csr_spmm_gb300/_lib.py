@@ -31,7 +31,7 @@ EXPORTED = ("spmm_create", "spmm_destroy", "spmm_reserve", "spmm_csr_f32", "spmm
             "spmm_fw_argmin_f32", "spmm_fw_argmin_f64", "spmm_ilu0_f32", "spmm_ilu0_f64",
             "spmm_plan_create", "spmm_plan_destroy", "spmm_plan_csr_f32", "spmm_plan_csr_f64",
             "spmm_plan_order_rows", "spmm_row_order_bfs", "spmm_plan_csr_squared_f32",
-            "spmm_plan_csr_squared_f64", "spmm_status_string")
+            "spmm_plan_csr_squared_f64", "spmm_measure_fp64_fma_rate", "spmm_status_string")
 
 
 class SpmmProfile(ctypes.Structure):
@@ -64,6 +64,13 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
     global _lib
     if _lib is not None:
         return _lib
+    _lib = load_library(path)
+    return _lib
+
+
+def load_library(path: str) -> ctypes.CDLL:
+    """Load a build of the library from `path` (a variant built with other
+    -D flags, for tests) with the C signatures declared; not cached."""
     if not os.path.exists(path):
         raise ImportError(
             f"CUDA library not built: {path} is missing. Run `python -m csr_spmm_gb300.build` "
@@ -107,6 +114,8 @@ def library(path: str = LIB_PATH) -> ctypes.CDLL:
         fn.restype = st
     lib.spmm_set_l2_persistence.argtypes = [vp, i64]
     lib.spmm_set_l2_persistence.restype = st
+    lib.spmm_measure_fp64_fma_rate.argtypes = [vp, ctypes.POINTER(ctypes.c_double)]
+    lib.spmm_measure_fp64_fma_rate.restype = st
     lib.spmm_plan_create.argtypes = [vp, ctypes.POINTER(vp), vp, i64, i64, i64, ctypes.c_int, vp]
     lib.spmm_plan_create.restype = st
     lib.spmm_plan_destroy.argtypes = [vp]
@@ -269,6 +278,15 @@ def spmm_plan_csr_f64(plan, alpha, row_ptr, col_idx, values, B, ldb, beta, C, ld
     if check:
         _check(s, "spmm_plan_csr_f64")
     return s
+
+
+def spmm_measure_fp64_fma_rate(handle) -> float:
+    """The device's binary64 FMA instructions per second (a measurement aid;
+    synchronises)."""
+    out = ctypes.c_double(0.0)
+    _check(library().spmm_measure_fp64_fma_rate(handle, ctypes.byref(out)),
+           "spmm_measure_fp64_fma_rate")
+    return out.value
 
 
 def spmm_set_l2_persistence(handle, nbytes) -> None:

@@ -53,13 +53,25 @@ def _digest(units, deps, extra) -> str:
     return h.hexdigest()
 
 
-def build(verbose: bool = False, force: bool = False, extra_flags=(), out: str = LIB) -> str:
+def build(verbose: bool = False, force: bool = False, extra_flags=(), out: str = LIB,
+          flag_units=None) -> str:
     """Compile and link the library if anything changed; return its path.
 
     ``extra_flags`` (e.g. -D tuning macros) and ``out`` build a variant
-    library elsewhere, with its own object directory."""
+    library elsewhere, with its own object directory.  With ``flag_units``
+    (names of .cu files) only those units are compiled with ``extra_flags``;
+    the others are linked from the library's own objects, which are brought
+    up to date first."""
     units, deps = _sources()
-    digest = _digest(units, deps, extra_flags)
+    if flag_units is not None:
+        flag_units = sorted(flag_units)
+        missing = [u for u in flag_units if u not in units]
+        if missing:
+            raise ValueError(f"no such units: {missing}")
+        if out == LIB:
+            raise ValueError("a build restricted to some units needs its own output path")
+        build(verbose=verbose)
+    digest = _digest(units, deps, list(extra_flags) + ["units:"] + list(flag_units or []))
     stamp = out + ".sha256"
     obj_dir = OBJ_DIR if out == LIB else out + ".objs"
     if not force and os.path.exists(out) and os.path.exists(stamp):
@@ -71,6 +83,8 @@ def build(verbose: bool = False, force: bool = False, extra_flags=(), out: str =
     os.makedirs(os.path.dirname(out), exist_ok=True)
 
     def compile_one(unit):
+        if flag_units is not None and unit not in flag_units:
+            return os.path.join(OBJ_DIR, unit[:-3] + ".o")      # the library's own object
         obj = os.path.join(obj_dir, unit[:-3] + ".o")
         cmd = [nvcc] + NVCC_FLAGS + list(extra_flags) + ["-c", os.path.join(CSRC, unit), "-o", obj]
         if verbose:

@@ -57,7 +57,7 @@ struct spmm_plan_s {
     int hdr_host[HDR_WORDS] = {};     // bin counts, read back once
 };
 
-namespace {
+namespace spmm {
 
 // Fraction of L2 a B column panel may occupy; panels are only used when B
 // itself exceeds PANEL_TRIGGER of L2.
@@ -82,6 +82,69 @@ constexpr int LONG_MIN_ROW = SPMM_LONG_MIN_ROW;
 #define SPMM_LONG_CTAS 4
 #endif
 constexpr int LONG_CTAS_PER_SM = SPMM_LONG_CTAS;
+
+int long_grid_for(int num_sms) { return LONG_CTAS_PER_SM * num_sms; }
+
+// Geometry for a product with k x n B of element size es on a device with
+// l2_bytes of L2; `vec` when B and C allow 16-byte accesses (base pointers
+// and leading dimensions).
+ProductPlan plan_product(int64_t l2_bytes, int64_t k, int64_t n, int es, bool vec) {
+    const int WV = 16 / es;
+    ProductPlan P{};
+    P.geo.W = vec ? WV : 1;
+    const int W = P.geo.W;
+
+    // column panels: keep the B panel being gathered resident in L2
+    int64_t panel = n;
+    const double bbytes = (double)k * (double)n * es;
+    if (l2_bytes > 0 && bbytes > PANEL_TRIGGER * (double)l2_bytes) {
+        const int64_t align = std::max<int64_t>(W, 128 / es);      // whole 128-byte lines
+        int64_t cols = (int64_t)(PANEL_FRACTION * (double)l2_bytes / ((double)k * es));
+        cols = cols / align * align;
+        if (cols < align) cols = std::max<int64_t>(W, align);
+        const int64_t np = (n + cols - 1) / cols;
+        panel = (n + np - 1) / np;
+        panel = (panel + W - 1) / W * W;
+    }
+    if (SPMM_PANEL_COLS > 0) panel = (SPMM_PANEL_COLS + W - 1) / W * W;
+    P.panel_cols = (int)std::min<int64_t>(panel, n);
+    P.npanels = (int)((n + P.panel_cols - 1) / P.panel_cols);
+
+    const int nvec = (P.panel_cols + W - 1) / W;
+    if (nvec <= 32) {
+        int g = 1;
+        while (g < nvec) g <<= 1;
+        P.geo.G = g;
+        P.geo.R = 1;
+    } else {
+        P.geo.G = 32;
+        P.geo.R = nvec <= 64 ? 2 : 4;
+    }
+    P.geo.whole = (n % W) == 0;
+    // Bin thresholds: those of the 16-byte geometry whatever the operands'
+    // alignment, so that the bins, and with them the summation order of every
+    // row, depend only on the row lengths, n and the element size.  A plan
+    // (binned once, for 16-byte operands) then gives the direct call's
+    // results bit for bit for any alignment; any threshold is correct for
+    // every geometry.
+    if (!vec) {
+        const ProductPlan V = plan_product(l2_bytes, k, n, es, true);
+        P.short_max = V.short_max;
+        P.long_min = V.long_min;
+        return P;
+    }
+    const int bytes_per_entry = P.geo.R * W * es;
+    const int batch_bytes = es == 8 ? SPMM_BATCH_BYTES_F64 : SPMM_BATCH_BYTES;
+    const int U = std::min(SPMM_BATCH_MAX, std::max(1, batch_bytes / bytes_per_entry));
+    const int CH = std::max(P.geo.G, U);
+    P.long_min = LONG_MIN_ROW;
+    P.short_max = (P.geo.G == 32) ? P.long_min - 1 : std::min(P.long_min - 1, 2 * CH);
+    return P;
+}
+
+}  // namespace spmm
+
+namespace {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -111,7 +174,7 @@ ScratchLayout layout_for(int64_t m, int64_t n, int es, int long_grid) {
     return L;
 }
 
-int long_grid_of(const spmm_handle_s* h) { return LONG_CTAS_PER_SM * h->num_sms; }
+int long_grid_of(const spmm_handle_s* h) { return long_grid_for(h->num_sms); }
 
 spmm_status_t ensure_scratch(spmm_handle_s* h, size_t bytes) {
     if (bytes <= h->scratch_bytes) return SPMM_OK;
@@ -133,66 +196,10 @@ spmm_status_t ensure_scratch(spmm_handle_s* h, size_t bytes) {
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-struct Plan {
-    Geometry geo;
-    int panel_cols;
-    int npanels;
-    int short_max;
-    int long_min;
-};
+using Plan = ProductPlan;
 
-// Geometry for a product with k x n B of element size es; `vec` when B and C
-// allow 16-byte accesses (base pointers and leading dimensions).
 Plan make_plan_es(const spmm_handle_s* h, int64_t k, int64_t n, int es, bool vec) {
-    const int WV = 16 / es;
-    Plan P{};
-    P.geo.W = vec ? WV : 1;
-    const int W = P.geo.W;
-
-    // column panels: keep the B panel being gathered resident in L2
-    int64_t panel = n;
-    const double bbytes = (double)k * (double)n * es;
-    if (h->l2_bytes > 0 && bbytes > PANEL_TRIGGER * (double)h->l2_bytes) {
-        const int64_t align = std::max<int64_t>(W, 128 / es);      // whole 128-byte lines
-        int64_t cols = (int64_t)(PANEL_FRACTION * (double)h->l2_bytes / ((double)k * es));
-        cols = cols / align * align;
-        if (cols < align) cols = std::max<int64_t>(W, align);
-        const int64_t np = (n + cols - 1) / cols;
-        panel = (n + np - 1) / np;
-        panel = (panel + W - 1) / W * W;
-    }
-    if (SPMM_PANEL_COLS > 0) panel = (SPMM_PANEL_COLS + W - 1) / W * W;
-    P.panel_cols = (int)std::min<int64_t>(panel, n);
-    P.npanels = (int)((n + P.panel_cols - 1) / P.panel_cols);
-
-    const int nvec = (P.panel_cols + W - 1) / W;
-    if (nvec <= 32) {
-        P.geo.G = next_pow2(nvec);
-        P.geo.R = 1;
-    } else {
-        P.geo.G = 32;
-        P.geo.R = nvec <= 64 ? 2 : 4;
-    }
-    P.geo.whole = (n % W) == 0;
-    // Bin thresholds: those of the 16-byte geometry whatever the operands'
-    // alignment, so that the bins, and with them the summation order of every
-    // row, depend only on the row lengths, n and the element size.  A plan
-    // (binned once, for 16-byte operands) then gives the direct call's
-    // results bit for bit for any alignment; any threshold is correct for
-    // every geometry.
-    if (!vec) {
-        const Plan V = make_plan_es(h, k, n, es, true);
-        P.short_max = V.short_max;
-        P.long_min = V.long_min;
-        return P;
-    }
-    const int bytes_per_entry = P.geo.R * W * es;
-    const int batch_bytes = es == 8 ? SPMM_BATCH_BYTES_F64 : SPMM_BATCH_BYTES;
-    const int U = std::min(SPMM_BATCH_MAX, std::max(1, batch_bytes / bytes_per_entry));
-    const int CH = std::max(P.geo.G, U);
-    P.long_min = LONG_MIN_ROW;
-    P.short_max = (P.geo.G == 32) ? P.long_min - 1 : std::min(P.long_min - 1, 2 * CH);
-    return P;
+    return plan_product(h->l2_bytes, k, n, es, vec);
 }
 
 template <typename T>
@@ -931,6 +938,49 @@ spmm_status_t spmm_csr_check(spmm_handle_t h, const int32_t* row_ptr, const int3
     }
     *host_status = status;
     return status == 0 ? SPMM_OK : SPMM_ERR_INVALID_CSR;
+}
+
+spmm_status_t spmm_measure_fp64_fma_rate(spmm_handle_t h, double* fma_per_second) {
+    if (!h) return SPMM_ERR_INVALID_ARGUMENT;
+    if (!fma_per_second) return SPMM_ERR_NULL_POINTER;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device) {
+        cudaGetLastError();
+        return SPMM_ERR_INVALID_ARGUMENT;
+    }
+    // 32 warps per SM, 8 independent chains per thread: enough FMAs in flight
+    // to cover the pipe's latency
+    const int grid = 4 * h->num_sms;
+    const int iters = 2048;
+    spmm_status_t s = ensure_scratch(h, (size_t)grid * 256 * sizeof(double));
+    if (s != SPMM_OK) return s;
+    double* sink = static_cast<double*>(h->scratch);
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+        cudaGetLastError();
+        if (e0) cudaEventDestroy(e0);
+        return SPMM_ERR_CUDA;
+    }
+    cudaStream_t st = nullptr;
+    int64_t fmas = 0;
+    double best = 0.0;
+    bool ok = launch_fp64_fma_probe(grid, iters, sink, st, &fmas) == cudaSuccess;   // warm-up
+    for (int rep = 0; ok && rep < 3; ++rep) {
+        ok = cudaEventRecord(e0, st) == cudaSuccess &&
+             launch_fp64_fma_probe(grid, iters, sink, st, &fmas) == cudaSuccess &&
+             cudaEventRecord(e1, st) == cudaSuccess && cudaEventSynchronize(e1) == cudaSuccess;
+        float ms = 0.0f;
+        if (ok) ok = cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess && ms > 0.0f;
+        if (ok) best = std::max(best, (double)fmas / (ms * 1e-3));
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    if (!ok) {
+        cudaGetLastError();
+        return SPMM_ERR_CUDA;
+    }
+    *fma_per_second = best;
+    return SPMM_OK;
 }
 
 spmm_status_t spmm_set_profiling(spmm_handle_t h, int enable) {

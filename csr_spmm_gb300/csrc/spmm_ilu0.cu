@@ -38,7 +38,20 @@ namespace {
 
 constexpr int ILU0_SINGULAR = 1;
 constexpr int ILU0_WAIT_TIMEOUT = 2;
-constexpr int ILU0_SPIN_LIMIT = 1 << 22;       // polls of one queue slot (about a second)
+// Polls of one queue slot with no row finished anywhere before a wait gives
+// up (about a second at the default).
+#ifndef SPMM_ILU0_SPIN_LIMIT
+#define SPMM_ILU0_SPIN_LIMIT (1 << 22)
+#endif
+constexpr int ILU0_SPIN_LIMIT = SPMM_ILU0_SPIN_LIMIT;
+// Test builds only (0 in the library): the last row gets one extra pending
+// dependency that no row counts down, so it is never queued and the waits for
+// it run out.  This reaches the wait-timeout status with valid input and no
+// fault: every other row is factored, the waits end by their limit, and the
+// kernel returns.
+#ifndef SPMM_ILU0_TEST_WITHHOLD_LAST_ROW
+#define SPMM_ILU0_TEST_WITHHOLD_LAST_ROW 0
+#endif
 #ifndef SPMM_ILU0_SLEEP_NS
 #define SPMM_ILU0_SLEEP_NS 128
 #endif
@@ -92,8 +105,9 @@ __global__ void __launch_bounds__(256) ilu0_count(Ilu0Params<T> p) {
             }
         p.piv[q] = make_int2(dp, ke);
     }
-    p.pending[i] = lower;
-    if (lower == 0) p.queue[atomicAdd(p.tail, 1)] = i;
+    const int withheld = (SPMM_ILU0_TEST_WITHHOLD_LAST_ROW && i == p.n - 1) ? 1 : 0;
+    p.pending[i] = lower + withheld;
+    if (lower + withheld == 0) p.queue[atomicAdd(p.tail, 1)] = i;
 }
 
 // 2. exclusive prefix sum of cnt into dep_ptr (one block; each thread owns a

@@ -167,6 +167,21 @@ struct L2Window {
     float hit_ratio;
 };
 
+// Geometry, column panels and bin thresholds of one product, chosen on the
+// host from the operands' shape and alignment and the device's L2 size
+// (spmm_api.cu).  Every entry point that launches the product takes its plan
+// from here, so equal inputs are binned and summed the same way everywhere.
+struct ProductPlan {
+    Geometry geo;
+    int panel_cols;   // columns per L2 panel of B / C
+    int npanels;
+    int short_max;    // longest row of the short bin
+    int long_min;     // shortest row of the long bin
+};
+ProductPlan plan_product(int64_t l2_bytes, int64_t k, int64_t n, int es, bool vec);
+// CTAs of the long-row launch on a device with num_sms SMs.
+int long_grid_for(int num_sms);
+
 // ---- pre-pass (spmm_bin.cu) ----
 // `overlap`: launch the dependent kernels of the chain with programmatic
 // dependent launch (the first kernel of a call always waits for the stream).
@@ -186,6 +201,10 @@ template <typename T>
 cudaError_t launch_scale(T* C, int64_t ldc, int m, int n, T beta, int grid, cudaStream_t st);
 cudaError_t launch_csr_check(const int* row_ptr, const int* col_idx, int64_t m, int64_t k,
                              int64_t nnz, int* status, cudaStream_t st);
+// Binary64 FMA throughput probe: `grid` blocks of 256 threads, grid * 256
+// doubles of sink; *fmas receives the FMA instructions one launch executes.
+cudaError_t launch_fp64_fma_probe(int grid, int iters, double* sink, cudaStream_t st,
+                                  int64_t* fmas);
 
 // Blocks per SM the rows kernel reaches for this geometry (occupancy query).
 template <typename T>

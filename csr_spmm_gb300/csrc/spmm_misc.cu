@@ -1,5 +1,6 @@
 // Epilogue-only kernel (alpha == 0 or k == 0: C = beta * C, C write-only when
-// beta == 0) and the CSR structure check.
+// beta == 0), the CSR structure check, and the binary64 FMA throughput probe
+// that the measurement of binary64 products is set against.
 #include "spmm_internal.h"
 
 namespace spmm {
@@ -39,7 +40,33 @@ csr_check_kernel(const int* __restrict__ row_ptr, const int* __restrict__ col_id
     if (bits) atomicOr(status, bits);
 }
 
+// Binary64 FMA throughput: each thread runs FMA_CHAINS independent chains of
+// dependent fma.rn.f64 (a = a * x + y, x and y known only at run time) for
+// `iters` steps; the chains' sum is stored so that no work is dead.
+constexpr int FMA_CHAINS = 8;
+__global__ void __launch_bounds__(256) fp64_fma_probe(double x, double y, int iters,
+                                                      double* __restrict__ sink) {
+    double a[FMA_CHAINS];
+#pragma unroll
+    for (int j = 0; j < FMA_CHAINS; ++j) a[j] = 1e-9 * threadIdx.x + j;
+#pragma unroll 4
+    for (int it = 0; it < iters; ++it)
+#pragma unroll
+        for (int j = 0; j < FMA_CHAINS; ++j) a[j] = fma(a[j], x, y);
+    double sum = 0.0;
+#pragma unroll
+    for (int j = 0; j < FMA_CHAINS; ++j) sum += a[j];
+    sink[(int64_t)blockIdx.x * blockDim.x + threadIdx.x] = sum;
+}
+
 }  // namespace
+
+cudaError_t launch_fp64_fma_probe(int grid, int iters, double* sink, cudaStream_t st,
+                                  int64_t* fmas) {
+    fp64_fma_probe<<<grid, 256, 0, st>>>(0.999999999, 1e-12, iters, sink);
+    *fmas = (int64_t)grid * 256 * FMA_CHAINS * iters;
+    return cudaGetLastError();
+}
 
 template <typename T>
 cudaError_t launch_scale(T* C, int64_t ldc, int m, int n, T beta, int grid, cudaStream_t st) {

@@ -26,7 +26,7 @@ namespace {
 // Limits of the static scratch (see include/csr_spmm.h).
 constexpr int64_t NOALLOC_MAX_ROWS = 1 << 19;      // m <= 524,288
 constexpr int64_t NOALLOC_MAX_COLS = 512;          // n <= 512
-constexpr int NOALLOC_LONG_GRID_MAX = 640;         // 4 CTAs per SM for up to 160 SMs
+constexpr int NOALLOC_LONG_GRID_MAX = 640;         // the long-row grid of up to 160 SMs
 
 constexpr size_t al256(size_t x) { return (x + 255) / 256 * 256; }
 constexpr int64_t NOALLOC_TILES = (NOALLOC_MAX_ROWS + BIN_TILE - 1) / BIN_TILE;
@@ -51,6 +51,10 @@ struct DeviceSetup {
     unsigned char* scratch = nullptr;    // device address of g_noalloc_scratch
     int num_sms = 0;
     int64_t l2_bytes = 0;
+    // rows-kernel blocks per SM by geometry (an occupancy query, made once)
+    struct Occ { int W, G, R, blocks; };
+    Occ occ[16];
+    int nocc = 0;
 };
 constexpr int MAX_DEVICES = 64;
 DeviceSetup g_setup[MAX_DEVICES];
@@ -69,7 +73,9 @@ spmm_status_t setup_device(int dev, DeviceSetup** out) {
             cudaGetLastError();
             return SPMM_ERR_CUDA;
         }
-        s.supported = (major == 10 && minor == 3);
+        // the static partial sums hold NOALLOC_LONG_GRID_MAX long-row CTAs, the
+        // handle path's long-row grid on devices of up to 160 SMs
+        s.supported = (major == 10 && minor == 3) && long_grid_for(sms) <= NOALLOC_LONG_GRID_MAX;
         if (s.supported) {
             // In host code g_noalloc_scratch names a host-side stand-in; the
             // device address is looked up here, with `dev` current.
@@ -91,10 +97,16 @@ spmm_status_t setup_device(int dev, DeviceSetup** out) {
 
 inline bool aligned16(const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
 
-inline int next_pow2(int x) {
-    int p = 1;
-    while (p < x) p <<= 1;
-    return p;
+// Rows-kernel blocks per SM for geometry g on this device (cached; the
+// first call with a geometry asks the occupancy calculator).
+int rows_blocks(DeviceSetup* ds, const Geometry& g) {
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    for (int i = 0; i < ds->nocc; ++i)
+        if (ds->occ[i].W == g.W && ds->occ[i].G == g.G && ds->occ[i].R == g.R)
+            return ds->occ[i].blocks;
+    const int b = rows_blocks_per_sm<float>(g);
+    if (ds->nocc < 16) ds->occ[ds->nocc++] = {g.W, g.G, g.R, b};
+    return b;
 }
 
 }  // namespace
@@ -130,49 +142,12 @@ extern "C" spmm_status_t spmm_csr_f32_noalloc(float alpha, const int32_t* row_pt
         return launch_scale<float>(C, ldc, (int)m, (int)n, beta, ds->num_sms * 8, st) == cudaSuccess
                    ? SPMM_OK : SPMM_ERR_CUDA;
 
-    // plan: vector width, one column panel (n <= 512 keeps k x n panels of
-    // small problems whole), lane groups, bin thresholds -- the same rules the
-    // handle path applies
-    struct Shape { Geometry geo; int panel_cols; };
-    auto shape_for = [&](int W) {
-        Shape sh{};
-        sh.geo.W = W;
-        int64_t panel = n;
-        const double bbytes = (double)k * (double)n * sizeof(float);
-        if (ds->l2_bytes > 0 && bbytes > 3.0 * (double)ds->l2_bytes) {
-            const int64_t align = std::max<int64_t>(W, 32);
-            int64_t cols = (int64_t)(0.5 * (double)ds->l2_bytes / ((double)k * sizeof(float)));
-            cols = cols / align * align;
-            if (cols < align) cols = align;
-            const int64_t np = (n + cols - 1) / cols;
-            panel = (n + np - 1) / np;
-            panel = (panel + W - 1) / W * W;
-        }
-        sh.panel_cols = (int)std::min<int64_t>(panel, n);
-        const int nvec = (sh.panel_cols + W - 1) / W;
-        if (nvec <= 32) {
-            sh.geo.G = next_pow2(nvec);
-            sh.geo.R = 1;
-        } else {
-            sh.geo.G = 32;
-            sh.geo.R = nvec <= 64 ? 2 : 4;
-        }
-        return sh;
-    };
+    // the handle path's plan (the same geometry, panels and bin thresholds),
+    // so the two entry points bin and sum every row alike
     const bool vec = aligned16(B) && aligned16(C) && ldb % 4 == 0 && ldc % 4 == 0;
-    const Shape sh = shape_for(vec ? 4 : 1);
-    const Geometry geo = sh.geo;
-    const int panel_cols = sh.panel_cols;
-    const int npanels = (int)((n + panel_cols - 1) / panel_cols);
-    // bin thresholds from the 16-byte geometry whatever the alignment (the
-    // bins then depend only on row lengths and n, as on the handle path)
-    const Geometry g16 = vec ? geo : shape_for(4).geo;
-    const int bytes_per_entry = g16.R * g16.W * (int)sizeof(float);
-    const int U = std::min(SPMM_BATCH_MAX, std::max(1, SPMM_BATCH_BYTES / bytes_per_entry));
-    const int CH = std::max(g16.G, U);
-    const int long_min = 1024;
-    const int short_max = g16.G == 32 ? long_min - 1 : std::min(long_min - 1, 2 * CH);
-    const int long_grid = std::min(4 * ds->num_sms, NOALLOC_LONG_GRID_MAX);
+    const ProductPlan P = plan_product(ds->l2_bytes, k, n, (int)sizeof(float), vec);
+    const Geometry geo = P.geo;
+    const int long_grid = long_grid_for(ds->num_sms);     // <= NOALLOC_LONG_GRID_MAX (set-up)
 
     BinScratch bs{};
     bs.hdr = reinterpret_cast<int*>(ds->scratch + OFF_HDR);
@@ -183,7 +158,8 @@ extern "C" spmm_status_t spmm_csr_f32_noalloc(float alpha, const int32_t* row_pt
     bs.long_cnt = reinterpret_cast<int*>(ds->scratch + OFF_LONG_CNT);
     bs.long_pre = reinterpret_cast<int*>(ds->scratch + OFF_LONG_PRE);
     bin_geometry(m, &bs.items, &bs.tiles);
-    if (launch_binning(row_ptr, (int)m, short_max, long_min, bs, st, SPMM_PDL) != cudaSuccess)
+    if (launch_binning(row_ptr, (int)m, P.short_max, P.long_min, bs, st, SPMM_PDL) !=
+        cudaSuccess)
         return SPMM_ERR_CUDA;
 
     SpmmParams<float> p{};
@@ -198,8 +174,8 @@ extern "C" spmm_status_t spmm_csr_f32_noalloc(float alpha, const int32_t* row_pt
     p.n = (int)n;
     p.alpha = alpha;
     p.beta = beta;
-    p.panel_cols = panel_cols;
-    p.npanels = npanels;
+    p.panel_cols = P.panel_cols;
+    p.npanels = P.npanels;
     p.rowlist = bs.rowlist;
     p.med_pre = bs.med_pre;
     p.long_cnt = bs.long_cnt;
@@ -207,7 +183,7 @@ extern "C" spmm_status_t spmm_csr_f32_noalloc(float alpha, const int32_t* row_pt
     p.hdr = bs.hdr;
     p.partials = reinterpret_cast<float*>(ds->scratch + OFF_PARTIALS);
     p.long_grid = long_grid;
-    const int grid = rows_blocks_per_sm<float>(geo) * ds->num_sms;
+    const int grid = rows_blocks(ds, geo) * ds->num_sms;
     if (launch_rows<float>(p, geo, grid, st, SPMM_PDL) != cudaSuccess) return SPMM_ERR_CUDA;
     if (launch_long<float>(p, geo, st, SPMM_PDL) != cudaSuccess) return SPMM_ERR_CUDA;
     return SPMM_OK;

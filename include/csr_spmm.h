@@ -368,6 +368,16 @@ spmm_status_t spmm_set_profiling(spmm_handle_t h, int enable);
  * launches == 1 and rows_ms == 0. */
 spmm_status_t spmm_get_profile(spmm_handle_t h, spmm_profile_t *out);
 
+/* Measurement aid (the pages have no counterpart): the device's binary64
+ * fused multiply-add rate, against which binary64 products are measured on
+ * parts whose FP64 units, not memory, bound them.  Runs a kernel in which
+ * every thread advances eight independent chains of fma.rn.f64 (32 warps per
+ * SM), times three launches after a warm-up with CUDA events on the legacy
+ * default stream, and writes the best rate in FMA instructions per second
+ * (one FMA = 2 flops) to *fma_per_second.  Synchronises the device; uses 8
+ * bytes of handle scratch per thread (1024 threads per SM). */
+spmm_status_t spmm_measure_fp64_fma_rate(spmm_handle_t h, double *fma_per_second);
+
 /* C = alpha * A * B + beta * C in binary32 without allocating anything.
  *
  * For callers that cannot call cudaMalloc: code running under a fixed or
@@ -389,7 +399,12 @@ spmm_status_t spmm_get_profile(spmm_handle_t h, spmm_profile_t *out);
  * the one array, which keeps the last call's contents: calls whose work
  * overlaps on the GPU (different streams, or different host threads) race and
  * must be serialised by the caller.  Nothing in the array needs to start at
- * zero.  Asynchronous on `stream`, like spmm_csr_f32. */
+ * zero.  Asynchronous on `stream`, like spmm_csr_f32.  The array's address
+ * is looked up once per device and kept: after cudaDeviceReset on a device
+ * the address may no longer be valid, so the entry point must not be called
+ * on that device again in the same process.  A device with more than 160
+ * SMs (more long-row CTAs than the array holds partial sums for) gets
+ * SPMM_ERR_UNSUPPORTED_DEVICE. */
 spmm_status_t spmm_csr_f32_noalloc(float alpha,
                                    const int32_t *row_ptr, const int32_t *col_idx,
                                    const float *values, int64_t m, int64_t k,

@@ -79,3 +79,23 @@ def test_reference_arm_line_on_cpu():
     assert d["steps"] == 2 and d["warmup"] == 1 and d["config"]["workload"] == "tiny_uniform"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
     assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_roofline_names_the_binding_unit():
+    """binary32 products are set against HBM; a binary64 product whose FP64
+    instruction rate is the larger fraction of its peak reports the ALU
+    bound, with both fractions on the line."""
+    from synth import laplacian_2d
+    p32 = uniform_rows(300, 200, 9, 4, seed=2, beta=0.5)
+    r = bench.roofline_of(p32, 1e9, 1.0, 6800.0, 6e11)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and "fp64_frac" not in r
+    assert abs(r["frac"] - 1e9 / 1e-3 / 1e9 / 6800.0) < 1e-4
+    p64 = laplacian_2d(20, 32, seed=3)                      # alpha = 2, beta = -1
+    # beta = -1: one FP64 instruction per entry and column, one per output
+    assert bench.fp64_pipe_ops(p64) == p64.nnz * 32 + p64.m * 32
+    ms = 2.0 * bench.fp64_pipe_ops(p64) / 1e12 * 1e3        # as if at 1 TFLOP/s
+    r = bench.roofline_of(p64, 1e3, ms, 6800.0, 0.6e12)     # peak 1.2 TFLOP/s
+    assert r["bound"] == "alu" and r["unit"] == "TFLOP/s"
+    assert abs(r["frac"] - 1.0 / 1.2) < 1e-3 and r["hbm_frac"] < r["frac"]
+    p64.beta = 0.5                                           # general beta: a multiply more
+    assert bench.fp64_pipe_ops(p64) == p64.nnz * 32 + 2 * p64.m * 32

@@ -320,6 +320,17 @@ def time_product_configs(torch, dev, hbm_peak, fma_rate, calls=20):
     return out
 
 
+def workload_config(p, world=1):
+    """The `config` object of a product workload's JSON line: what is
+    computed, on what, with which timing hygiene.  Both arms print the same
+    object; measured quantities go elsewhere on the line."""
+    return {"workload": p.name, "m": p.m, "k": p.k, "n": p.n, "nnz": p.nnz,
+            "alpha": p.alpha, "beta": p.beta, "algorithmic_bytes": problem_bytes(p),
+            "operation": "C = alpha*A(AB) + beta*C" if is_chain(p) else "C = alpha*AB + beta*C",
+            "l2_flush": "2x L2 buffer written before every timed step",
+            "parallelism": f"replicas x{world}"}
+
+
 def oracle_rows(p, rows):
     """The oracle on rows of the workload (all rows if None); returns its flops."""
     import numpy as np
@@ -415,14 +426,14 @@ def run_reference(args):
         times.append(time.perf_counter() - t0)
     total = sum(times)
     value = flops / total / 1e9
-    sample = f"{p.name}: every {stride}th row ({len(rows)} rows) per step, fp64 accumulation"
+    sample = (f"{p.name}: every {stride}th row ({len(rows)} rows) per step, fp64 "
+              "accumulation")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * total / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": p.name, "m": p.m, "k": p.k, "n": p.n, "nnz": p.nnz,
-                   "sampled_rows_per_step": int(len(rows))},
+        "config": workload_config(p, args.gpus),
         "cpu_baseline": {"value": round(value, 4), "unit": "GFLOP/s", "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
@@ -710,20 +721,16 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_ms, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
         "data": "synthetic",
-        "config": {"workload": p.name, "m": p.m, "k": p.k, "n": p.n, "nnz": p.nnz,
-                   "alpha": p.alpha, "beta": p.beta, "algorithmic_bytes": alg,
-                   "operation": "C = alpha*A(AB) + beta*C" if chain else "C = alpha*AB + beta*C",
-                   "l2_flush": "2x L2 buffer written before every timed step",
-                   "parallelism": f"replicas x{world}",
-                   "hbm_gbs_whole_call": round(alg / (mean_ms / 1e3) / 1e9, 1),
-                   "ms_per_call_unprofiled": round(unprofiled_ms, 5),
-                   "plan_ms_per_call": plan_ms,
-                   "plan": {k: profs[-1][k] for k in ("panels", "panel_cols", "vec_elems",
-                                                       "group_lanes", "slots", "short_max",
-                                                       "long_min", "rows_short", "rows_medium",
-                                                       "rows_long", "long_nnz")},
-                   "stage_ms": {k: round(statistics.mean(pr[k] for pr in profs), 5)
-                                for k in ("prepass_ms", "rows_ms", "long_ms", "fixup_ms")}},
+        "config": workload_config(p, world),
+        "details": {"hbm_gbs_whole_call": round(alg / (mean_ms / 1e3) / 1e9, 1),
+                    "ms_per_call_unprofiled": round(unprofiled_ms, 5),
+                    "plan_ms_per_call": plan_ms,
+                    "plan": {k: profs[-1][k] for k in ("panels", "panel_cols", "vec_elems",
+                                                        "group_lanes", "slots", "short_max",
+                                                        "long_min", "rows_short", "rows_medium",
+                                                        "rows_long", "long_nnz")},
+                    "stage_ms": {k: round(statistics.mean(pr[k] for pr in profs), 5)
+                                 for k in ("prepass_ms", "rows_ms", "long_ms", "fixup_ms")}},
         "roofline": dict(roof, **{
             "kernel": "rows_kernel (both products)" if chain else "rows_kernel",
             "peak_kind": peak_kind if roof["bound"] == "hbm"

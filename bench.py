@@ -607,9 +607,12 @@ def run_ours(args):
             pfn = cs.spmm_plan_csr_f32 if f32 else cs.spmm_plan_csr_f64
         plan = cs.spmm_plan_create(h.ptr, rp.data_ptr(), p.m, p.k, p.n, es, sptr)
         try:
-            for label in ("natural", "breadth_first"):
-                if label == "breadth_first":
-                    cs.spmm_plan_order_rows(plan, rp.data_ptr(), ci.data_ptr(), sptr)
+            for label in ("natural", "ordered"):
+                if label == "ordered":
+                    # breadth-first order where it raises B-row reuse
+                    applied = cs.spmm_plan_order_rows_auto(plan, rp.data_ptr(), ci.data_ptr(),
+                                                           sptr)
+                    plan_ms["ordered_rows"] = "breadth_first" if applied else "natural"
                 pev = [(torch.cuda.Event(enable_timing=True),
                         torch.cuda.Event(enable_timing=True)) for _ in range(min(args.steps, 50))]
                 for j in range(-3, len(pev)):

@@ -21,6 +21,7 @@ from ._lib import (EXPORTED, SPMM_ERR_ALLOC, SPMM_ERR_CUDA, SPMM_ERR_DIMENSION_M
                    spmm_plan_csr_f64, spmm_plan_csr_squared_f32, spmm_plan_csr_squared_f64,
                    spmm_plan_destroy, spmm_plan_order_rows,
                    spmm_row_order_bfs, spmm_set_l2_persistence, spmm_measure_fp64_fma_rate,
+                   spmm_plan_order_rows_auto,
                    spmm_csr_squared_f32, spmm_csr_squared_f64, spmm_fw_argmin,
                    spmm_ilu0, ILU0_SINGULAR, ILU0_WAIT_TIMEOUT,
                    spmm_reserve, spmm_set_profiling, status_string)
@@ -33,7 +34,7 @@ __all__ = ["Handle", "spmm", "csr_check", "SpmmError", "library", "spmm_create",
            "spmm_fw_argmin", "fw_argmin", "spmm_ilu0", "ilu0", "Ilu0Error",
            "spmm_plan_csr_f64", "spmm_plan_order_rows", "spmm_row_order_bfs",
            "spmm_plan_csr_squared_f32", "spmm_plan_csr_squared_f64", "Plan",
-           "spmm_measure_fp64_fma_rate", "EXPORTED"]
+           "spmm_measure_fp64_fma_rate", "spmm_plan_order_rows_auto", "EXPORTED"]
 
 
 class Handle:
@@ -198,11 +199,17 @@ class Plan:
         st = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
         self.ptr = spmm_plan_create(handle.ptr, _ptr(row_ptr), self.m, self.k, self.n, es, st)
 
-    def order_rows(self, row_ptr, col_idx, stream=None) -> None:
-        """Process rows in breadth-first order of A's pattern (spmm_plan_order_rows)."""
+    def order_rows(self, row_ptr, col_idx, stream=None, automatic=True) -> bool:
+        """Process rows in breadth-first order of A's pattern: where that raises
+        B-row reuse (spmm_plan_order_rows_auto, the default), or always
+        (automatic=False, spmm_plan_order_rows).  Returns whether the order
+        was changed."""
         import torch
         st = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+        if automatic:
+            return spmm_plan_order_rows_auto(self.ptr, _ptr(row_ptr), _ptr(col_idx), st)
         spmm_plan_order_rows(self.ptr, _ptr(row_ptr), _ptr(col_idx), st)
+        return True
 
     def __call__(self, alpha, row_ptr, col_idx, values, B, beta, C, stream=None) -> None:
         """C <- alpha * A * B + beta * C with A's structure from the plan."""

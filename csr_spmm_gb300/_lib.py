@@ -31,7 +31,8 @@ EXPORTED = ("spmm_create", "spmm_destroy", "spmm_reserve", "spmm_csr_f32", "spmm
             "spmm_fw_argmin_f32", "spmm_fw_argmin_f64", "spmm_ilu0_f32", "spmm_ilu0_f64",
             "spmm_plan_create", "spmm_plan_destroy", "spmm_plan_csr_f32", "spmm_plan_csr_f64",
             "spmm_plan_order_rows", "spmm_row_order_bfs", "spmm_plan_csr_squared_f32",
-            "spmm_plan_csr_squared_f64", "spmm_measure_fp64_fma_rate", "spmm_status_string")
+            "spmm_plan_csr_squared_f64", "spmm_measure_fp64_fma_rate", "spmm_plan_order_rows_auto",
+            "spmm_status_string")
 
 
 class SpmmProfile(ctypes.Structure):
@@ -114,6 +115,8 @@ def load_library(path: str) -> ctypes.CDLL:
         fn.restype = st
     lib.spmm_set_l2_persistence.argtypes = [vp, i64]
     lib.spmm_set_l2_persistence.restype = st
+    lib.spmm_plan_order_rows_auto.argtypes = [vp, vp, vp, vp, ctypes.POINTER(ctypes.c_int32)]
+    lib.spmm_plan_order_rows_auto.restype = st
     lib.spmm_measure_fp64_fma_rate.argtypes = [vp, ctypes.POINTER(ctypes.c_double)]
     lib.spmm_measure_fp64_fma_rate.restype = st
     lib.spmm_plan_create.argtypes = [vp, ctypes.POINTER(vp), vp, i64, i64, i64, ctypes.c_int, vp]
@@ -278,6 +281,15 @@ def spmm_plan_csr_f64(plan, alpha, row_ptr, col_idx, values, B, ldb, beta, C, ld
     if check:
         _check(s, "spmm_plan_csr_f64")
     return s
+
+
+def spmm_plan_order_rows_auto(plan, row_ptr, col_idx, stream=0) -> bool:
+    """Breadth-first row order for the plan where it raises B-row reuse;
+    returns whether the order was changed."""
+    out = ctypes.c_int32(0)
+    _check(library().spmm_plan_order_rows_auto(plan, row_ptr, col_idx, stream or None,
+                                               ctypes.byref(out)), "spmm_plan_order_rows_auto")
+    return bool(out.value)
 
 
 def spmm_measure_fp64_fma_rate(handle) -> float:

@@ -312,6 +312,19 @@ spmm_status_t spmm_plan_csr_squared_f64(spmm_plan_t plan, double alpha,
 spmm_status_t spmm_plan_order_rows(spmm_plan_t plan, const int32_t *row_ptr,
                                    const int32_t *col_idx, void *stream);
 
+/* The same reorder, kept only where it raises B-row reuse: over windows of 64
+ * consecutive list rows (about the rows one SM has in flight), the distinct
+ * B rows per stored entry must fall by at least a tenth in breadth-first
+ * order.  Otherwise (uniformly random columns, where the reorder only
+ * scatters the rows, or a numbering that is already local, like a row-major
+ * stencil) the lists are left as they are.  *applied (required) is set to 1
+ * when the order was changed, else 0.  Same arguments, errors and
+ * synchronisation as spmm_plan_order_rows; the reuse count adds O(nnz + k)
+ * host work. */
+spmm_status_t spmm_plan_order_rows_auto(spmm_plan_t plan, const int32_t *row_ptr,
+                                        const int32_t *col_idx, void *stream,
+                                        int32_t *applied);
+
 /* Host function (no GPU involved): order[i] = the i-th row of an m-row CSR
  * pattern (HOST arrays row_ptr[m + 1], col_idx[row_ptr[m]]) in breadth-first
  * order.  Row i is adjacent to row j for each stored entry (i, j) with

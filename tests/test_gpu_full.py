@@ -146,7 +146,7 @@ def test_full_seacells_plan_in_breadth_first_order(handle):
     C = torch.full((p.m, p.n), float("nan"), dtype=torch.float32, device=dev)
     plan = cs.Plan(handle, rp, p.k, p.n, torch.float32)
     try:
-        plan.order_rows(rp, ci)
+        assert plan.order_rows(rp, ci), "the kNN pattern should be reordered"
         for it, B in enumerate((p.B, p.B[::-1].copy())):
             plan(p.alpha, rp, ci, va, torch.from_numpy(B).to(dev), p.beta, C)
             torch.cuda.synchronize()

@@ -261,8 +261,30 @@ def test_plan_class_order_rows(handle):
     B = torch.from_numpy(p.B).to(dev)
     C = torch.empty(p.m, p.n, dtype=torch.float32, device=dev)
     plan = cs.Plan(handle, rp, p.k, p.n, torch.float32)
-    plan.order_rows(rp, ci)
+    assert plan.order_rows(rp, ci)              # a kNN pattern: the reorder is kept
     plan(p.alpha, rp, ci, va, B, p.beta, C)
     torch.cuda.synchronize()
     plan.close()
     assert_parity(p, C.cpu().numpy(), what="Plan class, ordered rows")
+
+
+@pytest.mark.parametrize("name,want", [("knn", True), ("power_law", False), ("tiny", False)])
+def test_plan_row_order_auto(handle, name, want):
+    """The automatic reorder keeps the breadth-first order only where it
+    raises B-row reuse (a kNN kernel pattern), leaves uniformly random
+    columns in their order, and either way the products equal the direct
+    call's bits."""
+    import torch
+    p = CASES[name]()
+    plan = _make_plan(handle, p)
+    try:
+        rp = torch.from_numpy(p.row_ptr).cuda()
+        ci = torch.from_numpy(p.col_idx).cuda()
+        applied = cs.spmm_plan_order_rows_auto(plan, rp.data_ptr(), ci.data_ptr(),
+                                              torch.cuda.current_stream().cuda_stream)
+        assert applied is want, name
+        direct, _ = run_problem(handle, p)
+        got = _plan_run(handle, plan, p)
+        assert np.array_equal(_bits(got[:, :p.n]), _bits(direct[:, :p.n])), name
+    finally:
+        cs.spmm_plan_destroy(plan)

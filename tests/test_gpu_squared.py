@@ -226,7 +226,7 @@ def test_plan_class_squared(handle):
     C = torch.empty(p.m, p.n, dtype=torch.float32, device=dev)
     plan = cs.Plan(handle, rp, p.k, p.n, torch.float32)
     try:
-        plan.order_rows(rp, ci)
+        assert plan.order_rows(rp, ci)
         plan.squared(p.alpha, rp, ci, va, B, p.beta, C)
         torch.cuda.synchronize()
     finally:

@@ -58,6 +58,15 @@ constexpr int ILU0_SPIN_LIMIT = SPMM_ILU0_SPIN_LIMIT;
 #ifndef SPMM_ILU0_POLL_EVERY
 #define SPMM_ILU0_POLL_EVERY 16        // a power of two
 #endif
+// A kept row was readied by this warp's own acquire-release count-down,
+// ordered before every lane's later loads by the warp barrier that ends the
+// count-down loop; 1 adds an acquire load of its counter by every lane.
+#ifndef SPMM_ILU0_KEPT_ACQUIRE
+#define SPMM_ILU0_KEPT_ACQUIRE 1
+#endif
+#ifndef SPMM_ILU0_FENCE
+#define SPMM_ILU0_FENCE 0              // 1: a full fence before the count-downs
+#endif
 #ifndef SPMM_ILU0_BLOCKS_PER_SM
 #define SPMM_ILU0_BLOCKS_PER_SM 1      // 0: as many as fit (measured slower: idle warps poll)
 #endif
@@ -353,7 +362,7 @@ __global__ void __launch_bounds__(ILU0_THREADS, 2) ilu0_factor(Ilu0Params<T> p) 
         const int d0 = p.dep_ptr[i], d1 = p.dep_ptr[i + 1];
         // a kept row: acquire the values its finished dependencies wrote (every
         // lane; the loads above are already in flight)
-        if (kept) ld_acquire(p.pending + i);
+        if (kept && SPMM_ILU0_KEPT_ACQUIRE) ld_acquire(p.pending + i);
         const bool short_row = e - s <= 32;
         int my_c = 0x7fffffff;
         T my_v = T(0);
@@ -372,8 +381,14 @@ __global__ void __launch_bounds__(ILU0_THREADS, 2) ilu0_factor(Ilu0Params<T> p) 
             ok = factor_row_long<T>(p, i, s, e, lane, dmax);
         if (!ok) return;
         if (p.depth && lane == 0) p.depth[i] = dmax + 1;
+        // Row i is final before it is counted down: every lane's stores are
+        // ordered before the warp barrier, and each count-down below is a
+        // release (acq_rel) atomic, which makes them visible to the warp whose
+        // acquiring count-down readies a dependent.  A separate fence here
+        // adds no ordering (measured on GB300, the 707 x 707 Laplacian: 8.38 ms
+        // with it, 7.17 ms without, bit for bit the same factors).
         __syncwarp();
-        __threadfence();                        // row i final before it is counted down
+        if (SPMM_ILU0_FENCE) __threadfence();
         // count down the rows that wait for row i (acquire: a row that becomes
         // ready here sees its other dependencies' values); keep one, queue the rest
         for (int d = d0; d < d1; d += 32) {

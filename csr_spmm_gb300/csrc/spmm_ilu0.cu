@@ -29,6 +29,7 @@
 // multiply and a rounded subtract (no fused multiply-add), so the factors
 // equal the host reference bit for bit, whatever order the rows run in.
 #include <algorithm>
+#include <climits>
 
 #include "spmm_internal.h"
 #include "spmm_ops.h"
@@ -63,6 +64,11 @@ constexpr int ILU0_SPIN_LIMIT = SPMM_ILU0_SPIN_LIMIT;
 // count-down loop; 1 adds an acquire load of its counter by every lane.
 #ifndef SPMM_ILU0_KEPT_ACQUIRE
 #define SPMM_ILU0_KEPT_ACQUIRE 1
+#endif
+// Fetch the structure records of a row's first two dependents while it is
+// factored (0: each row's record is read when the row starts).
+#ifndef SPMM_ILU0_PREFETCH
+#define SPMM_ILU0_PREFETCH 1
 #endif
 #ifndef SPMM_ILU0_FENCE
 #define SPMM_ILU0_FENCE 0              // 1: a full fence before the count-downs
@@ -155,6 +161,36 @@ __global__ void __launch_bounds__(256) ilu0_fill(Ilu0Params<T> p) {
         if (k >= i) break;
         p.dep_idx[p.dep_ptr[k] + atomicAdd(p.cnt + k, 1)] = i;
     }
+}
+
+// 3b. per-row structure records: everything static that the factorisation
+//     of a row reads before its pivot values (extents, columns, pivot
+//     positions, dependents) in one 256-byte record, so that it arrives in
+//     one round trip and can be fetched ahead for the rows a row readies.
+//     Rows of more than 16 entries or 14 dependents get no record (-1).
+template <typename T>
+__global__ void __launch_bounds__(256) ilu0_records(Ilu0Params<T> p) {
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t i64 = t / ILU0_REC_LANES;
+    if (i64 >= p.n) return;
+    const int i = (int)i64, q = (int)(t % ILU0_REC_LANES);
+    const int s = p.rp[i], e = p.rp[i + 1];
+    const int d0 = p.dep_ptr[i], d1 = p.dep_ptr[i + 1];
+    const int len = e - s, nd = d1 - d0;
+    const bool big = len > ILU0_REC_LANES || nd > ILU0_REC_LANES - 2;
+    int4 r = make_int4(INT_MAX, -1, 0, -1);
+    if (!big && q < len) {
+        r.x = p.ci[s + q];
+        if (r.x < i) {
+            const int2 pv = p.piv[s + q];
+            r.y = pv.x;
+            r.z = pv.y;
+        }
+    }
+    if (!big && q < nd) r.w = p.dep_idx[d0 + q];
+    if (q == ILU0_REC_LANES - 2) r.w = s;
+    if (q == ILU0_REC_LANES - 1) r.w = big ? -1 : (len | (nd << 8));
+    p.rec[i64 * ILU0_REC_LANES + q] = r;
 }
 
 __device__ __forceinline__ void stop(int* abort, int* status, int bit) {
@@ -320,10 +356,16 @@ __device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
 template <typename T>
 __global__ void __launch_bounds__(ILU0_THREADS, 2) ilu0_factor(Ilu0Params<T> p) {
     const int lane = threadIdx.x & 31;
+    const int4 NOREC = make_int4(INT_MAX, -1, 0, -1);
     int next = -1;                              // a row this warp made ready
+    int4 next_rc = NOREC;                       // its record, when fetched ahead
+    bool next_has = false;
     for (;;) {
         int i = next;
+        int4 rc = next_rc;
+        const bool have = next_has;
         next = -1;
+        next_has = false;
         const bool kept = i >= 0;
         if (!kept) {
             int h = 0;
@@ -357,22 +399,52 @@ __global__ void __launch_bounds__(ILU0_THREADS, 2) ilu0_factor(Ilu0Params<T> p) 
                 __nanosleep(SPMM_ILU0_SLEEP_NS);
             }
         }
-        // static data of row i: extents, entries, pivot records, dependents
-        const int s = p.rp[i], e = p.rp[i + 1];
-        const int d0 = p.dep_ptr[i], d1 = p.dep_ptr[i + 1];
+        // row i's structure record (already here when fetched ahead)
+        if (!have) rc = lane < ILU0_REC_LANES ? p.rec[(int64_t)i * ILU0_REC_LANES + lane] : NOREC;
         // a kept row: acquire the values its finished dependencies wrote (every
-        // lane; the loads above are already in flight)
+        // lane; the loads of static data are already in flight)
         if (kept && SPMM_ILU0_KEPT_ACQUIRE) ld_acquire(p.pending + i);
-        const bool short_row = e - s <= 32;
-        int my_c = 0x7fffffff;
+        const int meta = __shfl_sync(FULL, rc.w, ILU0_REC_LANES - 1);
+        const int s = __shfl_sync(FULL, rc.w, ILU0_REC_LANES - 2);
+        int e, d0 = 0, nd;
+        bool short_row;
+        int my_c = INT_MAX;
         T my_v = T(0);
         int2 my_piv = make_int2(-1, 0);
-        if (short_row && lane < e - s) {
-            my_c = p.ci[s + lane];
-            my_v = __ldcg(p.v + s + lane);      // row i's own entries: written by row i only
-            if (my_c < i) my_piv = p.piv[s + lane];
+        int dj = -1;
+        int dep0 = -1, dep1 = -1;
+        int4 pf0 = NOREC, pf1 = NOREC;
+        if (meta >= 0) {
+            // from the record: at most 16 entries, at most 14 dependents
+            const int len = meta & 0xff;
+            nd = meta >> 8;
+            e = s + len;
+            short_row = true;
+            my_c = rc.x;
+            my_piv = make_int2(rc.y, rc.z);
+            if (lane < len) my_v = __ldcg(p.v + s + lane);   // written by row i only
+            dj = lane < nd ? rc.w : -1;
+            // fetch the first two dependents' records ahead: one of them is
+            // likely the row this one readies and keeps
+            dep0 = nd > 0 ? __shfl_sync(FULL, rc.w, 0) : -1;
+            dep1 = nd > 1 ? __shfl_sync(FULL, rc.w, 1) : -1;
+            if (SPMM_ILU0_PREFETCH && lane < ILU0_REC_LANES) {
+                if (dep0 >= 0) pf0 = p.rec[(int64_t)dep0 * ILU0_REC_LANES + lane];
+                if (dep1 >= 0) pf1 = p.rec[(int64_t)dep1 * ILU0_REC_LANES + lane];
+            }
+        } else {
+            // no record: extents, entries, pivot records and dependents from the arrays
+            e = p.rp[i + 1];
+            d0 = p.dep_ptr[i];
+            nd = p.dep_ptr[i + 1] - d0;
+            short_row = e - s <= 32;
+            if (short_row && lane < e - s) {
+                my_c = p.ci[s + lane];
+                my_v = __ldcg(p.v + s + lane);
+                if (my_c < i) my_piv = p.piv[s + lane];
+            }
+            dj = lane < nd ? p.dep_idx[d0 + lane] : -1;
         }
-        const int dj = d0 + lane < d1 ? p.dep_idx[d0 + lane] : -1;
         int dmax = -1;
         bool ok;
         if (short_row)
@@ -391,16 +463,23 @@ __global__ void __launch_bounds__(ILU0_THREADS, 2) ilu0_factor(Ilu0Params<T> p) 
         if (SPMM_ILU0_FENCE) __threadfence();
         // count down the rows that wait for row i (acquire: a row that becomes
         // ready here sees its other dependencies' values); keep one, queue the rest
-        for (int d = d0; d < d1; d += 32) {
-            const int j = d == d0 ? dj : (d + lane < d1 ? p.dep_idx[d + lane] : -1);
+        for (int c = 0; c < nd; c += 32) {
+            const int j = c == 0 ? dj : (c + lane < nd ? p.dep_idx[d0 + c + lane] : -1);
             bool ready = false;
-            if (d + lane < d1) ready = atom_add_acq_rel(p.pending + j, -1) == 1;
+            if (c + lane < nd) ready = atom_add_acq_rel(p.pending + j, -1) == 1;
             unsigned rm = __ballot_sync(FULL, ready);
             if (next < 0 && rm) {
                 const int keep = __ffs(rm) - 1;
                 next = __shfl_sync(FULL, j, keep);
                 if (lane == keep) ready = false;
                 rm &= rm - 1;
+                if (SPMM_ILU0_PREFETCH && next == dep0) {
+                    next_rc = pf0;
+                    next_has = true;
+                } else if (SPMM_ILU0_PREFETCH && next == dep1) {
+                    next_rc = pf1;
+                    next_has = true;
+                }
             }
             if (ready) st_release(p.queue + atomicAdd(p.tail, 1), j);
         }
@@ -417,6 +496,7 @@ cudaError_t launch_ilu0(const Ilu0Params<T>& p, int grid, cudaStream_t st) {
     ilu0_count<T><<<rb, 256, 0, st>>>(p);
     ilu0_scan<T><<<1, 1024, 0, st>>>(p);
     ilu0_fill<T><<<rb, 256, 0, st>>>(p);
+    ilu0_records<T><<<(unsigned)(((int64_t)p.n * ILU0_REC_LANES + 255) / 256), 256, 0, st>>>(p);
     ilu0_factor<T><<<grid, ILU0_THREADS, 0, st>>>(p);
     return cudaGetLastError();
 }

@@ -53,6 +53,7 @@ struct Ilu0Params {
     int* dep_idx;          // [nnz] dependent rows, grouped by the row they depend on
     int2* piv;             // [nnz] per lower entry (i, k): the position of a_kk in row k
                            //       (-1: none) and the end of row k
+    int4* rec;             // [n * ILU0_REC_LANES] per-row structure records (ilu0_records)
     int* queue;            // [n] rows in the order they became ready (-1: not yet)
     int* head;             // next queue slot to take
     int* tail;             // next queue slot to fill
@@ -61,6 +62,11 @@ struct Ilu0Params {
     int* status;           // caller's: 0, or ILU0 failure bits
 };
 constexpr int ILU0_THREADS = 256;
+// A row's structure record: ILU0_REC_LANES int4 words, lane q holding
+// {column of entry q, pivot position and end of row k for a lower entry q,
+// dependent q}; lane 14's last word is the row's first entry, lane 15's its
+// length | dependents << 8 (or -1: too long for a record).
+constexpr int ILU0_REC_LANES = 16;
 template <typename T>
 cudaError_t launch_ilu0(const Ilu0Params<T>& p, int grid, cudaStream_t st);
 template <typename T>

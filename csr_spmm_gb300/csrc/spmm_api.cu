@@ -237,9 +237,43 @@ int rows_grid(spmm_handle_s* h, int es, const Geometry& g) {
     return b * h->num_sms;
 }
 
+// m <= SMALL_ROWS: the whole product in one launch, no pre-pass and no
+// handle scratch.  Profiling counts every row as short (the kernel bins them
+// itself) and reports the one launch as the rows stage.
+template <typename T>
+spmm_status_t small_product(spmm_handle_s* h, const Plan& P, const SpmmParams<T>& p,
+                            const L2Window* win, cudaStream_t st);
+
 // Records event i of the profiled call (no-op when profiling is off).
 inline void mark(spmm_handle_s* h, int i, cudaStream_t st) {
     if (h->profiling) cudaEventRecord(h->ev[i], st);
+}
+
+template <typename T>
+spmm_status_t small_product(spmm_handle_s* h, const Plan& P, const SpmmParams<T>& p,
+                            const L2Window* win, cudaStream_t st) {
+    mark(h, 0, st);
+    mark(h, 1, st);
+    if (launch_small<T>(p, P.geo, P.short_max, h->num_sms, st, win) != cudaSuccess)
+        return SPMM_ERR_CUDA;
+    mark(h, 2, st);
+    mark(h, 3, st);
+    mark(h, 4, st);
+    if (h->profiling) {
+        h->prof = spmm_profile_t{};
+        h->prof.launches = 1;
+        h->prof.rows_short = p.m;
+        h->prof.panels = P.npanels;
+        h->prof.panel_cols = P.panel_cols;
+        h->prof.vec_elems = P.geo.W;
+        h->prof.group_lanes = P.geo.G;
+        h->prof.slots = P.geo.R;
+        h->prof.short_max = P.short_max;
+        h->prof.long_min = P.long_min;
+        h->prof_hdr = nullptr;
+        h->have_profile = true;
+    }
+    return SPMM_OK;
 }
 
 template <typename T>
@@ -281,6 +315,24 @@ spmm_status_t spmm_csr_impl(spmm_handle_t h, T alpha, const int32_t* row_ptr,
     }
 
     const Plan P = make_plan<T>(h, k, n, B, ldb, C, ldc);
+    if (m <= SMALL_ROWS) {
+        SpmmParams<T> p{};
+        p.row_ptr = row_ptr;
+        p.col_idx = col_idx;
+        p.values = values;
+        p.B = B;
+        p.ldb = ldb;
+        p.C = C;
+        p.ldc = ldc;
+        p.m = (int)m;
+        p.n = (int)n;
+        p.alpha = alpha;
+        p.beta = beta;
+        p.panel_cols = P.panel_cols;
+        p.npanels = P.npanels;
+        L2Window wbuf;
+        return small_product<T>(h, P, p, b_window(h, B, k, ldb, n, &wbuf), st);
+    }
     const int lg = long_grid_of(h);
     const ScratchLayout L = layout_for(m, n, (int)sizeof(T), lg);
     spmm_status_t s = ensure_scratch(h, L.total);
@@ -404,6 +456,10 @@ spmm_status_t spmm_plan_impl(spmm_plan_t pl, T alpha, const int32_t* row_ptr,
     p.hdr = pl->hdr;
     p.partials = static_cast<T*>(pl->partials);
     p.long_grid = pl->long_grid;
+    if (m <= SMALL_ROWS) {                // the direct call's one-launch path, same bits
+        L2Window wbuf;
+        return small_product<T>(h, P, p, b_window(h, B, k, ldb, n, &wbuf), st);
+    }
     const bool overlap = SPMM_PDL && !h->profiling;
     const bool has_long = pl->hdr_host[HDR_COUNT_LONG] > 0;
     mark(h, 0, st);

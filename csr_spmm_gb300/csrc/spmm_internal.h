@@ -34,6 +34,10 @@ constexpr int BIN_SINGLE_ITEMS = 8;                     // rows per thread, one-
 constexpr int BIN_SINGLE_ROWS = BIN_THREADS * BIN_SINGLE_ITEMS;   // m up to this: one launch
 constexpr int BIN_REC = 8;    // int32 words per tile record
 
+// Products of at most SMALL_ROWS rows run as one launch (small_kernel: every
+// CTA bins the rows itself in shared memory).
+constexpr int SMALL_ROWS = 2048;
+
 // Long-row kernel geometry.
 constexpr int LONG_THREADS = 256;
 constexpr int LONG_WARPS = LONG_THREADS / 32;
@@ -195,6 +199,11 @@ cudaError_t launch_rows(const SpmmParams<T>& p, const Geometry& g, int grid, cud
 template <typename T>
 cudaError_t launch_long(const SpmmParams<T>& p, const Geometry& g, cudaStream_t st, bool overlap,
                         const L2Window* win = nullptr);
+// m <= SMALL_ROWS: the whole product in one launch (spmm_small_*.cu); p needs
+// no bins.  short_max: the short-row threshold of the product's plan.
+template <typename T>
+cudaError_t launch_small(const SpmmParams<T>& p, const Geometry& g, int short_max, int grid,
+                         cudaStream_t st, const L2Window* win = nullptr);
 
 // ---- epilogue-only and checking kernels (spmm_misc.cu) ----
 template <typename T>

@@ -470,6 +470,117 @@ rows_kernel(SpmmParams<T> p) {
 }
 
 // ---------------------------------------------------------------------------
+// Small products (m <= SMALL_ROWS rows): the whole product in one launch.
+// Every CTA bins all m rows itself in shared memory (their lengths are at
+// most 8 KB of row_ptr, read from L2), so no pre-pass launch and no global
+// bins are needed.  Short rows (<= short_max entries, the same threshold as
+// the binned path) are then processed as in rows_kernel: CTA c takes an
+// equal contiguous range of the short list and its warps interleave over it.
+// Every longer row is processed by one warp, as a medium row of rows_kernel
+// (the warp's groups split its entries and are combined at the row's end);
+// the grid's warps take equal shares of those rows' entries.  Short and
+// medium rows therefore give rows_kernel's results bit for bit; a row of
+// long_min or more entries, which the binned path splits across CTAs, is
+// summed in the medium-row order instead.  Rows keep their order in both
+// lists (stable scans).
+// ---------------------------------------------------------------------------
+// Exclusive scan of v over the block (blockDim.x threads, a multiple of 32,
+// at most 1024); returns this thread's prefix and sets *total.  s_warp holds
+// 33 ints: the warps' prefixes, then the block total.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* total, int* s_warp) {
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(FULL, incl, off);
+        if (lane >= off) incl += y;
+    }
+    __syncthreads();                                   // s_warp free from any earlier scan
+    if (lane == 31) s_warp[wib] = incl;
+    __syncthreads();
+    if (wib == 0) {
+        int w = lane < nw ? s_warp[lane] : 0;
+        int wi = w;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(FULL, wi, off);
+            if (lane >= off) wi += y;
+        }
+        if (lane < nw) s_warp[lane] = wi - w;          // exclusive prefix of warp totals
+        if (lane == 31) s_warp[32] = wi;               // block total
+    }
+    __syncthreads();
+    *total = s_warp[32];
+    return s_warp[wib] + incl - v;
+}
+
+template <typename T, int W, int G, int R, bool READ_C, bool WHOLE, int BS = 0>
+__global__ void __launch_bounds__(RowsOccupancy<T, W, G>::THREADS, 1)
+small_kernel(SpmmParams<T> p, int short_max) {
+    constexpr int THREADS = RowsOccupancy<T, W, G>::THREADS;
+    constexpr int WPB = THREADS / 32;
+    static_assert(WPB <= 32, "one scan word per warp");
+    constexpr int SLOT_BYTES = Bcast<T, W, G, R, true>::WARP_BYTES;
+    __shared__ __align__(16) unsigned char s_slots[SLOT_BYTES > 0 ? WPB * SLOT_BYTES : 16];
+    __shared__ int s_short[SMALL_ROWS];     // short rows, ascending
+    __shared__ int s_other[SMALL_ROWS];     // longer rows, ascending
+    __shared__ int s_pre[SMALL_ROWS + 1];   // exclusive prefix of the longer rows' lengths
+    __shared__ int s_warp[33];
+    unsigned char* wslot = s_slots + (threadIdx.x >> 5) * SLOT_BYTES;
+    const int m = p.m;
+
+    // bin every row (stable: chunk by chunk, ranks by block scans)
+    int n_short = 0, n_other = 0, other_nnz = 0;     // block-uniform
+    for (int c0 = 0; c0 < m; c0 += THREADS) {
+        const int r = c0 + (int)threadIdx.x;
+        int len = 0;
+        if (r < m) len = p.row_ptr[r + 1] - p.row_ptr[r];
+        const bool is_short = r < m && len <= short_max;
+        const bool is_other = r < m && !is_short;
+        int tot_s, tot_o, tot_e;
+        const int rank_s = block_exclusive_scan(is_short ? 1 : 0, &tot_s, s_warp);
+        const int rank_o = block_exclusive_scan(is_other ? 1 : 0, &tot_o, s_warp);
+        const int pre_e = block_exclusive_scan(is_other ? len : 0, &tot_e, s_warp);
+        if (is_short) s_short[n_short + rank_s] = r;
+        if (is_other) {
+            s_other[n_other + rank_o] = r;
+            s_pre[n_other + rank_o] = other_nnz + pre_e;
+        }
+        n_short += tot_s;
+        n_other += tot_o;
+        other_nnz += tot_e;
+    }
+    if (threadIdx.x == 0) s_pre[n_other] = other_nnz;
+    __syncthreads();
+
+    const uint64_t pol_s = policy_evict_first();
+    const int wib = threadIdx.x >> 5;
+    const int64_t nwarps = (int64_t)gridDim.x * WPB;
+    const int64_t w = (int64_t)blockIdx.x * WPB + wib;
+    // short rows: an equal contiguous range per CTA, the CTA's warps interleaved
+    const int cs0 = (int)((int64_t)blockIdx.x * n_short / gridDim.x);
+    const int cs1 = (int)((int64_t)(blockIdx.x + 1) * n_short / gridDim.x);
+    const int s_count = max(0, (cs1 - cs0 - wib + WPB - 1) / WPB);
+    // longer rows: equal shares of their entries per warp of the grid
+    int o0 = 0, o1 = 0;
+    if (n_other > 0) {
+        o0 = medium_lower_bound(s_pre, n_other, w * other_nnz / nwarps);
+        o1 = medium_lower_bound(s_pre, n_other, (w + 1) * other_nnz / nwarps);
+        if (w == nwarps - 1) o1 = n_other;
+    }
+    for (int panel = 0; panel < p.npanels; ++panel) {
+        const int c0 = panel * p.panel_cols;
+        const int pw = min(p.panel_cols, p.n - c0);
+        if (s_count > 0)
+            process_rows<T, W, G, R, false, READ_C, WHOLE, BS>(p, s_short, cs0 + wib, s_count, WPB,
+                                                               c0, pw, pol_s, wslot);
+        if (o1 > o0)
+            process_rows<T, W, G, R, true, READ_C, WHOLE, BS>(p, s_other, o0, o1 - o0, 1, c0, pw,
+                                                              pol_s, wslot);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Accumulate the entries [a, b) of one row, whole warp (groups interleaved as
 // in the medium-row mode), with the next step's entries prefetched.  The
 // caller combines the groups.

@@ -148,6 +148,24 @@ extern "C" spmm_status_t spmm_csr_f32_noalloc(float alpha, const int32_t* row_pt
     const ProductPlan P = plan_product(ds->l2_bytes, k, n, (int)sizeof(float), vec);
     const Geometry geo = P.geo;
     const int long_grid = long_grid_for(ds->num_sms);     // <= NOALLOC_LONG_GRID_MAX (set-up)
+    if (m <= SMALL_ROWS) {                // one launch, no scratch (as spmm_csr_f32 does)
+        SpmmParams<float> p{};
+        p.row_ptr = row_ptr;
+        p.col_idx = col_idx;
+        p.values = values;
+        p.B = B;
+        p.ldb = ldb;
+        p.C = C;
+        p.ldc = ldc;
+        p.m = (int)m;
+        p.n = (int)n;
+        p.alpha = alpha;
+        p.beta = beta;
+        p.panel_cols = P.panel_cols;
+        p.npanels = P.npanels;
+        return launch_small<float>(p, geo, P.short_max, ds->num_sms, st) == cudaSuccess
+                   ? SPMM_OK : SPMM_ERR_CUDA;
+    }
 
     BinScratch bs{};
     bs.hdr = reinterpret_cast<int*>(ds->scratch + OFF_HDR);

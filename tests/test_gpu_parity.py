@@ -147,15 +147,18 @@ def test_integer_wide_exact(handle):
 
 
 @pytest.mark.parametrize("n", [1, 16, 64, 200])
-def test_single_huge_row(handle, n):
+@pytest.mark.parametrize("pad", [0, 2100])
+def test_single_huge_row(handle, n, pad):
+    # pad: empty rows appended so that m exceeds 2,048 and the row is split
+    # across CTAs (pad = 0: the one-launch path, one warp for the row)
     k = 300_000
-    lens = np.array([3, 150_000, 0, 7])
+    lens = np.concatenate([np.array([3, 150_000, 0, 7]), np.zeros(pad, np.int64)])
     from synth import distinct_sorted_columns
     rp, ci = distinct_sorted_columns(lens, k, 9, 1)
     vals = rng.uniform(9, 2, int(rp[-1]), -1, 1)
     B = rng.uniform(9, 3, k * n, -1, 1).reshape(k, n)
-    C0 = rng.uniform(9, 4, 4 * n, -1, 1).reshape(4, n)
-    p = _problem("huge_row", 4, k, n, rp, ci, vals, B, 1.0, 1.0, C0, dtype=np.float32)
+    C0 = rng.uniform(9, 4, (4 + pad) * n, -1, 1).reshape(4 + pad, n)
+    p = _problem("huge_row", 4 + pad, k, n, rp, ci, vals, B, 1.0, 1.0, C0, dtype=np.float32)
     got, _ = run_problem(handle, p)
     assert_parity(p, got, what=f"huge row n={n}")
 
@@ -163,8 +166,11 @@ def test_single_huge_row(handle, n):
 def test_many_long_rows_across_ctas(handle):
     # 700 rows of 1000..9000 entries: rows span CTAs and CTAs span rows
     from synth import distinct_sorted_columns
-    m, k, n = 700, 20_000, 48
+    # 2,100 rows, so that the binned path (and its CTA split) takes them; the
+    # last 1,400 are empty
+    m, k, n = 2100, 20_000, 48
     lens = 1000 + np.floor(rng.uniform(11, 1, m) * 8000).astype(np.int64)
+    lens[700:] = 0
     rp, ci = distinct_sorted_columns(lens, k, 11, 2)
     vals = rng.uniform(11, 3, int(rp[-1]), -1, 1)
     B = rng.uniform(11, 4, k * n, -1, 1).reshape(k, n)

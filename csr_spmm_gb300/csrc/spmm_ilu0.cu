@@ -10,7 +10,8 @@
 //      itself to the dependent count of each of them; rows with none are
 //      queued; for each lower entry (i, k) it records where row k keeps its
 //      pivot and where row k ends;
-//   2. a prefix sum turns the dependent counts into list offsets;
+//   2. a prefix sum (three launches over tiles) turns the dependent counts
+//      into list offsets;
 //   3. the dependent lists are filled (the transpose of the strict lower
 //      pattern);
 //   4. one persistent launch: a warp takes the next queue slot, waits for it
@@ -125,30 +126,70 @@ __global__ void __launch_bounds__(256) ilu0_count(Ilu0Params<T> p) {
     if (lower + withheld == 0) p.queue[atomicAdd(p.tail, 1)] = i;
 }
 
-// 2. exclusive prefix sum of cnt into dep_ptr (one block; each thread owns a
-//    contiguous chunk), then cnt is cleared to serve as the fill cursor
-template <typename T>
-__global__ void __launch_bounds__(1024) ilu0_scan(Ilu0Params<T> p) {
-    __shared__ int s[1024];
-    const int per = (p.n + 1023) / 1024;
-    const int b = threadIdx.x * per, e = min(p.n, b + per);
-    int sum = 0;
-    for (int i = b; i < e; ++i) sum += p.cnt[i];
-    s[threadIdx.x] = sum;
-    __syncthreads();
-    for (int off = 1; off < 1024; off <<= 1) {           // inclusive Hillis-Steele
-        const int x = threadIdx.x >= off ? s[threadIdx.x - off] : 0;
-        __syncthreads();
-        s[threadIdx.x] += x;
-        __syncthreads();
+// 2. exclusive prefix sum of cnt into dep_ptr, then cnt is cleared to serve
+//    as the fill cursor.  Three launches over tiles of ILU0_SCAN_TILE rows
+//    (coalesced, every SM busy): the tiles' sums, one block scanning those
+//    sums, then each tile's own scan plus its offset.
+constexpr int ILU0_SCAN_TILE = 1024;
+
+// Inclusive scan of v over a 1024-thread block; s_w holds 32 ints.
+__device__ __forceinline__ int block_inclusive_scan_1024(int v, int* s_w) {
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(FULL, x, off);
+        if (lane >= off) x += y;
     }
-    int run = s[threadIdx.x] - sum;
-    for (int i = b; i < e; ++i) {
-        p.dep_ptr[i] = run;
-        run += p.cnt[i];
+    __syncthreads();                                   // s_w free from an earlier use
+    if (lane == 31) s_w[wib] = x;
+    __syncthreads();
+    if (wib == 0) {
+        int w = s_w[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(FULL, w, off);
+            if (lane >= off) w += y;
+        }
+        s_w[lane] = w;                                 // inclusive over the warps
+    }
+    __syncthreads();
+    return x + (wib > 0 ? s_w[wib - 1] : 0);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(ILU0_SCAN_TILE) ilu0_scan_tiles(Ilu0Params<T> p) {
+    __shared__ int s_w[32];
+    const int64_t i = (int64_t)blockIdx.x * ILU0_SCAN_TILE + threadIdx.x;
+    const int v = i < p.n ? p.cnt[i] : 0;
+    const int incl = block_inclusive_scan_1024(v, s_w);
+    if (threadIdx.x == ILU0_SCAN_TILE - 1) p.tile_sum[blockIdx.x] = incl;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(ILU0_SCAN_TILE) ilu0_scan_sums(Ilu0Params<T> p, int ntiles) {
+    __shared__ int s_w[32];
+    int carry = 0;
+    for (int t0 = 0; t0 < ntiles; t0 += ILU0_SCAN_TILE) {
+        const int t = t0 + (int)threadIdx.x;
+        const int v = t < ntiles ? p.tile_sum[t] : 0;
+        const int incl = block_inclusive_scan_1024(v, s_w);
+        if (t < ntiles) p.tile_sum[t] = carry + incl - v;   // exclusive offset of tile t
+        carry += s_w[31];
+    }
+    if (threadIdx.x == 0) p.dep_ptr[p.n] = carry;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(ILU0_SCAN_TILE) ilu0_scan_apply(Ilu0Params<T> p) {
+    __shared__ int s_w[32];
+    const int64_t i = (int64_t)blockIdx.x * ILU0_SCAN_TILE + threadIdx.x;
+    const int v = i < p.n ? p.cnt[i] : 0;
+    const int incl = block_inclusive_scan_1024(v, s_w);
+    if (i < p.n) {
+        p.dep_ptr[i] = p.tile_sum[blockIdx.x] + incl - v;
         p.cnt[i] = 0;
     }
-    if (threadIdx.x == 1023) p.dep_ptr[p.n] = s[1023];
 }
 
 // 3. dependent lists (the order within a list only decides queue order)
@@ -494,7 +535,10 @@ template <typename T>
 cudaError_t launch_ilu0(const Ilu0Params<T>& p, int grid, cudaStream_t st) {
     const int rb = (p.n + 255) / 256;
     ilu0_count<T><<<rb, 256, 0, st>>>(p);
-    ilu0_scan<T><<<1, 1024, 0, st>>>(p);
+    const int ntiles = (int)(((int64_t)p.n + ILU0_SCAN_TILE - 1) / ILU0_SCAN_TILE);
+    ilu0_scan_tiles<T><<<ntiles, ILU0_SCAN_TILE, 0, st>>>(p);
+    ilu0_scan_sums<T><<<1, ILU0_SCAN_TILE, 0, st>>>(p, ntiles);
+    ilu0_scan_apply<T><<<ntiles, ILU0_SCAN_TILE, 0, st>>>(p);
     ilu0_fill<T><<<rb, 256, 0, st>>>(p);
     ilu0_records<T><<<(unsigned)(((int64_t)p.n * ILU0_REC_LANES + 255) / 256), 256, 0, st>>>(p);
     ilu0_factor<T><<<grid, ILU0_THREADS, 0, st>>>(p);

@@ -54,6 +54,7 @@ struct Ilu0Params {
     int2* piv;             // [nnz] per lower entry (i, k): the position of a_kk in row k
                            //       (-1: none) and the end of row k
     int4* rec;             // [n * ILU0_REC_LANES] per-row structure records (ilu0_records)
+    int* tile_sum;         // [ceil(n / 1024)] tile sums, then tile offsets, of the dependent counts
     int* queue;            // [n] rows in the order they became ready (-1: not yet)
     int* head;             // next queue slot to take
     int* tail;             // next queue slot to fill

@@ -224,7 +224,7 @@ spmm_status_t spmm_fw_argmin_f64(spmm_handle_t h, int64_t n, int64_t k,
  * Requires n >= 1 (n == 0: SPMM_ERR_INVALID_ARGUMENT, as the page), a valid
  * CSR structure with column indices strictly ascending within each row (no
  * duplicates), and no concurrent call on the same handle (it uses handle
- * scratch: 68n + 3 nnz + 10 int32 words).  Asynchronous on `stream`. */
+ * scratch: 68n + n / 1024 + 3 nnz + 12 int32 words).  Asynchronous on `stream`. */
 #define SPMM_ILU0_SINGULAR 1
 #define SPMM_ILU0_WAIT_TIMEOUT 2
 spmm_status_t spmm_ilu0_f32(spmm_handle_t h, int64_t n, int64_t nnz, const int32_t *row_ptr,

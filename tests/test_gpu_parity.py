@@ -384,3 +384,17 @@ def test_prepass_beyond_one_wave_of_tiles(handle):
     rows = np.unique(np.concatenate([np.linspace(0, p.m - 1, 3000).astype(np.int64),
                                      np.flatnonzero(lens >= 1024)[:50]]))
     assert_parity(p, got, rows=rows, what="pre-pass with a scan launch")
+
+
+def test_fp64_fma_rate_probe(handle):
+    """The binary64 FMA-rate probe that binary64 rooflines are set against:
+    positive, repeatable within a few percent, and within the range a part
+    with 1-4 binary64 FMA per clock per SM at 1-2.5 GHz can reach."""
+    import torch
+    props = torch.cuda.get_device_properties(0)
+    sms = props.multi_processor_count
+    r1 = cs.spmm_measure_fp64_fma_rate(handle.ptr)
+    r2 = cs.spmm_measure_fp64_fma_rate(handle.ptr)
+    assert r1 > 0 and r2 > 0
+    assert abs(r1 - r2) <= 0.1 * max(r1, r2)
+    assert sms * 1.0 * 1.0e9 * 0.5 <= r1 <= sms * 4.0 * 2.5e9

@@ -161,6 +161,34 @@ __device__ __forceinline__ void fetch_pair(int& cj, T& av, int j,
     }
 }
 
+// The column of pair j alone, and its value alone.  In the binary32 kernels
+// with lane groups narrower than a warp the value is broadcast when its FMAs
+// run, not while the gathers are in flight, so it holds no register across
+// the gather latency: fewer spills, power-law 0.874 -> 0.863 ms and wide-N
+// 0.684 -> 0.678 ms per call on GB300, the same bits.  Full-warp groups keep
+// the early broadcast (SEACells: 0.244 -> 0.287 ms with the late one).
+template <typename T, int W, int G, int R, bool ROWS>
+__device__ __forceinline__ int fetch_col(int j, const int (&col)[Cfg<T, W, G, R, ROWS>::Q],
+                                         const unsigned char* slot) {
+    if constexpr (Bcast<T, W, G, R, ROWS>::SMEM)
+        return __double2loint(reinterpret_cast<const double2*>(slot + j * 16)->x);
+    else
+        return __shfl_sync(FULL, col[j / G], j % G, G);
+}
+template <typename T, int W, int G, int R, bool ROWS>
+__device__ __forceinline__ T fetch_val(int j, const T (&val)[Cfg<T, W, G, R, ROWS>::Q],
+                                       const unsigned char* slot) {
+    if constexpr (Bcast<T, W, G, R, ROWS>::SMEM)
+        return reinterpret_cast<const double2*>(slot + j * 16)->y;
+    else
+        return __shfl_sync(FULL, val[j / G], j % G, G);
+}
+#ifndef SPMM_LATE_VALUE
+#define SPMM_LATE_VALUE 1
+#endif
+template <typename T, int W, int G>
+constexpr bool late_value() { return SPMM_LATE_VALUE && narrow_f32<T, W, G>(); }
+
 // One step: the group consumes its `cnt` (<= CH) entries held in (col, val),
 // in batches of U.  cmax / cmin are warp-uniform bounds on every group's cnt:
 // batches below cmin are whole for every group and gather without checks.
@@ -189,7 +217,10 @@ __device__ __forceinline__ void consume_step(T (&acc)[R][W],
 #pragma unroll
             for (int u = 0; u < C::U; ++u) {
                 int cj;
-                fetch_pair<T, W, G, R, ROWS>(cj, av[u], j0 + u, col, val, slot);
+                if constexpr (late_value<T, W, G>())
+                    cj = fetch_col<T, W, G, R, ROWS>(j0 + u, col, slot);
+                else
+                    fetch_pair<T, W, G, R, ROWS>(cj, av[u], j0 + u, col, val, slot);
                 const int64_t roff = (int64_t)cj * ldb;
 #pragma unroll
                 for (int r = 0; r < R; ++r)
@@ -200,7 +231,10 @@ __device__ __forceinline__ void consume_step(T (&acc)[R][W],
             for (int u = 0; u < C::U; ++u) {
                 const int j = j0 + u;
                 int cj;
-                fetch_pair<T, W, G, R, ROWS>(cj, av[u], j, col, val, slot);
+                if constexpr (late_value<T, W, G>())
+                    cj = fetch_col<T, W, G, R, ROWS>(j, col, slot);
+                else
+                    fetch_pair<T, W, G, R, ROWS>(cj, av[u], j, col, val, slot);
                 const int64_t roff = (int64_t)cj * ldb;
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
@@ -214,11 +248,14 @@ __device__ __forceinline__ void consume_step(T (&acc)[R][W],
             }
         }
 #pragma unroll
-        for (int u = 0; u < C::U; ++u)
+        for (int u = 0; u < C::U; ++u) {
+            if constexpr (late_value<T, W, G>())
+                av[u] = fetch_val<T, W, G, R, ROWS>(j0 + u, val, slot);
 #pragma unroll
             for (int r = 0; r < R; ++r)
 #pragma unroll
                 for (int e = 0; e < W; ++e) acc[r][e] = fma(av[u], bv[u][r][e], acc[r][e]);
+        }
     }
 }
 

@@ -319,10 +319,13 @@ __device__ __forceinline__ void write_row_c0(T* __restrict__ Crow, const T (&acc
 //     group gi takes entries [s + gi*CH, s + gi*CH + CH) of each warp step of
 //     RPW*CH entries, and the groups are combined at the end of the row.
 // ---------------------------------------------------------------------------
+// ext (the one-launch path): each row's (first entry, length), indexed by row,
+// already in shared memory, in place of two row_ptr reads per row.
 template <typename T, int W, int G, int R, bool MEDIUM, bool READ_C, bool WHOLE, int BS>
 __device__ __forceinline__ void process_rows(const SpmmParams<T>& p, const int* __restrict__ list,
                                              int first, int count, int stride, int c0col, int pw,
-                                             uint64_t pol_s, unsigned char* wslot) {
+                                             uint64_t pol_s, unsigned char* wslot,
+                                             const int2* ext = nullptr) {
     using C = Cfg<T, W, G, R, true>;
     constexpr int Q = C::Q;
     const int lane = threadIdx.x & 31;
@@ -340,8 +343,14 @@ __device__ __forceinline__ void process_rows(const SpmmParams<T>& p, const int* 
         int my_row = -1, my_e0 = 0, my_len = 0;
         if (lane < nrows) {
             my_row = list[first + (int64_t)(sub + lane) * stride];
-            my_e0 = p.row_ptr[my_row];
-            my_len = p.row_ptr[my_row + 1] - my_e0;
+            if (ext) {
+                const int2 x = ext[my_row];
+                my_e0 = x.x;
+                my_len = x.y;
+            } else {
+                my_e0 = p.row_ptr[my_row];
+                my_len = p.row_ptr[my_row + 1] - my_e0;
+            }
         }
         for (int vbase = 0; vbase < nvec; vbase += C::SLOTS) {
             const LaneVecs<T, W, R> lv = lane_vecs<T, W, G, R>(Bp, vbase, pw);
@@ -559,35 +568,50 @@ small_kernel(SpmmParams<T> p, int short_max) {
     static_assert(WPB <= 32, "one scan word per warp");
     constexpr int SLOT_BYTES = Bcast<T, W, G, R, true>::WARP_BYTES;
     __shared__ __align__(16) unsigned char s_slots[SLOT_BYTES > 0 ? WPB * SLOT_BYTES : 16];
-    __shared__ int s_short[SMALL_ROWS];     // short rows, ascending
-    __shared__ int s_other[SMALL_ROWS];     // longer rows, ascending
+    // short rows ascending from the front; longer rows from the back, the
+    // j-th longer row (ascending) at SMALL_ROWS - 1 - j
+    __shared__ int s_list[SMALL_ROWS];
     __shared__ int s_pre[SMALL_ROWS + 1];   // exclusive prefix of the longer rows' lengths
+    __shared__ int2 s_ext[SMALL_ROWS];      // every row's first entry and length
     __shared__ int s_warp[33];
     unsigned char* wslot = s_slots + (threadIdx.x >> 5) * SLOT_BYTES;
     const int m = p.m;
 
-    // bin every row (stable: chunk by chunk, ranks by block scans)
-    int n_short = 0, n_other = 0, other_nnz = 0;     // block-uniform
-    for (int c0 = 0; c0 < m; c0 += THREADS) {
-        const int r = c0 + (int)threadIdx.x;
-        int len = 0;
-        if (r < m) len = p.row_ptr[r + 1] - p.row_ptr[r];
-        const bool is_short = r < m && len <= short_max;
-        const bool is_other = r < m && !is_short;
-        int tot_s, tot_o, tot_e;
-        const int rank_s = block_exclusive_scan(is_short ? 1 : 0, &tot_s, s_warp);
-        const int rank_o = block_exclusive_scan(is_other ? 1 : 0, &tot_o, s_warp);
-        const int pre_e = block_exclusive_scan(is_other ? len : 0, &tot_e, s_warp);
-        if (is_short) s_short[n_short + rank_s] = r;
-        if (is_other) {
-            s_other[n_other + rank_o] = r;
-            s_pre[n_other + rank_o] = other_nnz + pre_e;
-        }
-        n_short += tot_s;
-        n_other += tot_o;
-        other_nnz += tot_e;
+    // every row's extents, and whether all rows are short
+    bool all_short = true;
+    for (int r = (int)threadIdx.x; r < m; r += THREADS) {
+        const int e0 = p.row_ptr[r];
+        const int len = p.row_ptr[r + 1] - e0;
+        s_ext[r] = make_int2(e0, len);
+        all_short &= len <= short_max;
     }
-    if (threadIdx.x == 0) s_pre[n_other] = other_nnz;
+    all_short = __syncthreads_and(all_short);
+    int n_short = 0, n_other = 0, other_nnz = 0;     // block-uniform
+    if (all_short) {
+        for (int r = (int)threadIdx.x; r < m; r += THREADS) s_list[r] = r;
+        n_short = m;
+    } else {
+        // stable ranks, chunk by chunk, by block scans
+        for (int c0 = 0; c0 < m; c0 += THREADS) {
+            const int r = c0 + (int)threadIdx.x;
+            const int len = r < m ? s_ext[r].y : 0;
+            const bool is_short = r < m && len <= short_max;
+            const bool is_other = r < m && !is_short;
+            int tot_s, tot_o, tot_e;
+            const int rank_s = block_exclusive_scan(is_short ? 1 : 0, &tot_s, s_warp);
+            const int rank_o = block_exclusive_scan(is_other ? 1 : 0, &tot_o, s_warp);
+            const int pre_e = block_exclusive_scan(is_other ? len : 0, &tot_e, s_warp);
+            if (is_short) s_list[n_short + rank_s] = r;
+            if (is_other) {
+                s_list[SMALL_ROWS - 1 - (n_other + rank_o)] = r;
+                s_pre[n_other + rank_o] = other_nnz + pre_e;
+            }
+            n_short += tot_s;
+            n_other += tot_o;
+            other_nnz += tot_e;
+        }
+        if (threadIdx.x == 0) s_pre[n_other] = other_nnz;
+    }
     __syncthreads();
 
     const uint64_t pol_s = policy_evict_first();
@@ -609,11 +633,12 @@ small_kernel(SpmmParams<T> p, int short_max) {
         const int c0 = panel * p.panel_cols;
         const int pw = min(p.panel_cols, p.n - c0);
         if (s_count > 0)
-            process_rows<T, W, G, R, false, READ_C, WHOLE, BS>(p, s_short, cs0 + wib, s_count, WPB,
-                                                               c0, pw, pol_s, wslot);
-        if (o1 > o0)
-            process_rows<T, W, G, R, true, READ_C, WHOLE, BS>(p, s_other, o0, o1 - o0, 1, c0, pw,
-                                                              pol_s, wslot);
+            process_rows<T, W, G, R, false, READ_C, WHOLE, BS>(p, s_list, cs0 + wib, s_count, WPB,
+                                                               c0, pw, pol_s, wslot, s_ext);
+        if (o1 > o0)      // longer row j at SMALL_ROWS - 1 - j: a descending walk of s_list
+            process_rows<T, W, G, R, true, READ_C, WHOLE, BS>(p, s_list, SMALL_ROWS - 1 - o0,
+                                                              o1 - o0, -1, c0, pw, pol_s, wslot,
+                                                              s_ext);
     }
 }
 

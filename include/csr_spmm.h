@@ -85,7 +85,9 @@ spmm_status_t spmm_destroy(spmm_handle_t h);
 spmm_status_t spmm_reserve(spmm_handle_t h, int64_t m, int64_t n, int elem_size);
 
 /* C = alpha * A * B + beta * C in binary32 (oxicuda-sparse, ops/spmm.rs, `spmm`
- * with T = f32).  Arguments as described at the top of this file:
+ * with T = f32).  Up to m = 2048 rows the product is one kernel launch and
+ * uses no handle scratch; larger products bin the rows in a pre-pass first.
+ * Arguments as described at the top of this file:
  *   row_ptr [m+1], col_idx [nnz], values [nnz]   CSR of A (m x k)
  *   B  [k rows, stride ldb]   dense, row-major, only columns 0..n-1 are read
  *   C  [m rows, stride ldc]   dense, row-major, columns 0..n-1 are written
@@ -358,7 +360,8 @@ spmm_status_t spmm_plan_csr_f64(spmm_plan_t plan, double alpha,
  * GPU durations between CUDA events recorded on the call's stream around each
  * stage; the counts come from the device-side row bins. */
 typedef struct {
-    float prepass_ms;      /* row-binning pre-pass (1 to 3 launches) */
+    float prepass_ms;      /* row-binning pre-pass (1 to 3 launches; none for m <= 2048,
+                              where the whole product is one launch: rows_ms) */
     float rows_ms;         /* short + medium rows kernel (1 launch) */
     float long_ms;         /* long-row CTA split (1 launch) */
     float fixup_ms;        /* 0: the long-row fixup runs inside the long-row launch */

@@ -788,13 +788,15 @@ spmm_status_t spmm_ilu0_impl(spmm_handle_t h, int64_t n, int64_t nnz, const int3
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // int words: pending[n], cnt[n], head, tail, abort, finished | dep_ptr[n+1] | queue[n] |
     // dep_idx[nnz] | piv[nnz] (int2, 8-byte aligned) | rec[16 n] (int4, 16-byte aligned) |
-    // tile_sum[n / 1024]
+    // pub[nnz] (T, 16-byte aligned) | done[n] | tile_sum[n / 1024]
     const size_t zero_words = 2 * (size_t)n + 4;
     const size_t o_ptr = zero_words, o_q = o_ptr + (size_t)n + 1, o_dep = o_q + (size_t)n;
     const size_t nz1 = (size_t)std::max<int64_t>(nnz, 1);
     const size_t o_piv = (o_dep + nz1 + 1) & ~(size_t)1;
     const size_t o_rec = (o_piv + 2 * nz1 + 3) & ~(size_t)3;          // 16-byte aligned
-    const size_t o_tile = o_rec + 4 * (size_t)ILU0_REC_LANES * (size_t)n;
+    const size_t o_pub = o_rec + 4 * (size_t)ILU0_REC_LANES * (size_t)n;
+    const size_t o_done = o_pub + nz1 * (sizeof(T) / sizeof(int));
+    const size_t o_tile = o_done + (size_t)n;
     const size_t words = o_tile + ((size_t)n + 1023) / 1024 + 1;
     spmm_status_t s = ensure_scratch(h, words * sizeof(int));
     if (s != SPMM_OK) return s;
@@ -824,6 +826,8 @@ spmm_status_t spmm_ilu0_impl(spmm_handle_t h, int64_t n, int64_t nnz, const int3
     p.piv = reinterpret_cast<int2*>(w + o_piv);
     p.rec = reinterpret_cast<int4*>(w + o_rec);
     p.tile_sum = w + o_tile;
+    p.pub = reinterpret_cast<T*>(w + o_pub);
+    p.done = w + o_done;
     p.status = status;
     const int grid = ilu0_blocks_per_sm<T>() * h->num_sms;
     return launch_ilu0<T>(p, grid, st) == cudaSuccess ? SPMM_OK : SPMM_ERR_CUDA;

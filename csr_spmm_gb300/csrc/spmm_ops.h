@@ -55,6 +55,8 @@ struct Ilu0Params {
                            //       (-1: none) and the end of row k
     int4* rec;             // [n * ILU0_REC_LANES] per-row structure records (ilu0_records)
     int* tile_sum;         // [ceil(n / 1024)] tile sums, then tile offsets, of the dependent counts
+    T* pub;                // [nnz] published final values (the sentinel until written)
+    int* done;             // [n] 1: a value the row published is the sentinel's bit pattern
     int* queue;            // [n] rows in the order they became ready (-1: not yet)
     int* head;             // next queue slot to take
     int* tail;             // next queue slot to fill

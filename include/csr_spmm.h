@@ -217,7 +217,10 @@ spmm_status_t spmm_fw_argmin_f64(spmm_handle_t h, int64_t n, int64_t k,
  * the lists of dependent rows are built by three small kernels, then one
  * persistent launch factors each row as soon as the rows it depends on are
  * final (the page launches one kernel per level and synchronises between
- * them).  nnz = row_ptr[n] (the library cannot read it without a
+ * them).  Finished rows pass their values on through published copies in
+ * handle scratch, preset to a signalling-NaN sentinel; an input value with
+ * exactly the sentinel's bits is still handled, on a slower path.
+ * nnz = row_ptr[n] (the library cannot read it without a
  * synchronisation).  status (device, one int32, required) is
  * zeroed, then receives SPMM_ILU0_SINGULAR if a pivot row lacks its diagonal
  * or has a zero one, and SPMM_ILU0_WAIT_TIMEOUT if a wait for a pivot row ran
@@ -226,7 +229,8 @@ spmm_status_t spmm_fw_argmin_f64(spmm_handle_t h, int64_t n, int64_t k,
  * Requires n >= 1 (n == 0: SPMM_ERR_INVALID_ARGUMENT, as the page), a valid
  * CSR structure with column indices strictly ascending within each row (no
  * duplicates), and no concurrent call on the same handle (it uses handle
- * scratch: 68n + n / 1024 + 3 nnz + 12 int32 words).  Asynchronous on `stream`. */
+ * scratch: 69n + n / 1024 + 4 nnz + 12 int32 words for binary32, one more
+ * word per entry for binary64).  Asynchronous on `stream`. */
 #define SPMM_ILU0_SINGULAR 1
 #define SPMM_ILU0_WAIT_TIMEOUT 2
 spmm_status_t spmm_ilu0_f32(spmm_handle_t h, int64_t n, int64_t nnz, const int32_t *row_ptr,

@@ -154,3 +154,52 @@ def test_band_pivot_rows_past_one_warp(handle, dtype):
         rp = np.zeros(n + 1, np.int64)
         np.cumsum(np.bincount(r, minlength=n), out=rp[1:])
         check(handle, rp, c, vals.astype(dtype), f"band {w}")
+
+
+# The published-value sentinels of the factorisation (signalling NaNs that no
+# arithmetic returns): an input value with exactly these bits must still be
+# passed on, through the kernel's done-flag path.
+SENTINEL = {np.float64: np.uint64(0x7FF4C0DE5A5A5A5A), np.float32: np.uint32(0x7FA5C0DE)}
+
+
+def sentinel_value(dtype):
+    bits = np.uint64 if dtype == np.float64 else np.uint32
+    return np.array([SENTINEL[dtype]], dtype=bits).view(dtype)[0]
+
+
+@pytest.mark.parametrize("dtype", [np.float64, np.float32])
+def test_sentinel_bits_in_an_unused_upper_entry(handle, dtype):
+    """Row 0 stores the sentinel's bit pattern at (0, 2); row 1 reads row 0
+    from its pivot on, so it waits on that value, but stores no column 2, so
+    every factor is finite except the sentinel entry, which passes through."""
+    rp = np.array([0, 2, 4, 6, 8])
+    ci = np.array([0, 2, 0, 1, 1, 2, 2, 3])
+    v = np.array([4.0, 0.0, 1.0, 5.0, 1.0, 6.0, 1.0, 7.0], dtype=dtype)
+    v[1] = sentinel_value(dtype)
+    check(handle, rp, ci, v, "sentinel in an upper entry")
+
+
+@pytest.mark.parametrize("dtype", [np.float64, np.float32])
+def test_sentinel_bits_on_the_long_row_path(handle, dtype):
+    """Row 0 holds 40 entries (the long-row path) and 49 dependents (no
+    structure record); its last column holds the sentinel's bits, which row 39
+    uses (a NaN results) and every other row only reads past.  NaN factors
+    may differ in payload between the host and the GPU, so those compare as
+    NaN; the rest bit for bit."""
+    n = 50
+    rows = [list(range(40))] + [[0, i] for i in range(1, n)]
+    rp = np.zeros(n + 1, dtype=np.int64)
+    rp[1:] = np.cumsum([len(r) for r in rows])
+    ci = np.concatenate([np.array(r) for r in rows])
+    v = np.where(ci == np.repeat(np.arange(n), np.diff(rp)), 50.0, 1.0).astype(dtype)
+    v[39] = sentinel_value(dtype)
+    want, wdepth = oracle.ilu0(rp, ci, v)
+    got, depth = gpu_ilu0(handle, rp, ci, v)
+    bits = np.uint32 if dtype == np.float32 else np.uint64
+    nan_w, nan_g = np.isnan(want), np.isnan(got)
+    assert np.array_equal(nan_w, nan_g)
+    assert nan_w.sum() >= 2                          # the sentinel and row 39's diagonal
+    assert got.view(bits)[39] == SENTINEL[dtype]     # passed through unchanged
+    ok = ~nan_w
+    assert np.array_equal(got[ok].view(bits), want[ok].view(bits))
+    assert np.array_equal(depth, wdepth)

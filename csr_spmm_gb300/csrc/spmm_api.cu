@@ -77,6 +77,11 @@ constexpr double PANEL_TRIGGER = SPMM_PANEL_TRIGGER;
 #define SPMM_LONG_MIN_ROW 1024
 #endif
 constexpr int LONG_MIN_ROW = SPMM_LONG_MIN_ROW;
+// Narrow lane groups: rows of up to this many group steps stay in the short
+// bin (one group per row); longer ones get a whole warp (medium bin).
+#ifndef SPMM_SHORT_MAX_STEPS
+#define SPMM_SHORT_MAX_STEPS 2
+#endif
 // Long-row grid: CTAs per SM.
 #ifndef SPMM_LONG_CTAS
 #define SPMM_LONG_CTAS 4
@@ -138,7 +143,8 @@ ProductPlan plan_product(int64_t l2_bytes, int64_t k, int64_t n, int es, bool ve
     const int U = std::min(SPMM_BATCH_MAX, std::max(1, batch_bytes / bytes_per_entry));
     const int CH = std::max(P.geo.G, U);
     P.long_min = LONG_MIN_ROW;
-    P.short_max = (P.geo.G == 32) ? P.long_min - 1 : std::min(P.long_min - 1, 2 * CH);
+    P.short_max = (P.geo.G == 32) ? P.long_min - 1
+                                  : std::min(P.long_min - 1, SPMM_SHORT_MAX_STEPS * CH);
     return P;
 }
 

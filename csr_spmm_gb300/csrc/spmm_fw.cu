@@ -27,6 +27,10 @@ constexpr int FW_NONE = 0x7fffffff;   // "no row yet" (loses every index tie)
 #define SPMM_FW_SMEM 1
 #endif
 constexpr size_t FW_SMEM_MAX = 96 * 1024;
+// binary32 scans with k <= FWTC_MAXK run on the tensor cores (fw_scan_tc)
+#ifndef SPMM_FW_TC
+#define SPMM_FW_TC 1
+#endif
 
 template <typename T> __device__ __forceinline__ T largest();
 template <> __device__ __forceinline__ float largest<float>() { return FLT_MAX; }
@@ -254,6 +258,294 @@ __global__ void __launch_bounds__(FW_THREADS) fw_scan(FwParams<T> p) {
     }
 }
 
+
+// ---------------------------------------------------------------------------
+// Tensor-core scan (binary32, k <= FWTC_MAXK): the gradient of 128 rows at a
+// time is one tile D = A t1 on the fifth-generation tensor cores, A the
+// tile's K2B rows made dense (k columns) in shared memory.  Operands are
+// binary32 split into two tf32 parts, x = x_hi + x_lo (each rounded to tf32,
+// x - x_hi exact), and D = A_hi t1_hi + A_hi t1_lo + A_lo t1_hi: three
+// kind::tf32 MMAs per 8-wide k step, each product of tf32 parts exact in
+// binary32, the dropped A_lo t1_lo and rounding residues below 2^-21 of
+// |a||t|, with binary32 accumulation in tensor memory.  One thread issues
+// the MMAs; completion is signalled on an mbarrier; the 128 x N accumulator
+// is read back with tcgen05.ld (warp w: lanes 32w .. 32w + 31, one row per
+// thread) into a shared-memory tile where T2 is subtracted (duplicate
+// columns summed in stored order first, as in the CUDA-core scan), B's
+// entries add to the gap, and thread c keeps column c's minimum over the
+// block's rows in ascending order (strict <: lowest row).  Operand layout:
+// K-major, no swizzle, 8-row x 16-byte core matrices; within an 8-row group
+// the k direction's core matrices are 128 bytes apart (the descriptor's
+// leading byte offset), and the groups kp * 32 bytes apart (stride offset).
+constexpr int FWTC_THREADS = 512;
+constexpr int FWTC_UNROLL = 4;                   // entries per thread per round of loads
+constexpr int FWTC_M = 128;                      // rows per tile: the MMA's M
+constexpr int FWTC_MAXK = 104;
+constexpr int FWTC_WAIT_LIMIT = 1 << 24;
+
+struct FwTcGeo {
+    int kp;             // k rounded up to the MMA's k step (8)
+    int nn;             // N of the MMA: k rounded up to 16
+    int tcols;          // tensor-memory columns (a power of two, >= 32)
+    int gstride;        // row stride of the gradient tile (floats)
+    size_t a_bytes;     // one A part (128 x kp)
+    size_t b_bytes;     // one t1 part (nn x kp)
+    size_t region_a;    // both A parts, or the gradient tile, whichever is larger
+    size_t smem;        // dynamic shared memory
+};
+
+__host__ __device__ inline FwTcGeo fwtc_geo(int k) {
+    FwTcGeo g;
+    g.kp = (k + 7) / 8 * 8;
+    g.nn = (k + 15) / 16 * 16;
+    g.tcols = 32;
+    while (g.tcols < g.nn) g.tcols *= 2;
+    g.gstride = g.nn + 1;
+    g.a_bytes = (size_t)(FWTC_M / 8) * g.kp * 32;
+    g.b_bytes = (size_t)(g.nn / 8) * g.kp * 32;
+    const size_t gt = (size_t)FWTC_M * g.gstride * sizeof(float);
+    g.region_a = ((2 * g.a_bytes > gt ? 2 * g.a_bytes : gt) + 127) / 128 * 128;
+    g.smem = g.region_a + 2 * g.b_bytes;
+    return g;
+}
+
+inline bool fw_tc_ok(int k) {
+    return SPMM_FW_TC && k >= 1 && k <= FWTC_MAXK && fwtc_geo(k).smem <= 200 * 1024;
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+// shared-memory matrix descriptor: start, leading and stride byte offsets
+// (all in 16-byte units), descriptor version 1, no swizzle
+__device__ __forceinline__ uint64_t umma_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46);
+}
+__device__ __forceinline__ int kmajor_off(int r, int kk, int kp) {
+    return (r >> 3) * (kp * 32) + (kk >> 2) * 128 + (r & 7) * 16 + (kk & 3) * 4;
+}
+__device__ __forceinline__ void split_tf32(float v, float& hi, float& lo) {
+    uint32_t h, l;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(h) : "f"(v));
+    hi = __uint_as_float(h);
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(l) : "f"(v - hi));
+    lo = __uint_as_float(l);
+}
+__device__ __forceinline__ void umma_tf32(uint32_t tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                          int accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n"
+        ::"r"(tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+// row of a tile holding entry q: the largest r < nr with rp[r] <= q
+__device__ __forceinline__ int tile_row(const int* rp, int nr, int q) {
+    int lo = 0, hi = nr - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (rp[mid] <= q) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Every run of equal columns within a row among the tile's entries of one
+// CSR matrix: f(row in tile, column, sum of the run in stored order), called
+// by the thread holding the run's first entry.  Each thread loads
+// FWTC_UNROLL entries (and their neighbours' columns) per round before using
+// them, so that the loads of a round are in flight together.
+template <typename F>
+__device__ __forceinline__ void for_tile_runs(const int* rp, int nr, const int* __restrict__ ci,
+                                              const float* __restrict__ val, F f) {
+    const int e0 = rp[0], e1 = rp[nr];
+    for (int base = e0; base < e1; base += FWTC_THREADS * FWTC_UNROLL) {
+        int c[FWTC_UNROLL], cp[FWTC_UNROLL], cn[FWTC_UNROLL];
+        float v[FWTC_UNROLL];
+#pragma unroll
+        for (int j = 0; j < FWTC_UNROLL; ++j) {
+            const int q = base + j * FWTC_THREADS + (int)threadIdx.x;
+            c[j] = -1;
+            cp[j] = -2;
+            cn[j] = -2;
+            v[j] = 0.f;
+            if (q < e1) {
+                c[j] = ci[q];
+                v[j] = val[q];
+                if (q > e0) cp[j] = ci[q - 1];
+                if (q + 1 < e1) cn[j] = ci[q + 1];
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < FWTC_UNROLL; ++j) {
+            const int q = base + j * FWTC_THREADS + (int)threadIdx.x;
+            if (q >= e1) continue;
+            const int r = tile_row(rp, nr, q);
+            if (q > rp[r] && cp[j] == c[j]) continue;          // inside a run
+            float s = v[j];
+            if (q + 1 < rp[r + 1] && cn[j] == c[j])            // a run: sum it in order
+                for (int q2 = q + 1; q2 < rp[r + 1] && ci[q2] == c[j]; ++q2) s += val[q2];
+            f(r, c[j], s);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(FWTC_THREADS, 1) fw_scan_tc(FwParams<float> p) {
+    extern __shared__ __align__(1024) unsigned char tc_smem[];
+    __shared__ __align__(8) uint64_t s_mbar;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_rp[3][FWTC_M + 1];          // the tile's K2B, T2 and B row pointers
+    __shared__ double s_gap[FWTC_THREADS / 32];
+    const FwTcGeo g = fwtc_geo(p.k);
+    unsigned char* sAh = tc_smem;
+    unsigned char* sAl = tc_smem + g.a_bytes;
+    unsigned char* sBh = tc_smem + g.region_a;
+    unsigned char* sBl = sBh + g.b_bytes;
+    float* sG = reinterpret_cast<float*>(tc_smem);   // after the MMAs: the gradient tile
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_addr(&s_tmem)), "r"(g.tcols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    if (tid == 0) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&s_mbar)));
+    // t1 as the MMA's B operand (N x kp, K-major: B[c][m] = t1[m][c]), split
+#pragma unroll 4
+    for (int i = tid; i < g.nn * g.kp; i += FWTC_THREADS) {
+        const int c = i / g.kp, m = i - c * g.kp;
+        const float v = (c < p.k && m < p.k) ? p.t1d[(int64_t)m * p.ldk + c] : 0.f;
+        float hi, lo;
+        split_tf32(v, hi, lo);
+        const int off = kmajor_off(c, m, g.kp);
+        *reinterpret_cast<float*>(sBh + off) = hi;
+        *reinterpret_cast<float*>(sBl + off) = lo;
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = s_tmem;
+    const uint32_t idesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(g.nn >> 3) << 17) |
+                           ((uint32_t)(FWTC_M >> 4) << 24);
+    const uint32_t sbo = (uint32_t)g.kp * 32;
+
+    float best_v = FLT_MAX;
+    int best_i = FW_NONE;
+    double gap = 0.0;
+    bool ok = true;
+    const int ntiles = (p.n + FWTC_M - 1) / FWTC_M;
+    int iter = 0;
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++iter) {
+        const int r0 = tile * FWTC_M, nr = min(FWTC_M, p.n - r0);
+        for (int r = tid; r <= nr; r += FWTC_THREADS) {
+            s_rp[0][r] = p.k2b_rp[r0 + r];
+            s_rp[1][r] = p.t2_rp[r0 + r];
+            s_rp[2][r] = p.b_rp[r0 + r];
+        }
+        for (size_t i = tid; i < 2 * g.a_bytes / 16; i += FWTC_THREADS)
+            reinterpret_cast<float4*>(tc_smem)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        __syncthreads();
+        // the tile's K2B rows, dense and split (a run of equal columns summed
+        // in stored order by the thread holding its first entry)
+        for_tile_runs(s_rp[0], nr, p.k2b_ci, p.k2b_v, [&](int r, int c, float v) {
+            if (c < 0 || c >= p.k) return;
+            float hi, lo;
+            split_tf32(v, hi, lo);
+            const int off = kmajor_off(r, c, g.kp);
+            *reinterpret_cast<float*>(sAh + off) = hi;
+            *reinterpret_cast<float*>(sAl + off) = lo;
+        });
+        // the operands' generic-proxy stores, visible to the tensor cores
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncthreads();
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        if (tid == 0) {
+            const uint32_t ah = smem_addr(sAh), al = smem_addr(sAl);
+            const uint32_t bh = smem_addr(sBh), bl = smem_addr(sBl);
+            for (int s = 0; s < g.kp / 8; ++s) {
+                const uint32_t ko = (uint32_t)s * 256;     // two core matrices per k step
+                umma_tf32(tmem, umma_desc(ah + ko, 128, sbo), umma_desc(bh + ko, 128, sbo), idesc,
+                          s > 0);
+                umma_tf32(tmem, umma_desc(ah + ko, 128, sbo), umma_desc(bl + ko, 128, sbo), idesc, 1);
+                umma_tf32(tmem, umma_desc(al + ko, 128, sbo), umma_desc(bh + ko, 128, sbo), idesc, 1);
+            }
+            asm volatile(
+                "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                ::"r"(smem_addr(&s_mbar)) : "memory");
+        }
+        // the MMAs' completion (phase iter & 1), bounded
+        uint32_t done = 0;
+        for (int it = 0; it < FWTC_WAIT_LIMIT && !done; ++it) {
+            asm volatile(
+                "{\n .reg .pred q;\n mbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2;\n"
+                " selp.u32 %0, 1, 0, q;\n}\n"
+                : "=r"(done) : "r"(smem_addr(&s_mbar)), "r"((uint32_t)(iter & 1)) : "memory");
+        }
+        ok = __syncthreads_and(done != 0);
+        if (!ok) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        // accumulator -> gradient tile: warp w reads lanes 32 (w % 4) .. + 31
+        // (one row per thread), column chunks w / 4, w / 4 + 4, ...
+        {
+            const int quarter = warp & 3, row = quarter * 32 + lane;
+            for (int c0 = (warp >> 2) * 16; c0 < g.nn; c0 += (FWTC_THREADS / 128) * 16) {
+                uint32_t v[16];
+                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0;
+                asm volatile(
+                    "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,"
+                    "%12,%13,%14,%15}, [%16];"
+                    : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
+                      "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]),
+                      "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+                    : "r"(taddr));
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                for (int j = 0; j < 16; ++j) sG[row * g.gstride + c0 + j] = __uint_as_float(v[j]);
+            }
+        }
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncthreads();
+        // G = D - T2 (runs of equal columns summed first)
+        for_tile_runs(s_rp[1], nr, p.t2_ci, p.t2_v, [&](int r, int c, float v) {
+            if (c >= 0 && c < p.k) sG[r * g.gstride + c] -= v;
+        });
+        __syncthreads();
+        // gap += B[i, c] * G[i, c] over B's entries
+        for_tile_runs(s_rp[2], nr, p.b_ci, p.b_v, [&](int r, int c, float b) {
+            if (c >= 0 && c < p.k && b != 0.f) gap += (double)b * (double)sG[r * g.gstride + c];
+        });
+        // column tid's minimum over the tile's rows, ascending
+        if (tid < p.k) {
+            for (int r = 0; r < nr; ++r) {
+                const float v = sG[r * g.gstride + tid];
+                if (v < best_v) {
+                    best_v = v;
+                    best_i = r0 + r;
+                }
+            }
+        }
+        __syncthreads();                         // the tile is read before the next one overwrites it
+    }
+    if (tid < p.k) {
+        p.part_val[(int64_t)blockIdx.x * p.ldk + tid] = best_v;
+        p.part_idx[(int64_t)blockIdx.x * p.ldk + tid] = best_i;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) gap += __shfl_xor_sync(FULL, gap, off);
+    if (lane == 0) s_gap[warp] = gap;
+    __syncthreads();
+    if (tid == 0) {
+        double t = 0.0;
+        for (int w = 0; w < FWTC_THREADS / 32; ++w) t += s_gap[w];
+        // a wait that ran out leaves the gap not a number (every wait is bounded)
+        p.part_gap[blockIdx.x] = ok ? t : __longlong_as_double(0x7ff8000000000000LL);
+    }
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(g.tcols));
+}
+
 // Warps 0 .. k-1: one column each; lanes take blocks lane, lane + 32, ...
 // and the (value, row) candidates are combined by the order "smaller value,
 // then lower row", a total order, so the result does not depend on the
@@ -319,6 +611,17 @@ cudaError_t launch_fw(const FwParams<T>& p, int grid, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     if (p.k > 0) fw_densify<T><<<(p.k + 7) / 8, 256, 0, st>>>(p);
     const size_t smem = fw_smem_bytes<T>(p.k);
+    if constexpr (sizeof(T) == 4) {
+        if (fw_tc_ok(p.k)) {
+            const FwTcGeo g = fwtc_geo(p.k);
+            e = cudaFuncSetAttribute(fw_scan_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)g.smem);
+            if (e != cudaSuccess) return e;
+            fw_scan_tc<<<grid, FWTC_THREADS, g.smem, st>>>(p);
+            fw_reduce<T><<<(p.k + 7) / 8 + 1, 256, 0, st>>>(p);
+            return cudaGetLastError();
+        }
+    }
     if (smem > 0) {
         e = cudaFuncSetAttribute(fw_scan<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
@@ -333,6 +636,7 @@ cudaError_t launch_fw(const FwParams<T>& p, int grid, cudaStream_t st) {
 
 template <typename T>
 int fw_blocks_per_sm(int k) {
+    if (sizeof(T) == 4 && fw_tc_ok(k)) return 1;   // the tensor-core scan: one block per SM
     int b = 0;
     const size_t smem = fw_smem_bytes<T>(k);
     cudaError_t e;

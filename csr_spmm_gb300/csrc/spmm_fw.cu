@@ -278,7 +278,6 @@ __global__ void __launch_bounds__(FW_THREADS) fw_scan(FwParams<T> p) {
 // the k direction's core matrices are 128 bytes apart (the descriptor's
 // leading byte offset), and the groups kp * 32 bytes apart (stride offset).
 constexpr int FWTC_THREADS = 512;
-constexpr int FWTC_UNROLL = 4;                   // entries per thread per round of loads
 constexpr int FWTC_M = 128;                      // rows per tile: the MMA's M
 constexpr int FWTC_MAXK = 104;
 constexpr int FWTC_WAIT_LIMIT = 1 << 24;
@@ -339,53 +338,73 @@ __device__ __forceinline__ void umma_tf32(uint32_t tmem, uint64_t a, uint64_t b,
         " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n"
         ::"r"(tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
 }
-// row of a tile holding entry q: the largest r < nr with rp[r] <= q
-__device__ __forceinline__ int tile_row(const int* rp, int nr, int q) {
-    int lo = 0, hi = nr - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (rp[mid] <= q) lo = mid;
-        else hi = mid - 1;
+
+// The rows of a tile that one warp handles (tile rows warp, warp + 16, ...,
+// FWTC_RPW of them) and the first 32 entries of each, loaded ahead of their
+// use (while the MMAs run): lane j < FWTC_RPW holds row j's extents, lane l
+// holds entry l of every row.
+constexpr int FWTC_WARPS = FWTC_THREADS / 32;
+constexpr int FWTC_RPW = FWTC_M / FWTC_WARPS;
+struct FwRows {
+    int s, e;                                    // lane j < FWTC_RPW: row j's entries [s, e)
+    int c[FWTC_RPW];
+    float v[FWTC_RPW];
+};
+
+__device__ __forceinline__ void fw_rows_load(FwRows& R, const int* __restrict__ rp,
+                                             const int* __restrict__ ci,
+                                             const float* __restrict__ val, int r0, int nr) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    R.s = 0;
+    R.e = 0;
+    if (lane < FWTC_RPW) {
+        const int r = warp + FWTC_WARPS * lane;
+        if (r < nr) {
+            R.s = rp[r0 + r];
+            R.e = rp[r0 + r + 1];
+        }
     }
-    return lo;
+#pragma unroll
+    for (int j = 0; j < FWTC_RPW; ++j) {
+        const int s = __shfl_sync(FULL, R.s, j), e = __shfl_sync(FULL, R.e, j);
+        const int q = s + lane;
+        R.c[j] = q < e ? ci[q] : -1;
+        R.v[j] = q < e ? val[q] : 0.f;
+    }
 }
 
-// Every run of equal columns within a row among the tile's entries of one
-// CSR matrix: f(row in tile, column, sum of the run in stored order), called
-// by the thread holding the run's first entry.  Each thread loads
-// FWTC_UNROLL entries (and their neighbours' columns) per round before using
-// them, so that the loads of a round are in flight together.
+// Every run of equal columns in the warp's rows: f(row in tile, column, sum
+// of the run in stored order), called by the lane holding the run's first
+// entry.  The first 32 entries of each row come from R; longer rows load
+// the rest 32 at a time.  No block barrier: each warp touches only its rows.
 template <typename F>
-__device__ __forceinline__ void for_tile_runs(const int* rp, int nr, const int* __restrict__ ci,
+__device__ __forceinline__ void fw_rows_apply(const FwRows& R, const int* __restrict__ ci,
                                               const float* __restrict__ val, F f) {
-    const int e0 = rp[0], e1 = rp[nr];
-    for (int base = e0; base < e1; base += FWTC_THREADS * FWTC_UNROLL) {
-        int c[FWTC_UNROLL], cp[FWTC_UNROLL], cn[FWTC_UNROLL];
-        float v[FWTC_UNROLL];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-        for (int j = 0; j < FWTC_UNROLL; ++j) {
-            const int q = base + j * FWTC_THREADS + (int)threadIdx.x;
-            c[j] = -1;
-            cp[j] = -2;
-            cn[j] = -2;
-            v[j] = 0.f;
-            if (q < e1) {
-                c[j] = ci[q];
-                v[j] = val[q];
-                if (q > e0) cp[j] = ci[q - 1];
-                if (q + 1 < e1) cn[j] = ci[q + 1];
+    for (int j = 0; j < FWTC_RPW; ++j) {
+        const int s = __shfl_sync(FULL, R.s, j), e = __shfl_sync(FULL, R.e, j);
+        const int r = warp + FWTC_WARPS * j;
+        int last = -2;                           // the previous chunk's last column
+        for (int base = s; base < e; base += 32) {
+            const int q = base + lane;
+            int c = R.c[j];
+            float v = R.v[j];
+            if (base != s) {
+                c = q < e ? ci[q] : -1;
+                v = q < e ? val[q] : 0.f;
             }
-        }
-#pragma unroll
-        for (int j = 0; j < FWTC_UNROLL; ++j) {
-            const int q = base + j * FWTC_THREADS + (int)threadIdx.x;
-            if (q >= e1) continue;
-            const int r = tile_row(rp, nr, q);
-            if (q > rp[r] && cp[j] == c[j]) continue;          // inside a run
-            float s = v[j];
-            if (q + 1 < rp[r + 1] && cn[j] == c[j])            // a run: sum it in order
-                for (int q2 = q + 1; q2 < rp[r + 1] && ci[q2] == c[j]; ++q2) s += val[q2];
-            f(r, c[j], s);
+            int prev = __shfl_up_sync(FULL, c, 1);
+            if (lane == 0) prev = last;
+            int next = __shfl_down_sync(FULL, c, 1);
+            last = __shfl_sync(FULL, c, 31);
+            if (q < e && !(q > s && prev == c)) {
+                float sum = v;
+                if (lane == 31 && q + 1 < e) next = ci[q + 1];
+                if (q + 1 < e && next == c)      // a run: sum it in order
+                    for (int q2 = q + 1; q2 < e && ci[q2] == c; ++q2) sum += val[q2];
+                f(r, c, sum);
+            }
         }
     }
 }
@@ -394,8 +413,9 @@ __global__ void __launch_bounds__(FWTC_THREADS, 1) fw_scan_tc(FwParams<float> p)
     extern __shared__ __align__(1024) unsigned char tc_smem[];
     __shared__ __align__(8) uint64_t s_mbar;
     __shared__ uint32_t s_tmem;
-    __shared__ int s_rp[3][FWTC_M + 1];          // the tile's K2B, T2 and B row pointers
-    __shared__ double s_gap[FWTC_THREADS / 32];
+    __shared__ float s_bv[FWTC_THREADS];
+    __shared__ int s_bi[FWTC_THREADS];
+    __shared__ double s_gap[FWTC_WARPS];
     const FwTcGeo g = fwtc_geo(p.k);
     unsigned char* sAh = tc_smem;
     unsigned char* sAl = tc_smem + g.a_bytes;
@@ -410,16 +430,23 @@ __global__ void __launch_bounds__(FWTC_THREADS, 1) fw_scan_tc(FwParams<float> p)
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     if (tid == 0) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&s_mbar)));
-    // t1 as the MMA's B operand (N x kp, K-major: B[c][m] = t1[m][c]), split
+    // t1 as the MMA's B operand (N x kp, K-major: B[c][m] = t1[m][c]), split;
+    // consecutive threads read consecutive columns of a t1 row
 #pragma unroll 4
     for (int i = tid; i < g.nn * g.kp; i += FWTC_THREADS) {
-        const int c = i / g.kp, m = i - c * g.kp;
+        const int m = i / g.nn, c = i - m * g.nn;
         const float v = (c < p.k && m < p.k) ? p.t1d[(int64_t)m * p.ldk + c] : 0.f;
         float hi, lo;
         split_tf32(v, hi, lo);
         const int off = kmajor_off(c, m, g.kp);
         *reinterpret_cast<float*>(sBh + off) = hi;
         *reinterpret_cast<float*>(sBl + off) = lo;
+    }
+    const int ntiles = (p.n + FWTC_M - 1) / FWTC_M;
+    FwRows kr, tr;
+    if ((int)blockIdx.x < ntiles) {
+        const int r0 = blockIdx.x * FWTC_M;
+        fw_rows_load(kr, p.k2b_rp, p.k2b_ci, p.k2b_v, r0, min(FWTC_M, p.n - r0));
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
@@ -429,25 +456,21 @@ __global__ void __launch_bounds__(FWTC_THREADS, 1) fw_scan_tc(FwParams<float> p)
                            ((uint32_t)(FWTC_M >> 4) << 24);
     const uint32_t sbo = (uint32_t)g.kp * 32;
 
+    // column tid % 128 over rows 32 (tid / 128) .. + 31 of every tile
+    const int mcol = tid & (FWTC_M - 1), mgrp = tid / FWTC_M;
     float best_v = FLT_MAX;
     int best_i = FW_NONE;
     double gap = 0.0;
     bool ok = true;
-    const int ntiles = (p.n + FWTC_M - 1) / FWTC_M;
     int iter = 0;
     for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++iter) {
         const int r0 = tile * FWTC_M, nr = min(FWTC_M, p.n - r0);
-        for (int r = tid; r <= nr; r += FWTC_THREADS) {
-            s_rp[0][r] = p.k2b_rp[r0 + r];
-            s_rp[1][r] = p.t2_rp[r0 + r];
-            s_rp[2][r] = p.b_rp[r0 + r];
-        }
         for (size_t i = tid; i < 2 * g.a_bytes / 16; i += FWTC_THREADS)
             reinterpret_cast<float4*>(tc_smem)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         __syncthreads();
         // the tile's K2B rows, dense and split (a run of equal columns summed
-        // in stored order by the thread holding its first entry)
-        for_tile_runs(s_rp[0], nr, p.k2b_ci, p.k2b_v, [&](int r, int c, float v) {
+        // in stored order by the lane holding its first entry)
+        fw_rows_apply(kr, p.k2b_ci, p.k2b_v, [&](int r, int c, float v) {
             if (c < 0 || c >= p.k) return;
             float hi, lo;
             split_tf32(v, hi, lo);
@@ -474,6 +497,12 @@ __global__ void __launch_bounds__(FWTC_THREADS, 1) fw_scan_tc(FwParams<float> p)
                 "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                 ::"r"(smem_addr(&s_mbar)) : "memory");
         }
+        // while the MMAs run: this tile's T2 rows and the next tile's K2B rows
+        fw_rows_load(tr, p.t2_rp, p.t2_ci, p.t2_v, r0, nr);
+        const int next = tile + gridDim.x;
+        if (next < ntiles)
+            fw_rows_load(kr, p.k2b_rp, p.k2b_ci, p.k2b_v, next * FWTC_M,
+                         min(FWTC_M, p.n - next * FWTC_M));
         // the MMAs' completion (phase iter & 1), bounded
         uint32_t done = 0;
         for (int it = 0; it < FWTC_WAIT_LIMIT && !done; ++it) {
@@ -506,19 +535,26 @@ __global__ void __launch_bounds__(FWTC_THREADS, 1) fw_scan_tc(FwParams<float> p)
         }
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
         __syncthreads();
-        // G = D - T2 (runs of equal columns summed first)
-        for_tile_runs(s_rp[1], nr, p.t2_ci, p.t2_v, [&](int r, int c, float v) {
+        // G = D - T2 on this warp's rows (runs of equal columns summed first),
+        // then gap += B[i, c] * G[i, c] over B's entries of the same rows
+        fw_rows_apply(tr, p.t2_ci, p.t2_v, [&](int r, int c, float v) {
             if (c >= 0 && c < p.k) sG[r * g.gstride + c] -= v;
         });
+        __syncwarp();
+        {
+            FwRows br;
+            fw_rows_load(br, p.b_rp, p.b_ci, p.b_v, r0, nr);
+            fw_rows_apply(br, p.b_ci, p.b_v, [&](int r, int c, float bv) {
+                if (c >= 0 && c < p.k && bv != 0.f)
+                    gap += (double)bv * (double)sG[r * g.gstride + c];
+            });
+        }
         __syncthreads();
-        // gap += B[i, c] * G[i, c] over B's entries
-        for_tile_runs(s_rp[2], nr, p.b_ci, p.b_v, [&](int r, int c, float b) {
-            if (c >= 0 && c < p.k && b != 0.f) gap += (double)b * (double)sG[r * g.gstride + c];
-        });
-        // column tid's minimum over the tile's rows, ascending
-        if (tid < p.k) {
-            for (int r = 0; r < nr; ++r) {
-                const float v = sG[r * g.gstride + tid];
+        // column mcol's minimum over rows 32 mgrp .. + 31 of the tile, ascending
+        if (mcol < p.k) {
+            const int ra = mgrp * 32, rb = min(nr, ra + 32);
+            for (int r = ra; r < rb; ++r) {
+                const float v = sG[r * g.gstride + mcol];
                 if (v < best_v) {
                     best_v = v;
                     best_i = r0 + r;
@@ -526,6 +562,24 @@ __global__ void __launch_bounds__(FWTC_THREADS, 1) fw_scan_tc(FwParams<float> p)
             }
         }
         __syncthreads();                         // the tile is read before the next one overwrites it
+    }
+    // each column's four candidates (value, then lower row: a total order)
+    s_bv[tid] = best_v;
+    s_bi[tid] = best_i;
+    __syncthreads();
+    if (tid < p.k) {
+        float bv = s_bv[tid];
+        int bi = s_bi[tid];
+        for (int q = 1; q < FWTC_THREADS / FWTC_M; ++q) {
+            const float v = s_bv[q * FWTC_M + tid];
+            const int r = s_bi[q * FWTC_M + tid];
+            if (v < bv || (v == bv && r < bi)) {
+                bv = v;
+                bi = r;
+            }
+        }
+        best_v = bv;
+        best_i = bi;
     }
     if (tid < p.k) {
         p.part_val[(int64_t)blockIdx.x * p.ldk + tid] = best_v;
@@ -537,7 +591,7 @@ __global__ void __launch_bounds__(FWTC_THREADS, 1) fw_scan_tc(FwParams<float> p)
     __syncthreads();
     if (tid == 0) {
         double t = 0.0;
-        for (int w = 0; w < FWTC_THREADS / 32; ++w) t += s_gap[w];
+        for (int w = 0; w < FWTC_WARPS; ++w) t += s_gap[w];
         // a wait that ran out leaves the gap not a number (every wait is bounded)
         p.part_gap[blockIdx.x] = ok ? t : __longlong_as_double(0x7ff8000000000000LL);
     }

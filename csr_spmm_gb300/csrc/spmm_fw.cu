@@ -339,72 +339,88 @@ __device__ __forceinline__ void umma_tf32(uint32_t tmem, uint64_t a, uint64_t b,
         ::"r"(tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
-// The rows of a tile that one warp handles (tile rows warp, warp + 16, ...,
-// FWTC_RPW of them) and the first 32 entries of each, loaded ahead of their
-// use (while the MMAs run): lane j < FWTC_RPW holds row j's extents, lane l
-// holds entry l of every row.
+// The rows of a tile that one warp handles: tile rows 8 w .. 8 w + 7, four
+// lanes per row (lane l: row l / 4, entries l % 4, l % 4 + 4, ...), so that
+// the lanes of one store cover eight consecutive rows, whose 16-byte core
+// matrix rows lie in different shared-memory banks.  The first FWTC_STEPS
+// steps (4 entries of each row per step) are loaded ahead of their use,
+// while the MMAs run.
 constexpr int FWTC_WARPS = FWTC_THREADS / 32;
-constexpr int FWTC_RPW = FWTC_M / FWTC_WARPS;
+constexpr int FWTC_STEPS = 8;
+static_assert(FWTC_M == FWTC_WARPS * 8, "eight rows per warp");
 struct FwRows {
-    int s, e;                                    // lane j < FWTC_RPW: row j's entries [s, e)
-    int c[FWTC_RPW];
-    float v[FWTC_RPW];
+    int s, e;                                    // this lane's row: entries [s, e)
+    int c[FWTC_STEPS];
+    float v[FWTC_STEPS];
 };
 
-__device__ __forceinline__ void fw_rows_load(FwRows& R, const int* __restrict__ rp,
-                                             const int* __restrict__ ci,
-                                             const float* __restrict__ val, int r0, int nr) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+__device__ __forceinline__ void fw_rows_extents(FwRows& R, const int* __restrict__ rp, int r0,
+                                                int nr) {
+    const int r = (int)(threadIdx.x >> 5) * 8 + (int)((threadIdx.x & 31) >> 2);
     R.s = 0;
     R.e = 0;
-    if (lane < FWTC_RPW) {
-        const int r = warp + FWTC_WARPS * lane;
-        if (r < nr) {
-            R.s = rp[r0 + r];
-            R.e = rp[r0 + r + 1];
-        }
+    if (r < nr) {
+        R.s = rp[r0 + r];
+        R.e = rp[r0 + r + 1];
     }
+}
+
+__device__ __forceinline__ void fw_rows_entries(FwRows& R, const int* __restrict__ ci,
+                                                const float* __restrict__ val) {
+    const int sub = threadIdx.x & 3;
 #pragma unroll
-    for (int j = 0; j < FWTC_RPW; ++j) {
-        const int s = __shfl_sync(FULL, R.s, j), e = __shfl_sync(FULL, R.e, j);
-        const int q = s + lane;
-        R.c[j] = q < e ? ci[q] : -1;
-        R.v[j] = q < e ? val[q] : 0.f;
+    for (int t = 0; t < FWTC_STEPS; ++t) {
+        const int q = R.s + 4 * t + sub;
+        R.c[t] = q < R.e ? ci[q] : -1;
+        R.v[t] = q < R.e ? val[q] : 0.f;
     }
 }
 
 // Every run of equal columns in the warp's rows: f(row in tile, column, sum
 // of the run in stored order), called by the lane holding the run's first
-// entry.  The first 32 entries of each row come from R; longer rows load
-// the rest 32 at a time.  No block barrier: each warp touches only its rows.
+// entry.  Neighbouring entries of a row sit in neighbouring lanes of its
+// four; longer rows load their further steps here.  No block barrier: each
+// warp touches only its own rows.
 template <typename F>
 __device__ __forceinline__ void fw_rows_apply(const FwRows& R, const int* __restrict__ ci,
                                               const float* __restrict__ val, F f) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31, sub = lane & 3, g0 = lane & ~3;
+    const int r = (int)(threadIdx.x >> 5) * 8 + (lane >> 2);
+    const int steps = (__reduce_max_sync(FULL, (unsigned)(R.e - R.s)) + 3) / 4;
+    int last = -2;                               // the row's previous step's last column
 #pragma unroll
-    for (int j = 0; j < FWTC_RPW; ++j) {
-        const int s = __shfl_sync(FULL, R.s, j), e = __shfl_sync(FULL, R.e, j);
-        const int r = warp + FWTC_WARPS * j;
-        int last = -2;                           // the previous chunk's last column
-        for (int base = s; base < e; base += 32) {
-            const int q = base + lane;
-            int c = R.c[j];
-            float v = R.v[j];
-            if (base != s) {
-                c = q < e ? ci[q] : -1;
-                v = q < e ? val[q] : 0.f;
-            }
+    for (int t = 0; t < FWTC_STEPS; ++t) {
+        if (t < steps) {                         // warp-uniform
+            const int q = R.s + 4 * t + sub;
+            const int c = R.c[t];
             int prev = __shfl_up_sync(FULL, c, 1);
-            if (lane == 0) prev = last;
+            if (sub == 0) prev = last;
             int next = __shfl_down_sync(FULL, c, 1);
-            last = __shfl_sync(FULL, c, 31);
-            if (q < e && !(q > s && prev == c)) {
-                float sum = v;
-                if (lane == 31 && q + 1 < e) next = ci[q + 1];
-                if (q + 1 < e && next == c)      // a run: sum it in order
-                    for (int q2 = q + 1; q2 < e && ci[q2] == c; ++q2) sum += val[q2];
+            const int first_next = t + 1 < FWTC_STEPS ? __shfl_sync(FULL, R.c[(t + 1) % FWTC_STEPS], g0) : -2;
+            last = __shfl_sync(FULL, c, g0 + 3);
+            if (sub == 3) next = t + 1 < FWTC_STEPS ? first_next : (q + 1 < R.e ? ci[q + 1] : -2);
+            if (q < R.e && !(q > R.s && prev == c)) {
+                float sum = R.v[t];
+                if (q + 1 < R.e && next == c)    // a run: sum it in order
+                    for (int q2 = q + 1; q2 < R.e && ci[q2] == c; ++q2) sum += val[q2];
                 f(r, c, sum);
             }
+        }
+    }
+    // rows longer than the prefetched steps
+    for (int t = FWTC_STEPS; t < steps; ++t) {
+        const int q = R.s + 4 * t + sub;
+        const int c = q < R.e ? ci[q] : -1;
+        int prev = __shfl_up_sync(FULL, c, 1);
+        if (sub == 0) prev = last;
+        int next = __shfl_down_sync(FULL, c, 1);
+        last = __shfl_sync(FULL, c, g0 + 3);
+        if (sub == 3) next = q + 1 < R.e ? ci[q + 1] : -2;
+        if (q < R.e && !(q > R.s && prev == c)) {
+            float sum = val[q];
+            if (q + 1 < R.e && next == c)
+                for (int q2 = q + 1; q2 < R.e && ci[q2] == c; ++q2) sum += val[q2];
+            f(r, c, sum);
         }
     }
 }
@@ -446,7 +462,8 @@ __global__ void __launch_bounds__(FWTC_THREADS, 1) fw_scan_tc(FwParams<float> p)
     FwRows kr, tr;
     if ((int)blockIdx.x < ntiles) {
         const int r0 = blockIdx.x * FWTC_M;
-        fw_rows_load(kr, p.k2b_rp, p.k2b_ci, p.k2b_v, r0, min(FWTC_M, p.n - r0));
+        fw_rows_extents(kr, p.k2b_rp, r0, min(FWTC_M, p.n - r0));
+        fw_rows_entries(kr, p.k2b_ci, p.k2b_v);
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
@@ -497,12 +514,16 @@ __global__ void __launch_bounds__(FWTC_THREADS, 1) fw_scan_tc(FwParams<float> p)
                 "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                 ::"r"(smem_addr(&s_mbar)) : "memory");
         }
-        // while the MMAs run: this tile's T2 rows and the next tile's K2B rows
-        fw_rows_load(tr, p.t2_rp, p.t2_ci, p.t2_v, r0, nr);
+        // while the MMAs run: this tile's T2 and B rows, the next tile's K2B
+        // rows (all row extents first, so that their loads overlap)
+        FwRows br;
         const int next = tile + gridDim.x;
+        fw_rows_extents(tr, p.t2_rp, r0, nr);
+        fw_rows_extents(br, p.b_rp, r0, nr);
         if (next < ntiles)
-            fw_rows_load(kr, p.k2b_rp, p.k2b_ci, p.k2b_v, next * FWTC_M,
-                         min(FWTC_M, p.n - next * FWTC_M));
+            fw_rows_extents(kr, p.k2b_rp, next * FWTC_M, min(FWTC_M, p.n - next * FWTC_M));
+        fw_rows_entries(tr, p.t2_ci, p.t2_v);
+        if (next < ntiles) fw_rows_entries(kr, p.k2b_ci, p.k2b_v);
         // the MMAs' completion (phase iter & 1), bounded
         uint32_t done = 0;
         for (int it = 0; it < FWTC_WAIT_LIMIT && !done; ++it) {
@@ -541,9 +562,8 @@ __global__ void __launch_bounds__(FWTC_THREADS, 1) fw_scan_tc(FwParams<float> p)
             if (c >= 0 && c < p.k) sG[r * g.gstride + c] -= v;
         });
         __syncwarp();
-        {
-            FwRows br;
-            fw_rows_load(br, p.b_rp, p.b_ci, p.b_v, r0, nr);
+        if (__any_sync(FULL, br.e > br.s)) {     // most rows of B are empty
+            fw_rows_entries(br, p.b_ci, p.b_v);
             fw_rows_apply(br, p.b_ci, p.b_v, [&](int r, int c, float bv) {
                 if (c >= 0 && c < p.k && bv != 0.f)
                     gap += (double)bv * (double)sG[r * g.gstride + c];

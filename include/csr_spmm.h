@@ -168,13 +168,19 @@ spmm_status_t spmm_csr_squared_f64(spmm_handle_t h, double alpha,
  * are deterministic: no float atomics, and the gap is summed in binary64 in a
  * fixed order, then rounded to the element type.
  * Requires n, k >= 0 and valid CSR structures with column indices in [0, k)
- * (spmm_csr_check can verify them; the hot path does not), and t1's columns
- * ascending within each row, the page's convention (duplicates, if any, then
- * sit together and are added).
+ * (spmm_csr_check can verify them; the hot path does not), and columns
+ * ascending within each row of every matrix, the page's convention
+ * (duplicates, if any, then sit together and are added).
+ * binary32 with k <= 104 runs the contraction K2B t1 on the tensor cores:
+ * every value is split into two tf32 parts and each product is formed from
+ * three tf32 products (hi hi, hi lo, lo hi), exact in binary32 and short of
+ * the exact product by less than 2^-21 of |K2B[i, m]| |t1[m, c]|, with the
+ * sums accumulated in binary32; other scans sum K2B entry by entry with
+ * binary32 or binary64 fused multiply-adds.
  * Arrays may be NULL only when n == 0 (the n x k matrices) or k == 0 (t1,
  * min_val, min_idx); gap must always be valid.  Uses handle scratch, grown
  * with cudaMalloc: a dense, zero-padded copy of t1 (k rows of k rounded up to
- * 128 binary32 or 64 binary64 columns) and per-warp partial minima.  Asynchronous on `stream`;
+ * 128 binary32 or 64 binary64 columns) and per-block partial minima.  Asynchronous on `stream`;
  * SPMM_ERR_CUDA on a launch failure. */
 spmm_status_t spmm_fw_argmin_f32(spmm_handle_t h, int64_t n, int64_t k,
                                  const int32_t *k2b_row_ptr, const int32_t *k2b_col_idx,

@@ -155,3 +155,30 @@ def test_seacells_full_size(handle):
     """The SEACells-shaped scan bench.py times (200,000 cells, 100 archetypes)."""
     p = seacells_fw()
     check(p, run_fw(handle, p), "seacells_fw")
+
+
+def _with_adjacent_duplicates(mat, every):
+    """The same CSR matrix with every `every`-th stored entry repeated in
+    place (a duplicate column right after itself, half the value each), so
+    the sum of each row is unchanged but runs of equal columns appear."""
+    rp, ci, v = (np.asarray(x) for x in mat)
+    rows = np.repeat(np.arange(len(rp) - 1), np.diff(rp))
+    dup = (np.arange(len(ci)) % every) == 0
+    rep = np.where(dup, 2, 1)
+    ci2 = np.repeat(ci, rep)
+    v2 = np.repeat(np.where(dup, v / 2, v), rep).astype(v.dtype)
+    rows2 = np.repeat(rows, rep)
+    rp2 = np.zeros_like(rp)
+    np.cumsum(np.bincount(rows2, minlength=len(rp) - 1), out=rp2[1:])
+    return rp2.astype(rp.dtype), ci2.astype(ci.dtype), v2
+
+
+def test_long_rows_and_duplicates_on_the_tensor_core_path(handle):
+    """binary32, k = 100 (the tensor-core scan): K2B and T2 rows of 60
+    entries (past the 32 entries each warp loads ahead), runs of duplicate
+    columns in K2B, T2 and B, and a last tile of 37 rows."""
+    p = fw_random(3 * 128 + 37, 100, 60, seed=11)
+    q = FwProblem("dups", p.n, p.k, _with_adjacent_duplicates(p.k2b, 7), p.t1,
+                  _with_adjacent_duplicates(p.t2, 5), _with_adjacent_duplicates(p.b, 3))
+    assert np.diff(q.k2b[0]).max() > 64
+    check(q, run_fw(handle, q), "long rows with duplicates")

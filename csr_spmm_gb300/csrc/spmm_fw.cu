@@ -533,7 +533,18 @@ __global__ void __launch_bounds__(FWTC_THREADS, 1) fw_scan_tc(FwParams<float> p)
                 : "=r"(done) : "r"(smem_addr(&s_mbar)), "r"((uint32_t)(iter & 1)) : "memory");
         }
         ok = __syncthreads_and(done != 0);
-        if (!ok) break;
+        if (!ok) {
+            // the MMAs may still be running: wait once more (bounded) before
+            // the tensor memory is freed below
+            for (int it = 0; it < FWTC_WAIT_LIMIT && !done; ++it) {
+                asm volatile(
+                    "{\n .reg .pred q;\n mbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2;\n"
+                    " selp.u32 %0, 1, 0, q;\n}\n"
+                    : "=r"(done) : "r"(smem_addr(&s_mbar)), "r"((uint32_t)(iter & 1)) : "memory");
+            }
+            __syncthreads();
+            break;
+        }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         // accumulator -> gradient tile: warp w reads lanes 32 (w % 4) .. + 31
         // (one row per thread), column chunks w / 4, w / 4 + 4, ...

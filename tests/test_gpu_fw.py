@@ -182,3 +182,12 @@ def test_long_rows_and_duplicates_on_the_tensor_core_path(handle):
                   _with_adjacent_duplicates(p.t2, 5), _with_adjacent_duplicates(p.b, 3))
     assert np.diff(q.k2b[0]).max() > 64
     check(q, run_fw(handle, q), "long rows with duplicates")
+
+
+@pytest.mark.parametrize("k", [1, 8, 9, 16, 17, 103, 104, 105])
+def test_tensor_core_k_bounds(handle, k):
+    """The tensor-core scan's k geometry (k step 8, N a multiple of 16, at most
+    104 columns) at and around its edges, and the first k past it (the
+    CUDA-core scan), on a ragged last tile of rows."""
+    p = fw_random(300, k, min(k, 24), seed=100 + k)
+    check(p, run_fw(handle, p), f"k={k}")

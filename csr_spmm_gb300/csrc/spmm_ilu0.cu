@@ -494,7 +494,7 @@ __device__ bool factor_row_short(const Ilu0Params<T>& p, int i, int s, int e, in
 // dependents need no ordering; its pivot rows' values are their published
 // values, waited for while they are still the sentinel.  No fence and no
 // acquire-release pair lies on the path from one row to the next
-// (measured on GB300, the 707 x 707 Laplacian in binary64: 5.40 ms per call
+// (measured on GB300, the 707 x 707 Laplacian in binary64: 5.07 ms per call
 // against 5.76 ms with acquire-release count-downs and the values read after
 // the acquire; bit for bit the same factors).
 template <typename T>

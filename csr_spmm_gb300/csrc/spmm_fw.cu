@@ -482,6 +482,15 @@ __global__ void __launch_bounds__(FWTC_THREADS, 1) fw_scan_tc(FwParams<float> p)
     int iter = 0;
     for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++iter) {
         const int r0 = tile * FWTC_M, nr = min(FWTC_M, p.n - r0);
+        // the row extents that the loads during the MMAs need, requested now
+        // so that they have arrived by then: this tile's T2 and B rows, the
+        // next tile's K2B rows
+        FwRows br, nk;
+        const int next = tile + gridDim.x;
+        fw_rows_extents(tr, p.t2_rp, r0, nr);
+        fw_rows_extents(br, p.b_rp, r0, nr);
+        if (next < ntiles)
+            fw_rows_extents(nk, p.k2b_rp, next * FWTC_M, min(FWTC_M, p.n - next * FWTC_M));
         for (size_t i = tid; i < 2 * g.a_bytes / 16; i += FWTC_THREADS)
             reinterpret_cast<float4*>(tc_smem)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         __syncthreads();
@@ -514,16 +523,13 @@ __global__ void __launch_bounds__(FWTC_THREADS, 1) fw_scan_tc(FwParams<float> p)
                 "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                 ::"r"(smem_addr(&s_mbar)) : "memory");
         }
-        // while the MMAs run: this tile's T2 and B rows, the next tile's K2B
-        // rows (all row extents first, so that their loads overlap)
-        FwRows br;
-        const int next = tile + gridDim.x;
-        fw_rows_extents(tr, p.t2_rp, r0, nr);
-        fw_rows_extents(br, p.b_rp, r0, nr);
-        if (next < ntiles)
-            fw_rows_extents(kr, p.k2b_rp, next * FWTC_M, min(FWTC_M, p.n - next * FWTC_M));
+        // while the MMAs run: this tile's T2 rows and the next tile's K2B rows
         fw_rows_entries(tr, p.t2_ci, p.t2_v);
-        if (next < ntiles) fw_rows_entries(kr, p.k2b_ci, p.k2b_v);
+        if (next < ntiles) {
+            kr.s = nk.s;
+            kr.e = nk.e;
+            fw_rows_entries(kr, p.k2b_ci, p.k2b_v);
+        }
         // the MMAs' completion (phase iter & 1), bounded
         uint32_t done = 0;
         for (int it = 0; it < FWTC_WAIT_LIMIT && !done; ++it) {

@@ -425,6 +425,32 @@ __device__ __forceinline__ void fw_rows_apply(const FwRows& R, const int* __rest
     }
 }
 
+// The same walk over entries read through col(q) and val(q) (B's entries,
+// staged in shared memory while the MMAs run).
+constexpr int FWTC_BSTAGE = 512;                 // B entries of a tile staged at most
+template <typename C, typename V, typename F>
+__device__ __forceinline__ void fw_rows_apply_by(const FwRows& R, C col, V valf, F f) {
+    const int lane = threadIdx.x & 31, sub = lane & 3, g0 = lane & ~3;
+    const int r = (int)(threadIdx.x >> 5) * 8 + (lane >> 2);
+    const int steps = (__reduce_max_sync(FULL, (unsigned)(R.e - R.s)) + 3) / 4;
+    int last = -2;
+    for (int t = 0; t < steps; ++t) {
+        const int q = R.s + 4 * t + sub;
+        const int c = q < R.e ? col(q) : -1;
+        int prev = __shfl_up_sync(FULL, c, 1);
+        if (sub == 0) prev = last;
+        int next = __shfl_down_sync(FULL, c, 1);
+        last = __shfl_sync(FULL, c, g0 + 3);
+        if (sub == 3) next = q + 1 < R.e ? col(q + 1) : -2;
+        if (q < R.e && !(q > R.s && prev == c)) {
+            float sum = valf(q);
+            if (q + 1 < R.e && next == c)
+                for (int q2 = q + 1; q2 < R.e && col(q2) == c; ++q2) sum += valf(q2);
+            f(r, c, sum);
+        }
+    }
+}
+
 __global__ void __launch_bounds__(FWTC_THREADS, 1) fw_scan_tc(FwParams<float> p) {
     extern __shared__ __align__(1024) unsigned char tc_smem[];
     __shared__ __align__(8) uint64_t s_mbar;
@@ -432,6 +458,8 @@ __global__ void __launch_bounds__(FWTC_THREADS, 1) fw_scan_tc(FwParams<float> p)
     __shared__ float s_bv[FWTC_THREADS];
     __shared__ int s_bi[FWTC_THREADS];
     __shared__ double s_gap[FWTC_WARPS];
+    __shared__ int s_bcol[FWTC_BSTAGE];          // the tile's B entries, staged
+    __shared__ float s_bval[FWTC_BSTAGE];
     const FwTcGeo g = fwtc_geo(p.k);
     unsigned char* sAh = tc_smem;
     unsigned char* sAl = tc_smem + g.a_bytes;
@@ -491,6 +519,7 @@ __global__ void __launch_bounds__(FWTC_THREADS, 1) fw_scan_tc(FwParams<float> p)
         fw_rows_extents(br, p.b_rp, r0, nr);
         if (next < ntiles)
             fw_rows_extents(nk, p.k2b_rp, next * FWTC_M, min(FWTC_M, p.n - next * FWTC_M));
+        const int b0 = p.b_rp[r0], b1 = p.b_rp[r0 + nr];
         for (size_t i = tid; i < 2 * g.a_bytes / 16; i += FWTC_THREADS)
             reinterpret_cast<float4*>(tc_smem)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         __syncthreads();
@@ -523,12 +552,18 @@ __global__ void __launch_bounds__(FWTC_THREADS, 1) fw_scan_tc(FwParams<float> p)
                 "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                 ::"r"(smem_addr(&s_mbar)) : "memory");
         }
-        // while the MMAs run: this tile's T2 rows and the next tile's K2B rows
+        // while the MMAs run: this tile's T2 rows, the next tile's K2B rows,
+        // and this tile's B entries into shared memory
         fw_rows_entries(tr, p.t2_ci, p.t2_v);
         if (next < ntiles) {
             kr.s = nk.s;
             kr.e = nk.e;
             fw_rows_entries(kr, p.k2b_ci, p.k2b_v);
+        }
+        const bool bstaged = b1 - b0 <= FWTC_BSTAGE;
+        if (bstaged && b0 + tid < b1) {
+            s_bcol[tid] = p.b_ci[b0 + tid];
+            s_bval[tid] = p.b_v[b0 + tid];
         }
         // the MMAs' completion (phase iter & 1), bounded
         uint32_t done = 0;
@@ -580,11 +615,16 @@ __global__ void __launch_bounds__(FWTC_THREADS, 1) fw_scan_tc(FwParams<float> p)
         });
         __syncwarp();
         if (__any_sync(FULL, br.e > br.s)) {     // most rows of B are empty
-            fw_rows_entries(br, p.b_ci, p.b_v);
-            fw_rows_apply(br, p.b_ci, p.b_v, [&](int r, int c, float bv) {
+            const auto gap_add = [&](int r, int c, float bv) {
                 if (c >= 0 && c < p.k && bv != 0.f)
                     gap += (double)bv * (double)sG[r * g.gstride + c];
-            });
+            };
+            if (bstaged)
+                fw_rows_apply_by(br, [&](int q) { return s_bcol[q - b0]; },
+                                 [&](int q) { return s_bval[q - b0]; }, gap_add);
+            else
+                fw_rows_apply_by(br, [&](int q) { return p.b_ci[q]; },
+                                 [&](int q) { return p.b_v[q]; }, gap_add);
         }
         __syncthreads();
         // column mcol's minimum over rows 32 mgrp .. + 31 of the tile, ascending

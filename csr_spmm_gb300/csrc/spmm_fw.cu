@@ -541,12 +541,14 @@ __global__ void __launch_bounds__(FWTC_THREADS, 1) fw_scan_tc(FwParams<float> p)
         if (tid == 0) {
             const uint32_t ah = smem_addr(sAh), al = smem_addr(sAl);
             const uint32_t bh = smem_addr(sBh), bl = smem_addr(sBl);
+            // a k step moves each descriptor's start by 256 bytes (16 units)
+            const uint64_t dah = umma_desc(ah, 128, sbo), dal = umma_desc(al, 128, sbo);
+            const uint64_t dbh = umma_desc(bh, 128, sbo), dbl = umma_desc(bl, 128, sbo);
             for (int s = 0; s < g.kp / 8; ++s) {
-                const uint32_t ko = (uint32_t)s * 256;     // two core matrices per k step
-                umma_tf32(tmem, umma_desc(ah + ko, 128, sbo), umma_desc(bh + ko, 128, sbo), idesc,
-                          s > 0);
-                umma_tf32(tmem, umma_desc(ah + ko, 128, sbo), umma_desc(bl + ko, 128, sbo), idesc, 1);
-                umma_tf32(tmem, umma_desc(al + ko, 128, sbo), umma_desc(bh + ko, 128, sbo), idesc, 1);
+                const uint64_t ko = (uint64_t)s * 16;
+                umma_tf32(tmem, dah + ko, dbh + ko, idesc, s > 0);
+                umma_tf32(tmem, dah + ko, dbl + ko, idesc, 1);
+                umma_tf32(tmem, dal + ko, dbh + ko, idesc, 1);
             }
             asm volatile(
                 "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
@@ -630,11 +632,23 @@ __global__ void __launch_bounds__(FWTC_THREADS, 1) fw_scan_tc(FwParams<float> p)
         // column mcol's minimum over rows 32 mgrp .. + 31 of the tile, ascending
         if (mcol < p.k) {
             const int ra = mgrp * 32, rb = min(nr, ra + 32);
-            for (int r = ra; r < rb; ++r) {
-                const float v = sG[r * g.gstride + mcol];
-                if (v < best_v) {
-                    best_v = v;
-                    best_i = r0 + r;
+            if (rb - ra == 32) {                 // a full slice: loads first, then the compares in order
+                float vs[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) vs[j] = sG[(ra + j) * g.gstride + mcol];
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (vs[j] < best_v) {
+                        best_v = vs[j];
+                        best_i = r0 + ra + j;
+                    }
+            } else {
+                for (int r = ra; r < rb; ++r) {
+                    const float v = sG[r * g.gstride + mcol];
+                    if (v < best_v) {
+                        best_v = v;
+                        best_i = r0 + r;
+                    }
                 }
             }
         }

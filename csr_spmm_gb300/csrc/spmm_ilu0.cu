@@ -135,14 +135,12 @@ __device__ __forceinline__ double sub_rn(double a, double b) { return __dsub_rn(
 
 // 1. lower entries per row, dependents per row, the first ready rows; and
 //    for each lower entry (i, k) where row k keeps its pivot a_kk and where
-//    it ends (structure only: the factorisation then needs no search); the
-//    published values are set to the sentinel
+//    it ends (structure only: the factorisation then needs no search)
 template <typename T>
 __global__ void __launch_bounds__(256) ilu0_count(Ilu0Params<T> p) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= p.n) return;
-    // the row's published values start as the sentinel, its level as -1
-    for (int q = p.rp[i]; q < p.rp[i + 1]; ++q) set_sentinel(p.pub + q);
+    // the row's level starts as -1 (its published values: ilu0_records)
     p.done[i] = 0;
     if (p.depth) p.depth[i] = -1;
     int lower = 0;
@@ -248,6 +246,7 @@ __global__ void __launch_bounds__(256) ilu0_fill(Ilu0Params<T> p) {
 //     positions, dependents) in one 256-byte record, so that it arrives in
 //     one round trip and can be fetched ahead for the rows a row readies.
 //     Rows of more than 16 entries or 14 dependents get no record (-1).
+//     The row's published values are set to the sentinel here.
 template <typename T>
 __global__ void __launch_bounds__(256) ilu0_records(Ilu0Params<T> p) {
     const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -271,6 +270,9 @@ __global__ void __launch_bounds__(256) ilu0_records(Ilu0Params<T> p) {
     if (q == ILU0_REC_LANES - 2) r.w = s;
     if (q == ILU0_REC_LANES - 1) r.w = big ? -1 : (len | (nd << 8));
     p.rec[i64 * ILU0_REC_LANES + q] = r;
+    // the row's published values start as the sentinel (16 lanes per row,
+    // consecutive entries)
+    for (int u = s + q; u < e; u += ILU0_REC_LANES) set_sentinel(p.pub + u);
 }
 
 __device__ __forceinline__ void stop(int* abort, int* status, int bit) {

@@ -64,7 +64,13 @@ struct Ilu0Params {
     int* finished;         // rows factored so far (termination and progress)
     int* status;           // caller's: 0, or ILU0 failure bits
 };
-constexpr int ILU0_THREADS = 256;
+// Factorisation block, one per SM: four warps (the 707 x 707 Laplacian in
+// binary64 on GB300: 5.01 ms with 128 threads, 5.04 with 192, 5.06 with 256,
+// 5.10 with 384, 5.31 with 512; fewer idle warps polling the queue).
+#ifndef SPMM_ILU0_THREADS
+#define SPMM_ILU0_THREADS 128
+#endif
+constexpr int ILU0_THREADS = SPMM_ILU0_THREADS;
 // A row's structure record: ILU0_REC_LANES int4 words, lane q holding
 // {column of entry q, pivot position and end of row k for a lower entry q,
 // dependent q}; lane 14's last word is the row's first entry, lane 15's its

@@ -269,11 +269,14 @@ __global__ void __launch_bounds__(FW_THREADS) fw_scan(FwParams<T> p) {
 // binary32, the dropped A_lo t1_lo and rounding residues below 2^-21 of
 // |a||t|, with binary32 accumulation in tensor memory.  One thread issues
 // the MMAs; completion is signalled on an mbarrier; the 128 x N accumulator
-// is read back with tcgen05.ld (warp w: lanes 32w .. 32w + 31, one row per
-// thread) into a shared-memory tile where T2 is subtracted (duplicate
-// columns summed in stored order first, as in the CUDA-core scan), B's
-// entries add to the gap, and thread c keeps column c's minimum over the
-// block's rows in ascending order (strict <: lowest row).  Operand layout:
+// is read back with tcgen05.ld (warp w: lanes 32 (w % 4) .. + 31, one row
+// per thread, column chunks by w / 4) into a shared-memory tile where T2 is
+// subtracted (duplicate columns summed in stored order first, as in the
+// CUDA-core scan), B's entries add to the gap, and four groups of threads
+// keep each column's minimum over 32-row slices of the block's rows in
+// ascending order (strict <: lowest row), combined at the end by value,
+// then row.  While the MMAs run, the tile's T2 rows, the next tile's K2B
+// rows and the tile's B entries are loaded.  Operand layout:
 // K-major, no swizzle, 8-row x 16-byte core matrices; within an 8-row group
 // the k direction's core matrices are 128 bytes apart (the descriptor's
 // leading byte offset), and the groups kp * 32 bytes apart (stride offset).

@@ -12,7 +12,10 @@
 // owns a row and 32 x (16 / sizeof(T)) columns of it per pass; warps take rows
 // in increasing order, so a lane's strict < keeps the lowest row of its share,
 // and the cross-warp reduction breaks value ties on the row index.  No float
-// atomics: the result does not depend on scheduling.
+// atomics: the result does not depend on scheduling.  Binary32 scans with
+// k <= 104 take the tensor-core scan instead (fw_scan_tc, below): the same
+// outputs, with the contraction K2B t1 done by tcgen05 MMAs a tile of 128
+// rows at a time.
 #include <cfloat>
 
 #include "spmm_device.cuh"

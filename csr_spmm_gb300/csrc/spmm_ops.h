@@ -66,7 +66,8 @@ struct Ilu0Params {
 };
 // Factorisation block, one per SM: four warps (the 707 x 707 Laplacian in
 // binary64 on GB300: 5.01 ms with 128 threads, 5.04 with 192, 5.06 with 256,
-// 5.10 with 384, 5.31 with 512; fewer idle warps polling the queue).
+// 5.10 with 384, 5.31 with 512: fewer idle warps polling the queue; but
+// 5.19 with 96 and 6.21 with 64, too few warps for the widest levels).
 #ifndef SPMM_ILU0_THREADS
 #define SPMM_ILU0_THREADS 128
 #endif

@@ -99,3 +99,16 @@ def test_roofline_names_the_binding_unit():
     assert abs(r["frac"] - 1.0 / 1.2) < 1e-3 and r["hbm_frac"] < r["frac"]
     p64.beta = 0.5                                           # general beta: a multiply more
     assert bench.fp64_pipe_ops(p64) == p64.nnz * 32 + 2 * p64.m * 32
+
+
+def test_config_runs_cover_every_product_configuration_and_the_l2_window():
+    """The line's `configs` object times the five product configurations once
+    each, without the window, and SEACells once more with the persisting-L2
+    window on B (its 80 MB B fits the set-aside)."""
+    keys = [k for k, _, _ in bench.CONFIG_RUNS]
+    assert len(keys) == len(set(keys))
+    plain = [(k, w) for k, w, win in bench.CONFIG_RUNS if not win]
+    assert [w for _, w in plain] == list(bench.PRODUCT_CONFIGS)
+    assert all(k == w for k, w in plain)
+    windowed = [(k, w) for k, w, win in bench.CONFIG_RUNS if win]
+    assert windowed == [("seacells_knn_l2_window", "seacells_knn")]

@@ -402,7 +402,8 @@ __device__ __forceinline__ void fw_rows_apply(const FwRows& R, const int* __rest
             int prev = __shfl_up_sync(FULL, c, 1);
             if (sub == 0) prev = last;
             int next = __shfl_down_sync(FULL, c, 1);
-            const int first_next = t + 1 < FWTC_STEPS ? __shfl_sync(FULL, R.c[(t + 1) % FWTC_STEPS], g0) : -2;
+            const int first_next =
+                t + 1 < FWTC_STEPS ? __shfl_sync(FULL, R.c[(t + 1) % FWTC_STEPS], g0) : -2;
             last = __shfl_sync(FULL, c, g0 + 3);
             if (sub == 3) next = t + 1 < FWTC_STEPS ? first_next : (q + 1 < R.e ? ci[q + 1] : -2);
             if (q < R.e && !(q > R.s && prev == c)) {
@@ -638,7 +639,7 @@ __global__ void __launch_bounds__(FWTC_THREADS, 1) fw_scan_tc(FwParams<float> p)
         // column mcol's minimum over rows 32 mgrp .. + 31 of the tile, ascending
         if (mcol < p.k) {
             const int ra = mgrp * 32, rb = min(nr, ra + 32);
-            if (rb - ra == 32) {                 // a full slice: loads first, then the compares in order
+            if (rb - ra == 32) {                 // a full slice: loads first, compares in order
                 float vs[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) vs[j] = sG[(ra + j) * g.gstride + mcol];
@@ -658,7 +659,7 @@ __global__ void __launch_bounds__(FWTC_THREADS, 1) fw_scan_tc(FwParams<float> p)
                 }
             }
         }
-        __syncthreads();                         // the tile is read before the next one overwrites it
+        __syncthreads();                         // the tile is read before the next overwrites it
     }
     // each column's four candidates (value, then lower row: a total order)
     s_bv[tid] = best_v;
@@ -694,7 +695,8 @@ __global__ void __launch_bounds__(FWTC_THREADS, 1) fw_scan_tc(FwParams<float> p)
     }
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     if (warp == 0)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(g.tcols));
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                     ::"r"(tmem), "r"(g.tcols));
 }
 
 // Warps 0 .. k-1: one column each; lanes take blocks lane, lane + 32, ...

@@ -466,19 +466,25 @@ def run_reference(args):
     return 0
 
 
-def pipelined_e2e_ms(torch, dev, p, call_on, steps, host, dev0):
+def pipelined_e2e_ms(torch, dev, p, call_on, steps, host, dev0, nbuf=3, trials=1):
     """Time `steps` end-to-end steps (inputs uploaded from pinned host memory,
-    the product, the result downloaded) with two device copies of every
-    buffer and uploads, products and downloads on three streams.  Returns the
-    milliseconds from the first upload to the last download."""
+    the product, the result downloaded) with `nbuf` device copies of every
+    buffer and uploads, products and downloads on three streams, `trials`
+    times.  Returns each trial's milliseconds from the first upload to the
+    last download.
+
+    Step i's upload waits for the download of step i - nbuf (the set it
+    reuses).  With two sets that wait leaves the link carrying one direction
+    for part of every step; with three, uploads run back to back and the
+    link carries both directions nearly all the time."""
     h_rp, h_ci, h_va, h_B, h_C0 = host
-    sets = [dev0, tuple(torch.empty_like(t) for t in dev0)]
-    h_out = [torch.empty(dev0[4].shape, dtype=dev0[4].dtype).pin_memory() for _ in range(2)]
+    sets = [dev0] + [tuple(torch.empty_like(t) for t in dev0) for _ in range(nbuf - 1)]
+    h_out = [torch.empty(dev0[4].shape, dtype=dev0[4].dtype).pin_memory() for _ in range(nbuf)]
     s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
-    out_done = [None, None]
+    out_done = [None] * nbuf
 
     def step(i):
-        b = i % 2
+        b = i % nbuf
         t_rp, t_ci, t_va, t_B, t_C = sets[b]
         with torch.cuda.stream(s_in):
             if out_done[b] is not None:
@@ -501,17 +507,20 @@ def pipelined_e2e_ms(torch, dev, p, call_on, steps, host, dev0):
             out_done[b] = torch.cuda.Event()
             out_done[b].record(s_out)
 
-    for i in range(4):
+    for i in range(max(4, nbuf + 1)):
         step(i)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(s_in)
-    for i in range(steps):
-        step(i)
-    s_out.wait_event(out_done[(steps - 1) % 2])
-    e1.record(s_out)
-    torch.cuda.synchronize()
-    return e0.elapsed_time(e1)
+    out = []
+    for _ in range(trials):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s_in)
+        for i in range(steps):
+            step(i)
+        s_out.wait_event(out_done[(steps - 1) % nbuf])
+        e1.record(s_out)
+        torch.cuda.synchronize()
+        out.append(e0.elapsed_time(e1))
+    return out
 
 
 def run_ours(args):
@@ -712,18 +721,19 @@ def run_ours(args):
         torch.cuda.synchronize()
         e_ms = e0.elapsed_time(e1)
         e_ms = max_over_ranks(e_ms, pg, dev)
-        # Pipelined: the same steps with two device copies of the inputs and
+        # Pipelined: the same steps with three device copies of the inputs and
         # outputs, uploads, products and downloads on three streams, so that
-        # step i + 1 uploads while step i computes and step i - 1 downloads
+        # step i + 1 uploads while step i computes and earlier steps download
         # (the host link carries both directions at once).  Every step still
         # copies all its inputs in and its result out.
-        p_ms = pipelined_e2e_ms(torch, dev, p, call_on, e_steps,
-                                (h_rp, h_ci, h_va, h_B, h_C0), (rp, ci, va, B, C))
-        p_ms = max_over_ranks(p_ms, pg, dev)
+        # The host link is shared with the machine's other work, so a single
+        # run can land on a busy stretch: three runs, the median reported.
+        p_trials = pipelined_e2e_ms(torch, dev, p, call_on, e_steps,
+                                    (h_rp, h_ci, h_va, h_B, h_C0), (rp, ci, va, B, C), trials=3)
+        p_ms = max_over_ranks(statistics.median(p_trials), pg, dev)
         # the faster of the two schedules is the end-to-end figure; both are
-        # reported (on the wide-N workload the link carries 1.1 GB per step
-        # and overlapping directions gains nothing)
-        best_ms, sched = min((p_ms, "double-buffered device inputs and outputs; upload, "
+        # reported
+        best_ms, sched = min((p_ms, "three device copies of the inputs and outputs; upload, "
                                     "product and download on three streams"),
                              (e_ms, "one stream: upload, product, download in order"))
         e2e = {"value": round(flops * e_steps * world / (best_ms / 1e3) / 1e9, 3),
@@ -731,6 +741,7 @@ def run_ours(args):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": round(best_ms / e_steps, 4), "steps": e_steps, "schedule": sched,
                "ms_per_step_pipelined": round(p_ms / e_steps, 4),
+               "ms_per_step_pipelined_runs": [round(x / e_steps, 4) for x in p_trials],
                "ms_per_step_one_stream": round(e_ms / e_steps, 4)}
     h.close()
 

@@ -15,7 +15,8 @@ from __future__ import annotations
 
 from ._lib import (EXPORTED, SPMM_ERR_ALLOC, SPMM_ERR_CUDA, SPMM_ERR_DIMENSION_MISMATCH,
                    SPMM_ERR_INVALID_ARGUMENT, SPMM_ERR_INVALID_CSR, SPMM_ERR_NULL_POINTER,
-                   SPMM_ERR_UNSUPPORTED_DEVICE, SPMM_OK, SpmmError, library, spmm_create,
+                   SPMM_ERR_TOO_LARGE, SPMM_ERR_UNSUPPORTED_DEVICE, SPMM_OK, SpmmError,
+                   library, spmm_create,
                    spmm_csr_check, spmm_csr_f32, spmm_csr_f32_noalloc, spmm_csr_f64,
                    spmm_destroy, spmm_get_profile, spmm_plan_create, spmm_plan_csr_f32,
                    spmm_plan_csr_f64, spmm_plan_csr_squared_f32, spmm_plan_csr_squared_f64,

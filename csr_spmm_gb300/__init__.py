@@ -67,8 +67,32 @@ class Handle:
             pass
 
 
-def _ptr(t):
-    return 0 if t is None else t.data_ptr()
+def _ptr(t, device: int):
+    """Device address of a tensor the library reads or writes (0 for None).
+    Refused here, because its address would reach a kernel as device memory
+    of the call's GPU: a tensor not on CUDA, a tensor on another GPU than
+    the handle's, and a 1-D array whose entries are not contiguous."""
+    if t is None:
+        return 0
+    if not t.is_cuda:
+        raise ValueError(f"expected a CUDA tensor, got one on {t.device}")
+    if t.device.index != device:
+        raise ValueError(f"tensor on {t.device}, but the handle is on cuda:{device}")
+    if t.dim() <= 1 and not t.is_contiguous():
+        raise ValueError("1-D arrays (row_ptr, col_idx, values) must be contiguous")
+    return t.data_ptr()
+
+
+def _check_dense(B, C, b_rows: int, m: int, n: int, dtype) -> None:
+    """B holds at least b_rows x n and C at least m x n elements, row-major with
+    unit column stride, all of the values' dtype."""
+    if C.dim() != 2 or B.dim() != 2 or C.stride(1) != 1 or B.stride(1) != 1:
+        raise ValueError("B and C must be 2-D with unit column stride")
+    if B.shape[0] < b_rows or B.shape[1] < n or C.shape[0] < m or C.shape[1] < n:
+        raise ValueError(f"B {tuple(B.shape)} or C {tuple(C.shape)} smaller than the "
+                         f"product's {b_rows} x {n} and {m} x {n}")
+    if not (B.dtype == C.dtype == dtype):
+        raise TypeError("values, B and C must share one dtype")
 
 
 def spmm(handle: Handle, alpha: float, row_ptr, col_idx, values, k: int, B, beta: float, C,
@@ -90,11 +114,14 @@ def spmm(handle: Handle, alpha: float, row_ptr, col_idx, values, k: int, B, beta
         raise TypeError("row_ptr and col_idx must be int32")
     if not (values.dtype == B.dtype == C.dtype):
         raise TypeError("values, B and C must share one dtype")
+    if col_idx.numel() != values.numel():
+        raise ValueError("col_idx and values must hold the same number of entries")
+    d = handle.device
+    a_rp, a_ci, a_va, a_b, a_c = (_ptr(x, d) for x in (row_ptr, col_idx, values, B, C))
     st = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
     ldb = B.stride(0) if B.shape[0] > 1 else max(1, n)
     ldc = C.stride(0) if C.shape[0] > 1 else max(1, n)
-    args = (handle.ptr, alpha, _ptr(row_ptr), _ptr(col_idx), _ptr(values), m, k, _ptr(B), ldb, n,
-            beta, _ptr(C), ldc, st)
+    args = (handle.ptr, alpha, a_rp, a_ci, a_va, m, k, a_b, ldb, n, beta, a_c, ldc, st)
     if values.dtype == torch.float32:
         spmm_csr_f32(*args)
     elif values.dtype == torch.float64:
@@ -121,11 +148,14 @@ def spmm_squared(handle: Handle, alpha: float, row_ptr, col_idx, values, B, beta
         raise TypeError("row_ptr and col_idx must be int32")
     if not (values.dtype == B.dtype == C.dtype):
         raise TypeError("values, B and C must share one dtype")
+    if col_idx.numel() != values.numel():
+        raise ValueError("col_idx and values must hold the same number of entries")
+    d = handle.device
+    a_rp, a_ci, a_va, a_b, a_c = (_ptr(x, d) for x in (row_ptr, col_idx, values, B, C))
     st = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
     ldb = B.stride(0) if B.shape[0] > 1 else max(1, n)
     ldc = C.stride(0) if C.shape[0] > 1 else max(1, n)
-    args = (handle.ptr, alpha, _ptr(row_ptr), _ptr(col_idx), _ptr(values), m, _ptr(B), ldb, n,
-            beta, _ptr(C), ldc, st)
+    args = (handle.ptr, alpha, a_rp, a_ci, a_va, m, a_b, ldb, n, beta, a_c, ldc, st)
     if values.dtype == torch.float32:
         spmm_csr_squared_f32(*args)
     elif values.dtype == torch.float64:
@@ -147,16 +177,19 @@ def fw_argmin(handle: Handle, k: int, k2b, t1, t2, bmat, stream=None):
     for mat, rows in ((k2b, n), (t1, k), (t2, n), (bmat, n)):
         if int(mat[0].numel()) != rows + 1 or mat[2].dtype != dt:
             raise ValueError("CSR triples must be (row_ptr [rows+1], col_idx, values) of one dtype")
+        if mat[1].numel() != mat[2].numel():
+            raise ValueError("col_idx and values must hold the same number of entries")
         if mat[0].dtype != torch.int32 or mat[1].dtype != torch.int32:
             raise TypeError("row_ptr and col_idx must be int32")
+    d = handle.device
+    mats = [tuple(_ptr(x, d) for x in m) for m in (k2b, t1, t2, bmat)]
     dev = k2b[0].device
     min_val = torch.empty(max(k, 1), dtype=dt, device=dev)
     min_idx = torch.empty(max(k, 1), dtype=torch.int32, device=dev)
     gap = torch.empty(1, dtype=dt, device=dev)
     st = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
-    ptrs = lambda m: tuple(_ptr(x) for x in m)  # noqa: E731
-    spmm_fw_argmin(handle.ptr, n, k, ptrs(k2b), ptrs(t1), ptrs(t2), ptrs(bmat), _ptr(min_val),
-                   _ptr(min_idx), _ptr(gap), f64=dt == torch.float64, stream=st)
+    spmm_fw_argmin(handle.ptr, n, k, *mats, _ptr(min_val, d), _ptr(min_idx, d), _ptr(gap, d),
+                   f64=dt == torch.float64, stream=st)
     return min_val[:k], min_idx[:k], gap
 
 
@@ -174,12 +207,16 @@ def ilu0(handle: Handle, row_ptr, col_idx, values, with_depth: bool = False, str
         raise TypeError("row_ptr and col_idx must be int32")
     if values.dtype not in (torch.float32, torch.float64):
         raise TypeError("values must be float32 or float64")
+    if col_idx.numel() != values.numel():
+        raise ValueError("col_idx and values must hold the same number of entries")
+    d = handle.device
+    a_rp, a_ci, a_va = (_ptr(x, d) for x in (row_ptr, col_idx, values))
     dev = values.device
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     depth = torch.empty(max(n, 1), dtype=torch.int32, device=dev) if with_depth else None
     st = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
-    spmm_ilu0(handle.ptr, n, int(values.numel()), _ptr(row_ptr), _ptr(col_idx), _ptr(values),
-              _ptr(depth), _ptr(status), f64=values.dtype == torch.float64, stream=st)
+    spmm_ilu0(handle.ptr, n, int(values.numel()), a_rp, a_ci, a_va, _ptr(depth, d),
+              _ptr(status, d), f64=values.dtype == torch.float64, stream=st)
     code = int(status.item())                          # synchronises
     if code:
         why = "zero or missing pivot" if code & ILU0_SINGULAR else "a dependency wait ran out"
@@ -196,9 +233,14 @@ class Plan:
         self.m = int(row_ptr.numel()) - 1
         self.k, self.n = int(k), int(n)
         self.dtype = dtype
+        if dtype not in (torch.float32, torch.float64):
+            raise TypeError("dtype must be float32 or float64")
+        if row_ptr.dtype != torch.int32:
+            raise TypeError("row_ptr must be int32")
         es = 4 if dtype == torch.float32 else 8
+        a_rp = _ptr(row_ptr, handle.device)
         st = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
-        self.ptr = spmm_plan_create(handle.ptr, _ptr(row_ptr), self.m, self.k, self.n, es, st)
+        self.ptr = spmm_plan_create(handle.ptr, a_rp, self.m, self.k, self.n, es, st)
 
     def order_rows(self, row_ptr, col_idx, stream=None, automatic=True) -> bool:
         """Process rows in breadth-first order of A's pattern: where that raises
@@ -206,32 +248,42 @@ class Plan:
         (automatic=False, spmm_plan_order_rows).  Returns whether the order
         was changed."""
         import torch
+        d = self.handle.device
+        a_rp, a_ci = _ptr(row_ptr, d), _ptr(col_idx, d)
         st = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
         if automatic:
-            return spmm_plan_order_rows_auto(self.ptr, _ptr(row_ptr), _ptr(col_idx), st)
-        spmm_plan_order_rows(self.ptr, _ptr(row_ptr), _ptr(col_idx), st)
+            return spmm_plan_order_rows_auto(self.ptr, a_rp, a_ci, st)
+        spmm_plan_order_rows(self.ptr, a_rp, a_ci, st)
         return True
 
     def __call__(self, alpha, row_ptr, col_idx, values, B, beta, C, stream=None) -> None:
         """C <- alpha * A * B + beta * C with A's structure from the plan."""
         import torch
+        _check_dense(B, C, self.k, self.m, self.n, self.dtype)
+        if values.dtype != self.dtype:
+            raise TypeError("values must have the plan's dtype")
+        d = self.handle.device
+        a_rp, a_ci, a_va, a_b, a_c = (_ptr(x, d) for x in (row_ptr, col_idx, values, B, C))
         st = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
         ldb = B.stride(0) if B.shape[0] > 1 else max(1, self.n)
         ldc = C.stride(0) if C.shape[0] > 1 else max(1, self.n)
         fn = spmm_plan_csr_f32 if values.dtype == torch.float32 else spmm_plan_csr_f64
-        fn(self.ptr, alpha, _ptr(row_ptr), _ptr(col_idx), _ptr(values), _ptr(B), ldb, beta,
-           _ptr(C), ldc, st)
+        fn(self.ptr, alpha, a_rp, a_ci, a_va, a_b, ldb, beta, a_c, ldc, st)
 
     def squared(self, alpha, row_ptr, col_idx, values, B, beta, C, stream=None) -> None:
         """C <- alpha * A (A B) + beta * C with A's structure from the plan (square A)."""
         import torch
+        _check_dense(B, C, self.m, self.m, self.n, self.dtype)
+        if values.dtype != self.dtype:
+            raise TypeError("values must have the plan's dtype")
+        d = self.handle.device
+        a_rp, a_ci, a_va, a_b, a_c = (_ptr(x, d) for x in (row_ptr, col_idx, values, B, C))
         st = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
         ldb = B.stride(0) if B.shape[0] > 1 else max(1, self.n)
         ldc = C.stride(0) if C.shape[0] > 1 else max(1, self.n)
         fn = (spmm_plan_csr_squared_f32 if values.dtype == torch.float32
               else spmm_plan_csr_squared_f64)
-        fn(self.ptr, alpha, _ptr(row_ptr), _ptr(col_idx), _ptr(values), _ptr(B), ldb, beta,
-           _ptr(C), ldc, st)
+        fn(self.ptr, alpha, a_rp, a_ci, a_va, a_b, ldb, beta, a_c, ldc, st)
 
     def close(self) -> None:
         if self.ptr:
@@ -250,6 +302,8 @@ def csr_check(handle: Handle, row_ptr, col_idx, k: int, stream=None) -> int:
     import torch
     m = int(row_ptr.numel()) - 1
     nnz = int(col_idx.numel())
+    d = handle.device
+    a_rp, a_ci = _ptr(row_ptr, d), _ptr(col_idx, d)
     st = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
-    _, mask = spmm_csr_check(handle.ptr, _ptr(row_ptr), _ptr(col_idx), m, k, nnz, st)
+    _, mask = spmm_csr_check(handle.ptr, a_rp, a_ci, m, k, nnz, st)
     return mask
